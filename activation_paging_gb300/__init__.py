@@ -1,0 +1,274 @@
+"""GB300 token movement for a top-k MoE layer with a paged activation stash.
+
+Thin Python binding of ``libap.so`` (C ABI in ``include/ap.h``).  Every step
+runs in the library's CUDA kernels; this module only allocates tensors with
+PyTorch (device memory, pinned host memory, streams) and passes their
+addresses.  There is no CPU fallback: without the built library every call
+raises.
+
+    route_topk        softmax -> top-k -> renormalised weights
+    dispatch_permute  expert-major, capacity-bounded permutation (BF16 / E4M3)
+    Pool              paged stash: push / pop / reset / overflow read-out
+    combine_unpermute top-k weighted un-permute to dense BF16 [T, H]
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import APError, PoolConfig, PoolState, RecordInfo, check
+
+FLAG_POOL_OVERFLOW = 0x1
+FLAG_SPILL_OVERFLOW = 0x2
+FLAG_RECORD_OVERFLOW = 0x4
+FLAG_BAD_COUNT = 0x8
+FLAG_BAD_INDEX = 0x10
+FLAG_CORRUPT = 0x20
+DTYPE_BF16, DTYPE_E4M3 = 0, 1
+
+__all__ = ["route_topk", "dispatch_permute", "dispatch_scratch_bytes", "combine_unpermute", "cast_e4m3", "Pool",
+           "APError", "lib"]
+
+
+def lib():
+    return _lib.load()
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def route_topk(logits: torch.Tensor, k: int, idx: torch.Tensor | None = None, w: torch.Tensor | None = None,
+               stream=None):
+    """idx [T, k] int32 and w [T, k] float32 for float32 logits [T, E]."""
+    _need(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if idx is None:
+        idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if w is None:
+        w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    check(lib().ap_route_topk(_p(logits), T, E, k, _p(idx), _p(w), _stream(stream)), "route_topk")
+    return idx, w
+
+
+def dispatch_scratch_bytes(T: int, k: int, E: int) -> int:
+    n = ctypes.c_int64(0)
+    check(lib().ap_dispatch_scratch_bytes(T, k, E, ctypes.byref(n)), "dispatch_scratch_bytes")
+    return n.value
+
+
+def dispatch_permute(x: torch.Tensor, idx: torch.Tensor, E: int, capacity: int = 0, padded: bool = False,
+                     fp8: bool = False, out: dict | None = None, status: torch.Tensor | None = None, stream=None):
+    """Permute BF16 rows x [T, H] into expert-major rows.
+
+    Returns a dict with xd ([rows, H] bf16, or uint8 codes), xd_scale (E4M3
+    only), counts, live, seg_off ([E] int32), dest ([T, k] int32), src_tok
+    ([rows] int32, -1 where never written) and scratch.  Pass ``out`` (such a
+    dict) to reuse buffers."""
+    _need(x, torch.bfloat16, "x")
+    _need(idx, torch.int32, "idx")
+    T, H = x.shape
+    k = idx.shape[1]
+    dev = x.device
+    rows = E * capacity if padded else T * k
+    o = dict(out) if out is not None else {}
+    if "xd" not in o:
+        o["xd"] = torch.empty((rows, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    if fp8 and "xd_scale" not in o:
+        o["xd_scale"] = torch.empty(rows, dtype=torch.float32, device=dev)
+    for name, shape in (("counts", (E,)), ("live", (E,)), ("seg_off", (E,)), ("dest", (T, k))):
+        if name not in o:
+            o[name] = torch.empty(shape, dtype=torch.int32, device=dev)
+    if "src_tok" not in o:
+        o["src_tok"] = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+    sb = dispatch_scratch_bytes(T, k, E)
+    if "scratch" not in o or o["scratch"].numel() < sb:
+        o["scratch"] = torch.empty(sb, dtype=torch.uint8, device=dev)
+    xd = o["xd"]
+    check(lib().ap_dispatch_permute(_p(x), T, H, _p(idx), k, E, capacity, int(padded),
+                                    DTYPE_E4M3 if fp8 else DTYPE_BF16, _p(xd), _p(o.get("xd_scale")), xd.shape[0],
+                                    _p(o["counts"]), _p(o["live"]), _p(o["seg_off"]), _p(o["dest"]),
+                                    _p(o["src_tok"]), _p(o["scratch"]), o["scratch"].numel(), _p(status),
+                                    _stream(stream)), "dispatch_permute")
+    return o
+
+
+def combine_unpermute(y: torch.Tensor, dest: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
+                      status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out [T, H] bf16 = sum_j w[t, j] * y[dest[t, j]] (FP32 accumulation)."""
+    _need(y, torch.bfloat16, "y")
+    _need(dest, torch.int32, "dest")
+    _need(w, torch.float32, "w")
+    T, k = dest.shape
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    check(lib().ap_combine_unpermute(_p(y), y.shape[0], H, _p(dest), _p(w), T, k, _p(out), _p(status),
+                                     _stream(stream)), "combine_unpermute")
+    return out
+
+
+def cast_e4m3(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _need(x, torch.float32, "x")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    check(lib().ap_cast_e4m3(_p(x), _p(out), x.numel(), _stream(stream)), "cast_e4m3")
+    return out
+
+
+def page_bytes_for(page_tokens: int, row_bytes) -> int:
+    """Smallest page (multiple of 256 bytes) holding page_tokens rows of each plane."""
+    need = page_tokens * row_bytes[0]
+    if len(row_bytes) == 2:
+        need = (need + 15) // 16 * 16 + page_tokens * row_bytes[1]
+    return (need + 255) // 256 * 256
+
+
+class Pool:
+    """Paged activation stash over PyTorch-owned memory.
+
+    The device pool, its metadata and the pinned host spill are torch tensors
+    held by this object; the library keeps only their addresses.  Every push,
+    pop and reset runs on ``self.stream`` (a high-priority stream by
+    default).  Order work on other streams with ``stream.wait_stream`` /
+    ``self.stream.wait_stream``."""
+
+    def __init__(self, page_tokens: int, page_bytes: int, num_pages: int, num_slots: int = 1,
+                 max_records_per_slot: int = 8, max_segments: int = 1024, max_pages_per_record: int | None = None,
+                 spill_pages: int = 0, max_ctas: int = 0, device="cuda", stream: torch.cuda.Stream | None = None,
+                 fill: int | None = None):
+        self.lib = lib()
+        if max_pages_per_record is None:
+            max_pages_per_record = num_pages + spill_pages
+        self.cfg = PoolConfig(page_tokens, num_slots, page_bytes, num_pages, spill_pages, max_records_per_slot,
+                              max_segments, max_pages_per_record, max_ctas, 0)
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        check(self.lib.ap_pool_required_bytes(ctypes.byref(self.cfg), ctypes.byref(a), ctypes.byref(b),
+                                              ctypes.byref(c)), "pool_required_bytes")
+        self.device = torch.device(device)
+        self.pool = torch.empty(a.value, dtype=torch.uint8, device=self.device)
+        self.meta = torch.empty(b.value, dtype=torch.uint8, device=self.device)
+        self.spill = torch.empty(c.value, dtype=torch.uint8, pin_memory=True) if c.value else None
+        if fill is not None:
+            self.pool.fill_(fill)
+            if self.spill is not None:
+                self.spill.fill_(fill)
+            torch.cuda.synchronize(self.device)
+        self.stream = stream if stream is not None else torch.cuda.Stream(device=self.device, priority=-1)
+        self.handle = ctypes.c_void_p()
+        check(self.lib.ap_pool_init(ctypes.byref(self.handle), ctypes.byref(self.cfg), _p(self.pool),
+                                    _p(self.meta), _p(self.spill), self.stream.cuda_stream), "pool_init")
+        self.N, self.SP, self.P = num_pages, spill_pages, page_tokens
+        self.page_bytes = page_bytes
+        self.max_pages = max_pages_per_record
+
+    # -- lifecycle --------------------------------------------------------
+    def close(self):
+        if getattr(self, "handle", None) and self.handle.value:
+            self.lib.ap_pool_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self):
+        check(self.lib.ap_pool_reset(self.handle, self.stream.cuda_stream), "pool_reset")
+
+    @property
+    def max_ctas(self) -> int:
+        v = ctypes.c_int32()
+        check(self.lib.ap_pool_max_ctas(self.handle, ctypes.byref(v)), "pool_max_ctas")
+        return v.value
+
+    # -- data path ----------------------------------------------------------
+    @staticmethod
+    def _planes(planes):
+        rows = planes[0].shape[0]
+        ptrs = (ctypes.c_void_p * 2)()
+        rb = (ctypes.c_int64 * 2)()
+        for i, t in enumerate(planes):
+            if not t.is_contiguous() or t.shape[0] != rows:
+                raise ValueError("planes must be contiguous with the same number of rows")
+            ptrs[i] = t.data_ptr()
+            rb[i] = (t.numel() // rows) * t.element_size() if rows else t[0:0].element_size()
+        return ptrs, rb, rows
+
+    def push(self, slot: int, planes, seg_off: torch.Tensor, live: torch.Tensor) -> int:
+        """Stash the live prefixes of every segment of ``planes`` (list of 1-2 tensors)."""
+        ptrs, rb, rows = self._planes(planes)
+        rid = ctypes.c_uint64()
+        nseg = seg_off.numel()
+        check(self.lib.ap_stash_push(self.handle, slot, len(planes), ptrs, rb, rows, nseg, _p(seg_off), _p(live),
+                                     ctypes.byref(rid), self.stream.cuda_stream), "stash_push")
+        return rid.value
+
+    def pop(self, slot: int, planes) -> int:
+        """Reload the slot's oldest record into ``planes`` (same rows as pushed)."""
+        ptrs, _, rows = self._planes(planes)
+        rid = ctypes.c_uint64()
+        check(self.lib.ap_stash_pop(self.handle, slot, len(planes), ptrs, rows, ctypes.byref(rid),
+                                    self.stream.cuda_stream), "stash_pop")
+        return rid.value
+
+    def queue_len(self, slot: int) -> int:
+        v = ctypes.c_int32()
+        check(self.lib.ap_pool_queue_len(self.handle, slot, ctypes.byref(v)), "pool_queue_len")
+        return v.value
+
+    # -- read-outs (synchronise the paging stream) -------------------------------
+    def overflow(self, wait: bool = True) -> int:
+        f = ctypes.c_uint32()
+        check(self.lib.ap_overflow_query(self.handle, ctypes.byref(f), int(wait)), "overflow_query")
+        return f.value
+
+    def flags_device_ptr(self) -> int:
+        p = ctypes.c_void_p()
+        check(self.lib.ap_pool_flags_device_ptr(self.handle, ctypes.byref(p)), "pool_flags_device_ptr")
+        return p.value
+
+    def state(self) -> dict:
+        s = PoolState()
+        check(self.lib.ap_pool_read_state(self.handle, ctypes.byref(s)), "pool_read_state")
+        return dict(head=s.head, tail=s.tail, spill_head=s.spill_head, spill_tail=s.spill_tail, flags=s.flags,
+                    high_water=s.high_water, spill_high_water=s.spill_high_water)
+
+    def rings(self):
+        import numpy as np
+        ring = np.empty(self.N, np.int32)
+        sring = np.empty(max(self.SP, 1), np.int32)
+        check(self.lib.ap_pool_read_rings(self.handle, ring.ctypes.data, sring.ctypes.data if self.SP else None),
+              "pool_read_rings")
+        return ring, sring[: self.SP]
+
+    def record(self, slot: int, qpos: int = 0) -> dict:
+        import numpy as np
+        info = RecordInfo()
+        check(self.lib.ap_pool_read_record(self.handle, slot, qpos, ctypes.byref(info), None, None, None, 0),
+              "pool_read_record")
+        n = info.npages
+        pt = np.empty(max(n, 1), np.int32)
+        r0 = np.empty(max(n, 1), np.int64)
+        nr = np.empty(max(n, 1), np.int32)
+        check(self.lib.ap_pool_read_record(self.handle, slot, qpos, ctypes.byref(info), pt.ctypes.data,
+                                           r0.ctypes.data, nr.ctypes.data, n), "pool_read_record")
+        return dict(id=info.record_id, npages=n, ndev=info.ndev, nspill=info.nspill, nlost=info.nlost,
+                    nseg=info.nseg, page_table=pt[:n], row0=r0[:n], nrows=nr[:n])

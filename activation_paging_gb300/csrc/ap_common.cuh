@@ -1,0 +1,93 @@
+// Shared device and host helpers of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ap.h"
+
+namespace ap {
+
+constexpr int kWarp = 32;
+
+// ---- host-side error reporting ------------------------------------------------
+void set_error(const char *fmt, ...);
+ap_status fail(ap_status s, const char *fmt, ...);
+ap_status cuda_fail(cudaError_t e, const char *what);
+int sm_count();
+
+#define AP_CHECK_LAUNCH(what)                                   \
+    do {                                                        \
+        cudaError_t e_ = cudaGetLastError();                    \
+        if (e_ != cudaSuccess) return ::ap::cuda_fail(e_, what); \
+    } while (0)
+
+// ---- device helpers ----------------------------------------------------------
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ unsigned lanemask_lt()
+{
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Streaming (evict-first) global loads/stores for data touched once.
+__device__ __forceinline__ int4 ld_stream(const int4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(int4 *p, int4 v) { __stcs(p, v); }
+__device__ __forceinline__ int2 ld_stream(const int2 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(int2 *p, int2 v) { __stcs(p, v); }
+__device__ __forceinline__ int ld_stream(const int *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(int *p, int v) { __stcs(p, v); }
+__device__ __forceinline__ short ld_stream(const short *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(short *p, short v) { __stcs(p, v); }
+__device__ __forceinline__ char ld_stream(const char *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(char *p, char v) { __stcs(p, v); }
+
+// Copy n bytes from src to dst with all threads of the block, vectorised to the
+// widest width both pointers share (16, 8, 4, 2 or 1 bytes), with byte-wise
+// heads and tails.  Eight loads are issued before their stores so each
+// thread keeps 128 bytes in flight.
+template <typename V>
+__device__ __forceinline__ void block_copy_vec(uint8_t *dst, const uint8_t *src, int64_t nvec)
+{
+    const V *s = reinterpret_cast<const V *>(src);
+    V *d = reinterpret_cast<V *>(dst);
+    const int64_t nt = blockDim.x;
+    int64_t i = threadIdx.x;
+    constexpr int U = 8;
+    for (; i + (U - 1) * nt < nvec; i += U * nt) {
+        V r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = ld_stream(s + i + u * nt);
+#pragma unroll
+        for (int u = 0; u < U; ++u) st_stream(d + i + u * nt, r[u]);
+    }
+    for (; i < nvec; i += nt) st_stream(d + i, ld_stream(s + i));
+}
+
+__device__ __forceinline__ void block_copy(uint8_t *dst, const uint8_t *src, int64_t n)
+{
+    if (n <= 0) return;
+    const uintptr_t mis = (reinterpret_cast<uintptr_t>(dst) ^ reinterpret_cast<uintptr_t>(src));
+    int A = 16;
+    while (A > 1 && (mis & (uintptr_t)(A - 1))) A >>= 1;
+    int64_t head = (int64_t)((A - (reinterpret_cast<uintptr_t>(dst) & (uintptr_t)(A - 1))) & (uintptr_t)(A - 1));
+    if (head > n) head = n;
+    for (int64_t i = threadIdx.x; i < head; i += blockDim.x) dst[i] = src[i];
+    dst += head;
+    src += head;
+    n -= head;
+    const int64_t nvec = n / A;
+    switch (A) {
+    case 16: block_copy_vec<int4>(dst, src, nvec); break;
+    case 8: block_copy_vec<int2>(dst, src, nvec); break;
+    case 4: block_copy_vec<int>(dst, src, nvec); break;
+    case 2: block_copy_vec<short>(dst, src, nvec); break;
+    default: block_copy_vec<char>(dst, src, nvec); break;
+    }
+    const int64_t done = nvec * A;
+    for (int64_t i = done + threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+
+} // namespace ap

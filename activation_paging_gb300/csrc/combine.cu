@@ -1,0 +1,137 @@
+// Combine / un-permute: out[t] = bf16(sum_j w[t, j] * y[dest[t, j]]).
+//
+// The dense BF16 [T, H] output of combine with un-permute (OpenPipe/ART pull
+// 971, description and review).  One warp per token; each lane owns VE
+// consecutive columns per step and gathers the k expert rows of its columns,
+// all k loads in flight before the accumulation.  Accumulation is single
+// precision with separately rounded multiply and add, j ascending (no FMA),
+// then one round-to-nearest-even conversion to BF16.
+#include <cuda_bf16.h>
+
+#include "ap_common.cuh"
+
+namespace ap {
+namespace {
+
+template <int VE> struct Vec;
+template <> struct Vec<8> { using T = int4; };
+template <> struct Vec<4> { using T = int2; };
+template <> struct Vec<2> { using T = int; };
+template <> struct Vec<1> { using T = short; };
+
+__device__ __forceinline__ float lo_bf16(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+template <int VE>
+__device__ __forceinline__ void unpack(const typename Vec<VE>::T &v, float *f)
+{
+    if constexpr (VE == 1) {
+        f[0] = __uint_as_float(((uint32_t)(uint16_t)v) << 16);
+    } else {
+        uint32_t u[VE / 2];
+        memcpy(u, &v, sizeof(u));
+#pragma unroll
+        for (int i = 0; i < VE / 2; ++i) {
+            f[2 * i] = lo_bf16(u[i]);
+            f[2 * i + 1] = hi_bf16(u[i]);
+        }
+    }
+}
+
+template <int VE>
+__device__ __forceinline__ typename Vec<VE>::T pack(const float *f)
+{
+    typename Vec<VE>::T v;
+    uint16_t h[VE];
+#pragma unroll
+    for (int i = 0; i < VE; ++i) h[i] = __bfloat16_as_ushort(__float2bfloat16_rn(f[i]));
+    memcpy(&v, h, sizeof(v));
+    return v;
+}
+
+// U column steps are unrolled so that U*k row loads are in flight per lane.
+template <int VE, int U>
+__global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ y, int64_t y_rows, int H,
+                                                 const int32_t *__restrict__ dest, const float *__restrict__ w,
+                                                 int64_t T, int k, uint16_t *__restrict__ out, uint32_t *d_status)
+{
+    using V = typename Vec<VE>::T;
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int nstep = H / VE;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        int32_t my_d = -1;
+        float my_w = 0.f;
+        if (lane < k) {
+            my_d = __ldcs(dest + t * k + lane);
+            my_w = __ldcs(w + t * k + lane);
+            if (my_d >= y_rows) {
+                if (d_status) atomicOr(d_status, AP_FLAG_BAD_INDEX);
+                my_d = -1;
+            }
+        }
+        uint16_t *orow = out + t * H;
+        // warp-uniform loop over column steps
+        for (int s0 = 0; s0 < nstep; s0 += U * kWarp) {
+            float acc[U][VE];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int i = 0; i < VE; ++i) acc[u][i] = 0.f;
+            for (int j = 0; j < k; ++j) {
+                const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+                const float wj = __shfl_sync(0xffffffffu, my_w, j);
+                if (d < 0) continue;
+                const V *yrow = reinterpret_cast<const V *>(y + (int64_t)d * H);
+                V v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int s = s0 + u * kWarp + lane;
+                    if (s < nstep) v[u] = ld_stream(yrow + s);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float f[VE];
+                    unpack<VE>(v[u], f);
+#pragma unroll
+                    for (int i = 0; i < VE; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(wj, f[i]));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int s = s0 + u * kWarp + lane;
+                if (s < nstep) st_stream(reinterpret_cast<V *>(orow) + s, pack<VE>(acc[u]));
+            }
+        }
+    }
+}
+
+} // namespace
+} // namespace ap
+
+extern "C" ap_status ap_combine_unpermute(const void *y, int64_t y_rows, int32_t H, const int32_t *dest, const float *w,
+                                          int64_t T, int32_t k, void *out, uint32_t *d_status, void *stream)
+{
+    using namespace ap;
+    if (T < 0 || H < 1 || k < 1 || k > 32 || y_rows < 0)
+        return fail(AP_EINVAL, "combine_unpermute: bad sizes T=%lld H=%d k=%d", (long long)T, H, k);
+    if (T == 0) return AP_OK;
+    if (!dest || !w || !out || (!y && y_rows > 0)) return fail(AP_EINVAL, "combine_unpermute: NULL pointer");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t want = (T + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    const int grid = (int)(want < cap ? want : cap);
+    const uint16_t *yy = static_cast<const uint16_t *>(y);
+    uint16_t *oo = static_cast<uint16_t *>(out);
+    const uintptr_t al = reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(out);
+    if (H % 8 == 0 && (al & 15) == 0)
+        k_combine<8, 2><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+    else if (H % 4 == 0 && (al & 7) == 0)
+        k_combine<4, 2><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+    else if (H % 2 == 0 && (al & 3) == 0)
+        k_combine<2, 4><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+    else
+        k_combine<1, 4><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+    AP_CHECK_LAUNCH("combine launch");
+    return AP_OK;
+}

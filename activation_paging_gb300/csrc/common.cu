@@ -1,0 +1,60 @@
+// Status strings, per-thread error messages and device queries.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "ap_common.cuh"
+
+namespace ap {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+}
+
+ap_status fail(ap_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+ap_status cuda_fail(cudaError_t e, const char *what)
+{
+    set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+    return AP_ECUDA;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+} // namespace ap
+
+extern "C" const char *ap_status_str(ap_status s)
+{
+    switch (s) {
+    case AP_OK: return "AP_OK";
+    case AP_EINVAL: return "AP_EINVAL";
+    case AP_EEMPTY: return "AP_EEMPTY";
+    case AP_EQFULL: return "AP_EQFULL";
+    case AP_ECUDA: return "AP_ECUDA";
+    case AP_ESTREAM: return "AP_ESTREAM";
+    case AP_ENOTSUP: return "AP_ENOTSUP";
+    default: return "AP_UNKNOWN";
+    }
+}
+
+extern "C" const char *ap_last_error(void) { return ap::g_err; }
+
+extern "C" const char *ap_version(void) { return "0.1.0"; }

@@ -1,0 +1,397 @@
+// Dispatch: expert counts, stable capacity-bounded ranks and the row permute.
+//
+// Expert-major, capacity-shaped dispatch buffers (Megatron-LM pull 7342,
+// "Summary"; torchtitan pull 5541, "AI-Generated Details": the capacity shape
+// that reload restores).  Four launches on the caller's stream:
+//   1. k_count  - per block of kTokPerBlk tokens, a shared-memory histogram of
+//                 expert ids -> blk[b][e];
+//   2. k_scan   - one CTA: exclusive scan of blk over b per expert (block base
+//                 offsets), counts, live = min(count, C), segment offsets;
+//   3. k_rank   - per block: warp-level stable ranks (match_any + popc over
+//                 32 pairs at a time, pairs in t-then-j order) -> dest, src_tok;
+//   4. k_copy_* - one warp per token: the row is read once and written to its
+//                 k destinations with 16-byte vectors (BF16), or quantised
+//                 once to E4M3 with a per-row scale and written k times.
+// The ranks are deterministic: no global atomics decide any order.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "ap_common.cuh"
+
+namespace ap {
+namespace {
+
+constexpr int kTokPerBlk = 256; // tokens per count/rank block
+constexpr int kRankThreads = 256;
+constexpr int kRankWarps = kRankThreads / kWarp;
+
+__global__ void __launch_bounds__(256) k_count(const int32_t *__restrict__ idx, int64_t T, int k, int E,
+                                               int32_t *__restrict__ blk)
+{
+    extern __shared__ int32_t hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
+    int64_t p1 = p0 + (int64_t)kTokPerBlk * k;
+    if (p1 > T * k) p1 = T * k;
+    for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+        const int e = idx[p];
+        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) blk[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One CTA of 1024 threads.  blk[b][e] -> exclusive base over b (in place).
+__global__ void __launch_bounds__(1024) k_scan(int32_t *__restrict__ blk, int nblk, int E, int capacity,
+                                                int padded, int32_t *__restrict__ counts,
+                                                int32_t *__restrict__ live, int32_t *__restrict__ seg_off)
+{
+    __shared__ int32_t s_warp[32];
+    const int e = threadIdx.x;
+    int32_t total = 0;
+    if (e < E) {
+        int b = 0;
+        for (; b + 8 <= nblk; b += 8) {
+            int32_t c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                blk[(int64_t)(b + u) * E + e] = total;
+                total += c[u];
+            }
+        }
+        for (; b < nblk; ++b) {
+            const int32_t c = blk[(int64_t)b * E + e];
+            blk[(int64_t)b * E + e] = total;
+            total += c;
+        }
+        counts[e] = total;
+    }
+    const int32_t l = (e < E) ? ((capacity > 0 && total > capacity) ? capacity : total) : 0;
+    if (e < E) live[e] = l;
+    // exclusive scan of live over experts (compact layout)
+    int32_t x = l;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t v = s_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += y;
+        }
+        s_warp[lane] = v;
+    }
+    __syncthreads();
+    const int32_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
+    if (e < E) seg_off[e] = padded ? e * capacity : incl - l;
+}
+
+// Stable ranks.  The block's pairs are split into kRankWarps contiguous
+// ranges; each warp counts its range, a per-expert scan over warps gives each
+// warp's base, then each warp walks its range 32 pairs at a time in order.
+__global__ void __launch_bounds__(kRankThreads) k_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
+                                                       int capacity, const int32_t *__restrict__ blk_base,
+                                                       const int32_t *__restrict__ seg_off,
+                                                       int32_t *__restrict__ dest, int32_t *__restrict__ src_tok,
+                                                       uint32_t *d_status)
+{
+    extern __shared__ int32_t cnt[]; // [kRankWarps][E]
+    const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
+    for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
+    int64_t p1 = p0 + (int64_t)kTokPerBlk * k;
+    if (p1 > T * k) p1 = T * k;
+    const int64_t per_warp = ((p1 - p0) + kRankWarps - 1) / kRankWarps;
+    const int64_t w0 = p0 + wid * per_warp;
+    const int64_t w1 = (w0 + per_warp < p1) ? w0 + per_warp : p1;
+    int32_t *my = cnt + wid * E;
+    bool bad = false;
+    // phase 1: count per warp
+    for (int64_t p = w0 + lane; p < w1; p += kWarp) {
+        const int e = idx[p];
+        if (e >= 0 && e < E) atomicAdd(&my[e], 1);
+        else bad = true;
+    }
+    __syncthreads();
+    // phase 2: per expert, exclusive scan over warps starting at the block base
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t run = blk_base[(int64_t)blockIdx.x * E + e];
+#pragma unroll
+        for (int w2 = 0; w2 < kRankWarps; ++w2) {
+            const int32_t c = cnt[w2 * E + e];
+            cnt[w2 * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // phase 3: ordered walk, 32 pairs per step
+    for (int64_t pb = w0; pb < w1; pb += kWarp) {
+        const int64_t p = pb + lane;
+        const bool in = p < w1;
+        int e = in ? idx[p] : -1;
+        const bool valid = in && e >= 0 && e < E;
+        if (!valid) e = -1 - (int)(in ? 0 : 1); // -1: bad id, -2: past the end
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (valid) {
+            const int32_t r = my[e] + __popc(peers & lanemask_lt());
+            int32_t d = -1;
+            if (capacity <= 0 || r < capacity) {
+                d = seg_off[e] + r;
+                if (src_tok) src_tok[d] = (int32_t)(p / k);
+            }
+            dest[p] = d;
+        } else if (in) {
+            dest[p] = -1;
+        }
+        __syncwarp();
+        if (valid && (peers & lanemask_lt()) == 0) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    if (bad && d_status) atomicOr(d_status, AP_FLAG_BAD_INDEX);
+}
+
+// ---- BF16 row copy: one warp per token, row read once, written k times ------
+template <typename V>
+__global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x, int64_t T, int64_t rb,
+                                                   const int32_t *__restrict__ dest, int k,
+                                                   uint8_t *__restrict__ xd)
+{
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int64_t nvec = rb / (int64_t)sizeof(V);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        const int32_t my_d = (lane < k) ? __ldcs(dest + t * k + lane) : -1;
+        const V *src = reinterpret_cast<const V *>(x + t * rb);
+        constexpr int U = 4;
+        // warp-uniform loop: every lane reaches the shuffles below
+        for (int64_t base = 0; base < nvec; base += U * kWarp) {
+            V r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = base + u * kWarp + lane;
+                if (v < nvec) r[u] = ld_stream(src + v);
+            }
+            for (int j = 0; j < k; ++j) {
+                const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+                if (d < 0) continue;
+                V *dst = reinterpret_cast<V *>(xd + (int64_t)d * rb);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = base + u * kWarp + lane;
+                    if (v < nvec) dst[v] = r[u];
+                }
+            }
+        }
+    }
+}
+
+// ---- E4M3 quantise + copy: one warp per token -------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ uint8_t to_e4m3(float v)
+{
+    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// VE bf16 elements per lane step: 8 (16-byte loads, 8-byte stores), 4, 2 or 1.
+template <int VE>
+__global__ void __launch_bounds__(256) k_copy_rows_e4m3(const uint16_t *__restrict__ x, int64_t T, int H,
+                                                        const int32_t *__restrict__ dest, int k,
+                                                        uint8_t *__restrict__ xd, float *__restrict__ xd_scale)
+{
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int nstep = H / VE;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        const int32_t my_d = (lane < k) ? __ldcs(dest + t * k + lane) : -1;
+        const uint16_t *row = x + t * H;
+        // pass 1: amax
+        float amax = 0.f;
+        for (int s = lane; s < nstep; s += kWarp) {
+            uint16_t e[VE];
+            if constexpr (VE == 8) {
+                const int4 v = *reinterpret_cast<const int4 *>(row + s * 8);
+                memcpy(e, &v, 16);
+            } else if constexpr (VE == 4) {
+                const int2 v = *reinterpret_cast<const int2 *>(row + s * 4);
+                memcpy(e, &v, 8);
+            } else if constexpr (VE == 2) {
+                const int v = *reinterpret_cast<const int *>(row + s * 2);
+                memcpy(e, &v, 4);
+            } else {
+                e[0] = row[s];
+            }
+#pragma unroll
+            for (int i = 0; i < VE; ++i) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(e[i])));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+        const float inv = (amax == 0.f) ? 1.f : __fdiv_rn(448.f, amax);
+        if (lane < k && my_d >= 0) xd_scale[my_d] = scale;
+        // pass 2: quantise once, store to every destination (warp-uniform loop)
+        for (int s0 = 0; s0 < nstep; s0 += kWarp) {
+            const int s = s0 + lane;
+            const bool on = s < nstep;
+            uint16_t e[VE];
+#pragma unroll
+            for (int i = 0; i < VE; ++i) e[i] = 0;
+            if (on) {
+            if constexpr (VE == 8) {
+                const int4 v = *reinterpret_cast<const int4 *>(row + s * 8);
+                memcpy(e, &v, 16);
+            } else if constexpr (VE == 4) {
+                const int2 v = *reinterpret_cast<const int2 *>(row + s * 4);
+                memcpy(e, &v, 8);
+            } else if constexpr (VE == 2) {
+                const int v = *reinterpret_cast<const int *>(row + s * 2);
+                memcpy(e, &v, 4);
+            } else {
+                e[0] = row[s];
+            }
+            }
+            uint8_t q[VE];
+#pragma unroll
+            for (int i = 0; i < VE; ++i) q[i] = to_e4m3(__fmul_rn(bf16_bits_to_f32(e[i]), inv));
+            for (int j = 0; j < k; ++j) {
+                const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+                if (d < 0 || !on) continue;
+                uint8_t *dst = xd + (int64_t)d * H + (int64_t)s * VE;
+                if constexpr (VE == 8) {
+                    int2 o;
+                    memcpy(&o, q, 8);
+                    *reinterpret_cast<int2 *>(dst) = o;
+                } else if constexpr (VE == 4) {
+                    int o;
+                    memcpy(&o, q, 4);
+                    *reinterpret_cast<int *>(dst) = o;
+                } else if constexpr (VE == 2) {
+                    short o;
+                    memcpy(&o, q, 2);
+                    *reinterpret_cast<short *>(dst) = o;
+                } else {
+                    dst[0] = q[0];
+                }
+            }
+        }
+    }
+}
+
+__global__ void k_cast_e4m3(const float *__restrict__ in, uint8_t *__restrict__ out, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = to_e4m3(in[i]);
+}
+
+int64_t nblocks(int64_t T) { return (T + kTokPerBlk - 1) / kTokPerBlk; }
+
+int copy_grid(int64_t T)
+{
+    const int64_t want = (T + 7) / 8; // 8 warps (tokens) per block
+    const int64_t cap = (int64_t)sm_count() * 8;
+    return (int)(want < cap ? want : cap);
+}
+
+} // namespace
+} // namespace ap
+
+extern "C" ap_status ap_dispatch_scratch_bytes(int64_t T, int32_t k, int32_t E, int64_t *bytes)
+{
+    using namespace ap;
+    if (!bytes || T < 0 || k < 1 || E < 1) return fail(AP_EINVAL, "dispatch_scratch_bytes: bad arguments");
+    *bytes = (nblocks(T) * E * (int64_t)sizeof(int32_t) + 255) / 256 * 256;
+    if (*bytes == 0) *bytes = 256;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, const int32_t *idx, int32_t k,
+                                         int32_t E, int32_t capacity, int32_t padded, int32_t out_dtype, void *xd,
+                                         float *xd_scale, int64_t xd_rows, int32_t *counts, int32_t *live,
+                                         int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
+                                         int64_t scratch_bytes, uint32_t *d_status, void *stream)
+{
+    using namespace ap;
+    if (T < 0 || H < 1 || k < 1 || k > 32 || E < 1 || E > 1024 || T * (int64_t)k >= (int64_t(1) << 31))
+        return fail(AP_EINVAL, "dispatch_permute: bad sizes T=%lld H=%d k=%d E=%d", (long long)T, H, k, E);
+    if (padded && capacity <= 0) return fail(AP_EINVAL, "dispatch_permute: padded layout needs capacity > 0");
+    if (out_dtype != AP_DTYPE_BF16 && out_dtype != AP_DTYPE_E4M3)
+        return fail(AP_EINVAL, "dispatch_permute: unknown out_dtype %d", out_dtype);
+    const int64_t need_rows = padded ? (int64_t)E * capacity : T * (int64_t)k;
+    if (xd_rows < need_rows)
+        return fail(AP_EINVAL, "dispatch_permute: xd_rows %lld < %lld", (long long)xd_rows, (long long)need_rows);
+    int64_t need_scratch = 0;
+    ap_dispatch_scratch_bytes(T, k, E, &need_scratch);
+    if (scratch_bytes < need_scratch)
+        return fail(AP_EINVAL, "dispatch_permute: scratch %lld < %lld bytes", (long long)scratch_bytes,
+                    (long long)need_scratch);
+    if (!counts || !live || !seg_off || !scratch || (T > 0 && (!x || !idx || !dest || !xd)))
+        return fail(AP_EINVAL, "dispatch_permute: NULL pointer");
+    if (out_dtype == AP_DTYPE_E4M3 && T > 0 && !xd_scale)
+        return fail(AP_EINVAL, "dispatch_permute: E4M3 needs xd_scale");
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t *blk = static_cast<int32_t *>(scratch);
+    const int64_t nb = nblocks(T);
+    if (nb > 0) {
+        k_count<<<(unsigned)nb, 256, E * sizeof(int32_t), st>>>(idx, T, k, E, blk);
+        AP_CHECK_LAUNCH("dispatch count launch");
+    }
+    k_scan<<<1, 1024, 0, st>>>(blk, (int)nb, E, capacity, padded, counts, live, seg_off);
+    AP_CHECK_LAUNCH("dispatch scan launch");
+    if (T == 0) return AP_OK;
+    const size_t rank_smem = (size_t)kRankWarps * E * sizeof(int32_t);
+    k_rank<<<(unsigned)nb, kRankThreads, rank_smem, st>>>(idx, T, k, E, capacity, blk, seg_off, dest, src_tok,
+                                                         d_status);
+    AP_CHECK_LAUNCH("dispatch rank launch");
+    const int grid = copy_grid(T);
+    if (out_dtype == AP_DTYPE_BF16) {
+        const int64_t rb = (int64_t)H * 2;
+        const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xd) | (uintptr_t)rb;
+        const uint8_t *xs = static_cast<const uint8_t *>(x);
+        uint8_t *xo = static_cast<uint8_t *>(xd);
+        if ((al & 15) == 0)
+            k_copy_rows<int4><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+        else if ((al & 7) == 0)
+            k_copy_rows<int2><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+        else if ((al & 3) == 0)
+            k_copy_rows<int><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+        else
+            k_copy_rows<short><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+    } else {
+        const uint16_t *xs = static_cast<const uint16_t *>(x);
+        uint8_t *xo = static_cast<uint8_t *>(xd);
+        const uintptr_t ax = reinterpret_cast<uintptr_t>(x), ao = reinterpret_cast<uintptr_t>(xd);
+        if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0)
+            k_copy_rows_e4m3<8><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+        else if (H % 4 == 0 && (ax & 7) == 0 && (ao & 3) == 0)
+            k_copy_rows_e4m3<4><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+        else if (H % 2 == 0 && (ax & 3) == 0 && (ao & 1) == 0)
+            k_copy_rows_e4m3<2><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+        else
+            k_copy_rows_e4m3<1><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+    }
+    AP_CHECK_LAUNCH("dispatch copy launch");
+    return AP_OK;
+}
+
+extern "C" ap_status ap_cast_e4m3(const float *in, uint8_t *out, int64_t n, void *stream)
+{
+    using namespace ap;
+    if (n < 0) return fail(AP_EINVAL, "cast_e4m3: n < 0");
+    if (n == 0) return AP_OK;
+    if (!in || !out) return fail(AP_EINVAL, "cast_e4m3: NULL pointer");
+    const int64_t want = (n + 255) / 256;
+    const int grid = (int)(want < (int64_t)sm_count() * 8 ? want : (int64_t)sm_count() * 8);
+    k_cast_e4m3<<<grid, 256, 0, (cudaStream_t)stream>>>(in, out, n);
+    AP_CHECK_LAUNCH("cast_e4m3 launch");
+    return AP_OK;
+}

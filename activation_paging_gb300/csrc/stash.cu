@@ -1,0 +1,731 @@
+// Paged activation stash: fixed page pool, free rings, spill, FIFO records.
+//
+// torchtitan pull 5541, "AI-Generated Details": live counts bound to the
+// source that pushes them; one high-priority paging stream serialises every
+// free-list change; records stay FIFO per slot; the copy loops run over
+// page-aligned multi-token tiles, each tile resolving its page once, and only
+// the first tile of a page records it (push) or recycles it (pop); live-prefix
+// and page-tail masks keep the payload bytes exact with 64-bit addressing;
+// host spill and a sticky overflow flag; a grid bound (default 2048) that
+// changes neither the capacity nor the rows copied.  "Verification": wrapped
+// allocation and recycling, device counts that change under CUDA-graph replay,
+// BF16/FP8 payloads, host spill and overflow.
+//
+// A push is two launches on the paging stream:
+//   k_push_plan (1 CTA): snapshot live/seg_off, page ordinals by a prefix sum of
+//     ceil(live/P), one (first row, rows) descriptor per page, and the
+//     allocation: pages [0, ndev) come from the device ring at the head
+//     snapshot, the next nspill from the spill ring, the rest are lost; head
+//     counters advance and sticky flags are set here, once.
+//   k_push_copy (grid-stride over tiles): tile -> page ordinal; the page id is
+//     read from the ring at head0 + ordinal; tile 0 of the page writes the
+//     page-table entry; the tile's rows are copied as one contiguous range per
+//     plane.
+// A pop is k_pop_plan (1 thread: tail snapshot, tail advance) and k_pop_copy
+// (tile 0 of a page writes its id back into the ring at tail0 + ordinal).
+// Nothing here waits on the device: there are no spin loops.
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "ap_common.cuh"
+
+namespace ap {
+namespace {
+
+struct RecHdr {
+    int32_t nseg;
+    int32_t pad0;
+    int64_t npages, ndev, nspill, nlost;
+    uint64_t head0, spill_head0, tail0, spill_tail0;
+    int64_t pad1[7];
+};
+static_assert(sizeof(RecHdr) == 128, "record header layout");
+static_assert(sizeof(ap_pool_state) == 64, "state layout");
+
+struct PageDesc {
+    int64_t row0; // first row in the source / destination planes
+    int32_t nrows;
+    int32_t pad;
+};
+
+struct RecLayout {
+    int64_t seg_off, live, pg_base, desc, page_table, stride;
+};
+
+__host__ __device__ inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+RecLayout record_layout(const ap_pool_config &c)
+{
+    RecLayout L;
+    int64_t o = sizeof(RecHdr);
+    L.seg_off = o;
+    o = align_up(o + 4 * (int64_t)c.max_segments, 16);
+    L.live = o;
+    o = align_up(o + 4 * (int64_t)c.max_segments, 16);
+    L.pg_base = o;
+    o = align_up(o + 8 * ((int64_t)c.max_segments + 1), 16);
+    L.desc = o;
+    o = align_up(o + (int64_t)sizeof(PageDesc) * c.max_pages_per_record, 16);
+    L.page_table = o;
+    o = align_up(o + 4 * c.max_pages_per_record, 256);
+    L.stride = o;
+    return L;
+}
+
+struct MetaLayout {
+    int64_t ring, spill_ring, records, total;
+    RecLayout rec;
+};
+
+MetaLayout meta_layout(const ap_pool_config &c)
+{
+    MetaLayout M;
+    M.ring = 256;
+    M.spill_ring = align_up(M.ring + 4 * c.num_pages, 256);
+    M.records = align_up(M.spill_ring + 4 * c.spill_pages, 256);
+    M.rec = record_layout(c);
+    M.total = M.records + M.rec.stride * (int64_t)c.num_slots * c.max_records_per_slot;
+    return M;
+}
+
+// Pointers to one record inside the metadata buffer.
+struct RecPtr {
+    RecHdr *hdr;
+    int32_t *seg_off, *live;
+    int64_t *pg_base;
+    PageDesc *desc;
+    int32_t *page_table;
+};
+
+RecPtr rec_ptr(uint8_t *meta, const MetaLayout &M, int64_t index)
+{
+    uint8_t *b = meta + M.records + M.rec.stride * index;
+    RecPtr r;
+    r.hdr = reinterpret_cast<RecHdr *>(b);
+    r.seg_off = reinterpret_cast<int32_t *>(b + M.rec.seg_off);
+    r.live = reinterpret_cast<int32_t *>(b + M.rec.live);
+    r.pg_base = reinterpret_cast<int64_t *>(b + M.rec.pg_base);
+    r.desc = reinterpret_cast<PageDesc *>(b + M.rec.desc);
+    r.page_table = reinterpret_cast<int32_t *>(b + M.rec.page_table);
+    return r;
+}
+
+// ---- kernels -------------------------------------------------------------------
+__global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int32_t *spill_ring, int64_t SP)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride) ring[i] = (int32_t)i;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < SP; i += stride) spill_ring[i] = (int32_t)i;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        st->head = 0;
+        st->tail = (uint64_t)N;
+        st->spill_head = 0;
+        st->spill_tail = (uint64_t)SP;
+        st->flags = 0;
+        st->pad0 = 0;
+        st->high_water = 0;
+        st->spill_high_water = 0;
+        st->pad1 = 0;
+    }
+}
+
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, RecPtr rec, int nseg,
+                                                             const int32_t *__restrict__ d_seg_off,
+                                                             const int32_t *__restrict__ d_live, int64_t src_rows,
+                                                             int P, int64_t max_pages, int64_t N, int64_t SP)
+{
+    __shared__ int64_t s_warp[kPlanThreads / kWarp];
+    __shared__ int64_t s_carry;
+    __shared__ uint32_t s_flags;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) {
+        s_carry = 0;
+        s_flags = 0;
+    }
+    __syncthreads();
+    // 1. snapshot + validation + prefix sum of pages per segment
+    for (int base = 0; base < nseg; base += kPlanThreads) {
+        const int s = base + tid;
+        int64_t n = 0;
+        if (s < nseg) {
+            const int32_t o = d_seg_off[s];
+            int32_t l = d_live[s];
+            if (l < 0 || o < 0 || (int64_t)o + (int64_t)l > src_rows) {
+                atomicOr(&s_flags, AP_FLAG_BAD_COUNT);
+                l = 0;
+            }
+            rec.seg_off[s] = o;
+            rec.live[s] = l;
+            n = ((int64_t)l + P - 1) / P;
+        }
+        int64_t x = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) s_warp[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int64_t v = s_warp[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += y;
+            }
+            s_warp[lane] = v;
+        }
+        __syncthreads();
+        const int64_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
+        if (s < nseg) rec.pg_base[s] = s_carry + incl - n;
+        __syncthreads();
+        if (tid == kPlanThreads - 1) s_carry += incl;
+        __syncthreads();
+    }
+    const int64_t total = s_carry;
+    if (tid == 0) rec.pg_base[nseg] = total;
+    const int64_t kept = total < max_pages ? total : max_pages;
+    __syncthreads();
+    // 2. one descriptor per page: segment by binary search over pg_base
+    for (int64_t ord = tid; ord < kept; ord += kPlanThreads) {
+        int lo = 0, hi = nseg - 1; // largest s with pg_base[s] <= ord
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (rec.pg_base[mid] <= ord) lo = mid;
+            else hi = mid - 1;
+        }
+        const int64_t pg = ord - rec.pg_base[lo];
+        const int64_t r0 = pg * P;
+        int64_t nr = (int64_t)rec.live[lo] - r0;
+        if (nr > P) nr = P;
+        PageDesc d;
+        d.row0 = (int64_t)rec.seg_off[lo] + r0;
+        d.nrows = (int32_t)nr;
+        d.pad = 0;
+        rec.desc[ord] = d;
+    }
+    // 3. allocation: device pages first, then spill pages, then lost
+    if (tid == 0) {
+        uint32_t f = s_flags;
+        if (total > max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
+        const uint64_t head = st->head, tail = st->tail;
+        const uint64_t sh = st->spill_head, stl = st->spill_tail;
+        const int64_t avail = (int64_t)(tail - head);
+        const int64_t savail = (int64_t)(stl - sh);
+        const int64_t ndev = kept < avail ? kept : avail;
+        int64_t nspill = kept - ndev;
+        if (nspill > savail) nspill = savail;
+        const int64_t nlost = kept - ndev - nspill;
+        if (kept > avail) f |= AP_FLAG_POOL_OVERFLOW;
+        if (nlost > 0) f |= AP_FLAG_SPILL_OVERFLOW;
+        rec.hdr->nseg = nseg;
+        rec.hdr->npages = kept;
+        rec.hdr->ndev = ndev;
+        rec.hdr->nspill = nspill;
+        rec.hdr->nlost = nlost;
+        rec.hdr->head0 = head;
+        rec.hdr->spill_head0 = sh;
+        st->head = head + (uint64_t)ndev;
+        st->spill_head = sh + (uint64_t)nspill;
+        const int64_t in_use = N - (int64_t)(tail - (head + (uint64_t)ndev));
+        if (in_use > st->high_water) st->high_water = in_use;
+        const int64_t s_use = SP - (int64_t)(stl - (sh + (uint64_t)nspill));
+        if (s_use > st->spill_high_water) st->spill_high_water = s_use;
+        st->flags |= f;
+    }
+}
+
+struct Planes {
+    uint8_t *p[2];
+    int64_t rb[2];
+    int64_t page_off[2];
+    int n;
+};
+
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st, RecPtr rec,
+                                                             const int32_t *__restrict__ ring,
+                                                             const int32_t *__restrict__ spill_ring, int64_t N,
+                                                             int64_t SP, uint8_t *pool, uint8_t *spill,
+                                                             int64_t page_bytes, Planes src, int rows_per_tile,
+                                                             int tiles_per_page)
+{
+    const int64_t npages = rec.hdr->npages;
+    const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
+    const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
+    const int64_t tiles = npages * tiles_per_page;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t ord = tile / tiles_per_page;
+        const int sub = (int)(tile - ord * tiles_per_page);
+        const PageDesc d = rec.desc[ord];
+        const int64_t r0 = (int64_t)sub * rows_per_tile;
+        if (r0 >= d.nrows) continue;
+        const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
+        // resolve this tile's page once
+        int64_t id = -1;
+        if (ord < ndev) id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
+        else if (ord < ndev + nspill) id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
+        const bool ok = (ord < ndev) ? (id >= 0 && id < N) : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+            id = -1;
+        }
+        if (sub == 0 && threadIdx.x == 0) rec.page_table[ord] = (int32_t)id; // first tile records the page
+        if (id < 0) continue;
+        uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+            if (p < src.n)
+                block_copy(page + src.page_off[p] + r0 * src.rb[p], src.p[p] + (d.row0 + r0) * src.rb[p],
+                           nr * src.rb[p]);
+    }
+}
+
+__global__ void k_pop_plan(ap_pool_state *st, RecHdr *hdr)
+{
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->tail0 = st->tail;
+        hdr->spill_tail0 = st->spill_tail;
+        st->tail = st->tail + (uint64_t)hdr->ndev;
+        st->spill_tail = st->spill_tail + (uint64_t)hdr->nspill;
+    }
+}
+
+__global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st, RecPtr rec, int32_t *ring,
+                                                            int32_t *spill_ring, int64_t N, int64_t SP,
+                                                            const uint8_t *pool, const uint8_t *spill,
+                                                            int64_t page_bytes, Planes dst, int64_t dst_rows,
+                                                            int rows_per_tile, int tiles_per_page)
+{
+    const int64_t npages = rec.hdr->npages;
+    const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
+    const uint64_t tail0 = rec.hdr->tail0, stail0 = rec.hdr->spill_tail0;
+    const int64_t tiles = npages * tiles_per_page;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t ord = tile / tiles_per_page;
+        const int sub = (int)(tile - ord * tiles_per_page);
+        const PageDesc d = rec.desc[ord];
+        const int64_t r0 = (int64_t)sub * rows_per_tile;
+        if (r0 >= d.nrows) continue;
+        const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
+        int64_t id = rec.page_table[ord];
+        const bool ok = (ord < ndev) ? (id >= 0 && id < N) : (ord < ndev + nspill) ? (id >= N && id < N + SP) : (id == -1);
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+            continue;
+        }
+        if (sub == 0 && threadIdx.x == 0) { // first tile recycles the page
+            if (ord < ndev) ring[(tail0 + (uint64_t)ord) % (uint64_t)N] = (int32_t)id;
+            else if (id >= 0) spill_ring[(stail0 + (uint64_t)(ord - ndev)) % (uint64_t)SP] = (int32_t)(id - N);
+        }
+        if (id < 0) continue;
+        if (d.row0 + d.nrows > dst_rows) {
+            if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
+            continue;
+        }
+        const uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+            if (p < dst.n)
+                block_copy(dst.p[p] + (d.row0 + r0) * dst.rb[p], page + dst.page_off[p] + r0 * dst.rb[p],
+                           nr * dst.rb[p]);
+    }
+}
+
+} // namespace
+} // namespace ap
+
+// ---- host runtime ------------------------------------------------------------------
+namespace {
+
+struct HostRec {
+    uint64_t id;
+    int64_t index; // record index in the metadata buffer
+    int32_t nplanes;
+    int64_t rb[2];
+    int32_t rows_per_tile, tiles_per_page;
+    int64_t bound_pages; // upper bound of the record's pages (grid sizing)
+};
+
+} // namespace
+
+struct ap_pool {
+    ap_pool_config cfg;
+    uint8_t *dev_pool = nullptr;
+    uint8_t *dev_meta = nullptr;
+    uint8_t *host_spill = nullptr;
+    uint8_t *spill_dev = nullptr;
+    cudaStream_t stream = nullptr;
+    ap::MetaLayout M;
+    int32_t max_ctas = 2048;
+    HostRec *q = nullptr; // [S][R]
+    int32_t *q_head = nullptr, *q_count = nullptr;
+    uint64_t next_id = 1;
+    void *pinned = nullptr; // small pinned host buffer for read-outs
+    uint32_t last_flags = 0;
+};
+
+namespace {
+
+using ap::fail;
+
+ap_status check_config(const ap_pool_config *c)
+{
+    if (!c) return fail(AP_EINVAL, "pool config is NULL");
+    if (c->page_tokens < 1) return fail(AP_EINVAL, "page_tokens must be >= 1");
+    if (c->page_bytes < 16 || c->page_bytes % 16) return fail(AP_EINVAL, "page_bytes must be a positive multiple of 16");
+    if (c->num_pages < 1 || c->spill_pages < 0 || c->num_pages + c->spill_pages >= (int64_t(1) << 31))
+        return fail(AP_EINVAL, "num_pages + spill_pages must lie in [1, 2^31)");
+    if (c->num_slots < 1 || c->max_records_per_slot < 1) return fail(AP_EINVAL, "num_slots and max_records_per_slot must be >= 1");
+    if (c->max_segments < 1 || c->max_segments > (1 << 20)) return fail(AP_EINVAL, "max_segments must lie in [1, 2^20]");
+    if (c->max_pages_per_record < 1 || c->max_pages_per_record >= (int64_t(1) << 31))
+        return fail(AP_EINVAL, "max_pages_per_record must lie in [1, 2^31)");
+    if (c->max_ctas < 0) return fail(AP_EINVAL, "max_ctas must be >= 0");
+    if (c->reserved != 0) return fail(AP_EINVAL, "reserved must be 0");
+    return AP_OK;
+}
+
+int resolve_max_ctas(int32_t cfg_value)
+{
+    if (cfg_value > 0) return cfg_value;
+    const char *env = getenv("AP_STASH_MAX_CTAS");
+    if (env && *env) {
+        char *end = nullptr;
+        const long v = strtol(env, &end, 10);
+        if (end && *end == '\0' && v >= 1 && v <= (1L << 30)) return (int)v;
+    }
+    return 2048;
+}
+
+bool plane_fit(const ap_pool *p, int32_t nplanes, const int64_t *rb, int64_t *page_off)
+{
+    if (nplanes < 1 || nplanes > 2) return false;
+    const int64_t P = p->cfg.page_tokens;
+    if (rb[0] < 1 || (nplanes == 2 && rb[1] < 1)) return false;
+    page_off[0] = 0;
+    int64_t need = P * rb[0];
+    page_off[1] = 0;
+    if (nplanes == 2) {
+        page_off[1] = ap::align_up(P * rb[0], 16);
+        need = page_off[1] + P * rb[1];
+    }
+    return need <= p->cfg.page_bytes;
+}
+
+ap_status sync_read(ap_pool *p, void *host, const void *dev, size_t bytes)
+{
+    cudaError_t e = cudaMemcpyAsync(host, dev, bytes, cudaMemcpyDeviceToHost, p->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+    if (e != cudaSuccess) return ap::cuda_fail(e, "pool read-out");
+    return AP_OK;
+}
+
+} // namespace
+
+extern "C" ap_status ap_pool_required_bytes(const ap_pool_config *cfg, int64_t *dev_pool_bytes,
+                                            int64_t *dev_meta_bytes, int64_t *host_spill_bytes)
+{
+    ap_status s = check_config(cfg);
+    if (s != AP_OK) return s;
+    const ap::MetaLayout M = ap::meta_layout(*cfg);
+    if (dev_pool_bytes) *dev_pool_bytes = cfg->num_pages * cfg->page_bytes;
+    if (dev_meta_bytes) *dev_meta_bytes = M.total;
+    if (host_spill_bytes) *host_spill_bytes = cfg->spill_pages * cfg->page_bytes;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_init(ap_pool **out, const ap_pool_config *cfg, void *dev_pool, void *dev_meta,
+                                  void *host_spill, void *paging_stream)
+{
+    if (!out) return fail(AP_EINVAL, "pool_init: out is NULL");
+    *out = nullptr;
+    ap_status s = check_config(cfg);
+    if (s != AP_OK) return s;
+    if (!dev_pool || !dev_meta) return fail(AP_EINVAL, "pool_init: NULL pool or metadata buffer");
+    if ((reinterpret_cast<uintptr_t>(dev_pool) | reinterpret_cast<uintptr_t>(dev_meta)) & 255)
+        return fail(AP_EINVAL, "pool_init: pool and metadata buffers must be 256-byte aligned");
+    if ((cfg->spill_pages > 0) != (host_spill != nullptr))
+        return fail(AP_EINVAL, "pool_init: host_spill must be given iff spill_pages > 0");
+    uint8_t *spill_dev = nullptr;
+    if (host_spill) {
+        // pinned host memory is mapped into the device address space; its
+        // attributes give the device-side address (also for interior pointers)
+        cudaPointerAttributes attr;
+        cudaError_t e = cudaPointerGetAttributes(&attr, host_spill);
+        if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) {
+            (void)cudaGetLastError();
+            return fail(AP_EINVAL, "pool_init: host_spill is not mapped pinned host memory (%s)",
+                        e != cudaSuccess ? cudaGetErrorString(e) : "not page-locked");
+        }
+        spill_dev = static_cast<uint8_t *>(attr.devicePointer);
+    }
+    ap_pool *p = new (std::nothrow) ap_pool();
+    if (!p) return fail(AP_EINVAL, "pool_init: out of host memory");
+    p->cfg = *cfg;
+    p->dev_pool = static_cast<uint8_t *>(dev_pool);
+    p->dev_meta = static_cast<uint8_t *>(dev_meta);
+    p->host_spill = static_cast<uint8_t *>(host_spill);
+    p->spill_dev = spill_dev;
+    p->stream = static_cast<cudaStream_t>(paging_stream);
+    p->M = ap::meta_layout(*cfg);
+    p->max_ctas = resolve_max_ctas(cfg->max_ctas);
+    const int64_t nrec = (int64_t)cfg->num_slots * cfg->max_records_per_slot;
+    p->q = new (std::nothrow) HostRec[nrec];
+    p->q_head = new (std::nothrow) int32_t[cfg->num_slots]();
+    p->q_count = new (std::nothrow) int32_t[cfg->num_slots]();
+    if (!p->q || !p->q_head || !p->q_count) {
+        ap_pool_destroy(p);
+        return fail(AP_EINVAL, "pool_init: out of host memory");
+    }
+    cudaError_t e = cudaMallocHost(&p->pinned, 256);
+    if (e != cudaSuccess) {
+        p->pinned = nullptr;
+        ap_pool_destroy(p);
+        return ap::cuda_fail(e, "pool_init: pinned read-out buffer");
+    }
+    s = ap_pool_reset(p, paging_stream);
+    if (s != AP_OK) {
+        ap_pool_destroy(p);
+        return s;
+    }
+    *out = p;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_reset(ap_pool *p, void *stream)
+{
+    if (!p) return fail(AP_EINVAL, "pool_reset: NULL pool");
+    if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "pool_reset: not the paging stream");
+    for (int32_t s = 0; s < p->cfg.num_slots; ++s) {
+        p->q_head[s] = 0;
+        p->q_count[s] = 0;
+    }
+    p->last_flags = 0;
+    const int64_t n = p->cfg.num_pages > p->cfg.spill_pages ? p->cfg.num_pages : p->cfg.spill_pages;
+    int64_t grid = (n + 255) / 256;
+    if (grid > 1024) grid = 1024;
+    if (grid < 1) grid = 1;
+    ap::k_reset<<<(unsigned)grid, 256, 0, p->stream>>>(reinterpret_cast<ap_pool_state *>(p->dev_meta),
+                                                      reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),
+                                                      p->cfg.num_pages,
+                                                      reinterpret_cast<int32_t *>(p->dev_meta + p->M.spill_ring),
+                                                      p->cfg.spill_pages);
+    AP_CHECK_LAUNCH("pool reset launch");
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_destroy(ap_pool *p)
+{
+    if (!p) return AP_OK;
+    if (p->pinned) cudaFreeHost(p->pinned);
+    delete[] p->q;
+    delete[] p->q_head;
+    delete[] p->q_count;
+    delete p;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_max_ctas(const ap_pool *p, int32_t *max_ctas)
+{
+    if (!p || !max_ctas) return fail(AP_EINVAL, "pool_max_ctas: NULL argument");
+    *max_ctas = p->max_ctas;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, const void *const *src_planes,
+                                   const int64_t *row_bytes, int64_t src_rows, int32_t nseg,
+                                   const int32_t *d_seg_off, const int32_t *d_live, uint64_t *record_id,
+                                   void *stream)
+{
+    if (!p) return fail(AP_EINVAL, "stash_push: NULL pool");
+    if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "stash_push: not the paging stream");
+    if (slot < 0 || slot >= p->cfg.num_slots) return fail(AP_EINVAL, "stash_push: slot %d out of range", slot);
+    if (!src_planes || !row_bytes) return fail(AP_EINVAL, "stash_push: NULL plane arrays");
+    if (nseg < 0 || nseg > p->cfg.max_segments)
+        return fail(AP_EINVAL, "stash_push: nseg %d outside [0, %d]", nseg, p->cfg.max_segments);
+    if (src_rows < 0) return fail(AP_EINVAL, "stash_push: src_rows < 0");
+    int64_t rb[2] = {row_bytes[0], nplanes == 2 ? row_bytes[1] : 0};
+    int64_t page_off[2];
+    if (!plane_fit(p, nplanes, rb, page_off))
+        return fail(AP_EINVAL, "stash_push: %d plane(s) of the given row bytes do not fit a page", nplanes);
+    for (int i = 0; i < nplanes; ++i)
+        if (!src_planes[i] && src_rows > 0) return fail(AP_EINVAL, "stash_push: NULL source plane");
+    if (nseg > 0 && (!d_seg_off || !d_live)) return fail(AP_EINVAL, "stash_push: NULL seg_off/live");
+    if (p->q_count[slot] >= p->cfg.max_records_per_slot) return fail(AP_EQFULL, "stash_push: slot %d queue full", slot);
+
+    const int32_t pos = (p->q_head[slot] + p->q_count[slot]) % p->cfg.max_records_per_slot;
+    const int64_t index = (int64_t)slot * p->cfg.max_records_per_slot + pos;
+    HostRec &h = p->q[index];
+    h.id = p->next_id;
+    h.index = index;
+    h.nplanes = nplanes;
+    h.rb[0] = rb[0];
+    h.rb[1] = rb[1];
+    const int64_t P = p->cfg.page_tokens;
+    int64_t rpt = 32768 / rb[0];
+    if (rpt < 1) rpt = 1;
+    if (rpt > P) rpt = P;
+    h.rows_per_tile = (int32_t)rpt;
+    h.tiles_per_page = (int32_t)((P + rpt - 1) / rpt);
+    int64_t bound = nseg + (src_rows + P - 1) / P;
+    if (bound > p->cfg.max_pages_per_record) bound = p->cfg.max_pages_per_record;
+    h.bound_pages = bound;
+
+    ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
+    ap_pool_state *st = reinterpret_cast<ap_pool_state *>(p->dev_meta);
+    ap::k_push_plan<<<1, ap::kPlanThreads, 0, p->stream>>>(st, rec, nseg, d_seg_off, d_live, src_rows,
+                                                           p->cfg.page_tokens, p->cfg.max_pages_per_record,
+                                                           p->cfg.num_pages, p->cfg.spill_pages);
+    AP_CHECK_LAUNCH("stash push plan launch");
+    ap::Planes pl;
+    for (int i = 0; i < 2; ++i) {
+        pl.p[i] = (i < nplanes) ? const_cast<uint8_t *>(static_cast<const uint8_t *>(src_planes[i])) : nullptr;
+        pl.rb[i] = rb[i];
+        pl.page_off[i] = page_off[i];
+    }
+    pl.n = nplanes;
+    int64_t grid = bound * h.tiles_per_page;
+    if (grid > p->max_ctas) grid = p->max_ctas;
+    if (grid < 1) grid = 1;
+    ap::k_push_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(
+        st, rec, reinterpret_cast<const int32_t *>(p->dev_meta + p->M.ring),
+        reinterpret_cast<const int32_t *>(p->dev_meta + p->M.spill_ring), p->cfg.num_pages, p->cfg.spill_pages,
+        p->dev_pool, p->spill_dev, p->cfg.page_bytes, pl, h.rows_per_tile, h.tiles_per_page);
+    AP_CHECK_LAUNCH("stash push copy launch");
+    p->next_id += 1;
+    p->q_count[slot] += 1;
+    if (record_id) *record_id = h.id;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, void *const *dst_planes,
+                                  int64_t dst_rows, uint64_t *record_id, void *stream)
+{
+    if (!p) return fail(AP_EINVAL, "stash_pop: NULL pool");
+    if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "stash_pop: not the paging stream");
+    if (slot < 0 || slot >= p->cfg.num_slots) return fail(AP_EINVAL, "stash_pop: slot %d out of range", slot);
+    if (p->q_count[slot] == 0) return fail(AP_EEMPTY, "stash_pop: slot %d is empty", slot);
+    const int64_t index = (int64_t)slot * p->cfg.max_records_per_slot + p->q_head[slot];
+    const HostRec &h = p->q[index];
+    if (nplanes != h.nplanes) return fail(AP_EINVAL, "stash_pop: record has %d plane(s), got %d", h.nplanes, nplanes);
+    if (!dst_planes || dst_rows < 0) return fail(AP_EINVAL, "stash_pop: bad destination");
+    for (int i = 0; i < nplanes; ++i)
+        if (!dst_planes[i]) return fail(AP_EINVAL, "stash_pop: NULL destination plane");
+    int64_t page_off[2];
+    plane_fit(p, h.nplanes, h.rb, page_off);
+    ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
+    ap_pool_state *st = reinterpret_cast<ap_pool_state *>(p->dev_meta);
+    ap::k_pop_plan<<<1, 32, 0, p->stream>>>(st, rec.hdr);
+    AP_CHECK_LAUNCH("stash pop plan launch");
+    ap::Planes pl;
+    for (int i = 0; i < 2; ++i) {
+        pl.p[i] = (i < nplanes) ? static_cast<uint8_t *>(dst_planes[i]) : nullptr;
+        pl.rb[i] = h.rb[i];
+        pl.page_off[i] = page_off[i];
+    }
+    pl.n = nplanes;
+    int64_t grid = h.bound_pages * h.tiles_per_page;
+    if (grid > p->max_ctas) grid = p->max_ctas;
+    if (grid < 1) grid = 1;
+    ap::k_pop_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(
+        st, rec, reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),
+        reinterpret_cast<int32_t *>(p->dev_meta + p->M.spill_ring), p->cfg.num_pages, p->cfg.spill_pages,
+        p->dev_pool, p->spill_dev, p->cfg.page_bytes, pl, dst_rows, h.rows_per_tile, h.tiles_per_page);
+    AP_CHECK_LAUNCH("stash pop copy launch");
+    if (record_id) *record_id = h.id;
+    p->q_head[slot] = (p->q_head[slot] + 1) % p->cfg.max_records_per_slot;
+    p->q_count[slot] -= 1;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_queue_len(const ap_pool *p, int32_t slot, int32_t *len)
+{
+    if (!p || !len) return fail(AP_EINVAL, "pool_queue_len: NULL argument");
+    if (slot < 0 || slot >= p->cfg.num_slots) return fail(AP_EINVAL, "pool_queue_len: slot out of range");
+    *len = p->q_count[slot];
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_flags_device_ptr(const ap_pool *p, uint32_t **d_flags)
+{
+    if (!p || !d_flags) return fail(AP_EINVAL, "pool_flags_device_ptr: NULL argument");
+    *d_flags = &reinterpret_cast<ap_pool_state *>(p->dev_meta)->flags;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_overflow_query(ap_pool *p, uint32_t *flags, int32_t wait)
+{
+    if (!p || !flags) return fail(AP_EINVAL, "overflow_query: NULL argument");
+    if (wait) {
+        ap_status s = sync_read(p, p->pinned, &reinterpret_cast<ap_pool_state *>(p->dev_meta)->flags, 4);
+        if (s != AP_OK) return s;
+        memcpy(&p->last_flags, p->pinned, 4);
+    }
+    *flags = p->last_flags;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_read_state(ap_pool *p, ap_pool_state *state)
+{
+    if (!p || !state) return fail(AP_EINVAL, "pool_read_state: NULL argument");
+    ap_status s = sync_read(p, p->pinned, p->dev_meta, sizeof(ap_pool_state));
+    if (s != AP_OK) return s;
+    memcpy(state, p->pinned, sizeof(ap_pool_state));
+    p->last_flags = state->flags;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_read_rings(ap_pool *p, int32_t *ring, int32_t *spill_ring)
+{
+    if (!p || !ring) return fail(AP_EINVAL, "pool_read_rings: NULL argument");
+    ap_status s = sync_read(p, ring, p->dev_meta + p->M.ring, 4 * (size_t)p->cfg.num_pages);
+    if (s == AP_OK && spill_ring && p->cfg.spill_pages > 0)
+        s = sync_read(p, spill_ring, p->dev_meta + p->M.spill_ring, 4 * (size_t)p->cfg.spill_pages);
+    return s;
+}
+
+extern "C" ap_status ap_pool_read_record(ap_pool *p, int32_t slot, int32_t qpos, ap_record_info *info,
+                                         int32_t *page_table, int64_t *row0, int32_t *nrows, int64_t cap)
+{
+    if (!p) return fail(AP_EINVAL, "pool_read_record: NULL pool");
+    if (slot < 0 || slot >= p->cfg.num_slots || qpos < 0 || qpos >= p->q_count[slot])
+        return fail(AP_EINVAL, "pool_read_record: no record at slot %d position %d", slot, qpos);
+    const int64_t index =
+        (int64_t)slot * p->cfg.max_records_per_slot + (p->q_head[slot] + qpos) % p->cfg.max_records_per_slot;
+    ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
+    ap::RecHdr hdr;
+    ap_status s = sync_read(p, &hdr, rec.hdr, sizeof(hdr));
+    if (s != AP_OK) return s;
+    if (info) {
+        info->record_id = p->q[index].id;
+        info->slot = slot;
+        info->nseg = hdr.nseg;
+        info->npages = hdr.npages;
+        info->ndev = hdr.ndev;
+        info->nspill = hdr.nspill;
+        info->nlost = hdr.nlost;
+    }
+    int64_t n = hdr.npages < cap ? hdr.npages : cap;
+    if (n <= 0) return AP_OK;
+    if (page_table) {
+        s = sync_read(p, page_table, rec.page_table, 4 * (size_t)n);
+        if (s != AP_OK) return s;
+    }
+    if (row0 || nrows) {
+        ap::PageDesc *tmp = static_cast<ap::PageDesc *>(malloc(sizeof(ap::PageDesc) * (size_t)n));
+        if (!tmp) return fail(AP_EINVAL, "pool_read_record: out of host memory");
+        s = sync_read(p, tmp, rec.desc, sizeof(ap::PageDesc) * (size_t)n);
+        if (s == AP_OK)
+            for (int64_t i = 0; i < n; ++i) {
+                if (row0) row0[i] = tmp[i].row0;
+                if (nrows) nrows[i] = tmp[i].nrows;
+            }
+        free(tmp);
+    }
+    return s;
+}

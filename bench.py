@@ -1,0 +1,435 @@
+"""Benchmark: MoE token movement with a paged activation stash on one GPU.
+
+One step is the whole path over one batch of the Qwen3-MoE-like layer
+(T = 16384 tokens as 2 chunks of 8192, H = 2048, E = 128, top-8, dropless,
+64-token pages, pool = 1.1x the live rows): for each chunk route -> dispatch
+-> stash push; then for each chunk stash pop -> combine of the expert outputs.
+All calls go through the C ABI on one high-priority stream.  Inputs are
+seeded synthetic tensors resident in HBM; the step's working set (~1.4 GB)
+is larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+stash+combine tokens/s and HBM GB/s (% of GB300 peak), 1 GPU"
+WORKLOAD = "qwen3_moe"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------------
+# distributed helpers (replicas: no collective on the data path)
+# ----------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate_max(value: float, world: int) -> float:
+    """Maximum of a per-rank number over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ----------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", str(period_ms)], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+# ----------------------------------------------------------------------------------
+# the native step
+# ----------------------------------------------------------------------------------
+def op_bytes(wl, R):
+    """Algorithmic bytes of each op for one chunk (R kept rows)."""
+    T, H, E, k = wl.T, wl.H, wl.E, wl.k
+    rb = wl.row_bytes[0]
+    return {
+        "route": T * E * 4 + T * k * 8,
+        "dispatch": T * H * 2 + R * rb + T * k * 8 + R * 4,
+        "push": 2 * R * rb,
+        "pop": 2 * R * rb,
+        "combine": R * H * 2 + T * H * 2 + T * k * 8,
+    }
+
+
+class Step:
+    """Buffers and calls of one step; every call is enqueued on ``self.stream``."""
+
+    def __init__(self, wl, device, seed_base: int):
+        import torch
+        import activation_paging_gb300 as ap
+        from activation_paging_gb300 import inputs
+
+        self.torch, self.ap, self.wl = torch, ap, wl
+        self.device = device
+        self.pool = ap.Pool(wl.page_tokens, wl.page_bytes, wl.num_pages, wl.num_slots, 4, wl.E, wl.num_pages,
+                            device=device)
+        self.stream = self.pool.stream
+        self.chunks = []
+        for c in range(wl.chunks):
+            seed = seed_base + c
+            logits = inputs.router_logits(seed, wl.T, wl.E)
+            x = inputs.normal_bf16(seed, inputs.X_STREAM, (wl.T, wl.H))
+            y = inputs.normal_bf16(seed, inputs.Y_STREAM, (wl.rows, wl.H))
+            h = {"logits": torch.from_numpy(logits).pin_memory(),
+                 "x": torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                 "y": torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).pin_memory()}
+            d = {key: t.to(device) for key, t in h.items()}
+            self.stream.wait_stream(torch.cuda.current_stream())  # uploads ran on the current stream
+            d["idx"] = torch.empty((wl.T, wl.k), dtype=torch.int32, device=device)
+            d["w"] = torch.empty((wl.T, wl.k), dtype=torch.float32, device=device)
+            ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=self.stream)
+            d["disp"] = ap.dispatch_permute(d["x"], d["idx"], wl.E, stream=self.stream)  # allocates outputs
+            d["dst"] = torch.empty_like(d["disp"]["xd"])
+            d["out"] = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device)
+            h["out"] = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+            self.chunks.append((h, d))
+        torch.cuda.synchronize(device)
+        self.R = wl.rows
+        self.bytes = op_bytes(wl, self.R)
+        self.launches_per_step = wl.chunks * (1 + 4 + 2 + 2 + 1)
+
+    def run(self, events=None, e2e=False):
+        """Enqueue one step.  events: dict op -> list of (start, end) event pairs."""
+        torch, ap, wl, s = self.torch, self.ap, self.wl, self.stream
+
+        def rec(name, fn):
+            if events is None:
+                fn()
+                return
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            events.setdefault(name, []).append((a, b))
+
+        with torch.cuda.stream(s):
+            for c, (h, d) in enumerate(self.chunks):
+                if e2e:
+                    d["logits"].copy_(h["logits"], non_blocking=True)
+                    d["x"].copy_(h["x"], non_blocking=True)
+                    d["y"].copy_(h["y"], non_blocking=True)
+                rec("route", lambda: ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=s))
+                rec("dispatch", lambda: ap.dispatch_permute(d["x"], d["idx"], wl.E, out=d["disp"], stream=s))
+                rec("push", lambda: self.pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"], d["disp"]["live"]))
+            for c, (h, d) in enumerate(self.chunks):
+                rec("pop", lambda: self.pool.pop(0, [d["dst"]]))
+                rec("combine", lambda: ap.combine_unpermute(d["y"], d["disp"]["dest"], d["w"], out=d["out"],
+                                                            stream=s))
+                if e2e:
+                    h["out"].copy_(d["out"], non_blocking=True)
+
+    def transfer_bytes(self):
+        h2d = sum(h["logits"].nbytes + h["x"].nbytes + h["y"].nbytes for h, _ in self.chunks)
+        d2h = sum(h["out"].nbytes for h, _ in self.chunks)
+        return h2d, d2h
+
+
+def kernel_hash() -> str:
+    path = os.path.join(ROOT, "activation_paging_gb300", "csrc", "stash.cu")
+    common = os.path.join(ROOT, "activation_paging_gb300", "csrc", "ap_common.cuh")
+    h = hashlib.sha256()
+    for p in (path, common):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def native(args):
+    import torch
+    from activation_paging_gb300 import inputs, build as cuda_build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    cuda_build.build()
+    wl = inputs.WORKLOADS[WORKLOAD]
+    step = Step(wl, device, seed_base=1000 * rank)
+    tokens_per_step = wl.T * wl.chunks
+
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize(device)
+
+    # timed region: K steps, events around every call on the launching stream
+    events = {}
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(step.stream)
+    for _ in range(args.steps):
+        step.run(events)
+    t1.record(step.stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    max_elapsed = aggregate_max(elapsed, world)
+    value = whole_job_rate(tokens_per_step * args.steps, world, max_elapsed)
+
+    per_op = {}
+    for name, pairs in events.items():
+        ms = [a.elapsed_time(b) for a, b in pairs]
+        per_op[name] = sum(ms) / len(ms)  # per launch (per chunk)
+    total_bytes = sum(step.bytes.values()) * wl.chunks
+    ms_per_step = max_elapsed * 1e3 / args.steps
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
+    peak_src = "measured" if peaks and "hbm_gbs" in peaks else "fallback"
+    ops = {name: {"ms": round(per_op[name], 5), "bytes": step.bytes[name],
+                  "gbs": round(step.bytes[name] / (per_op[name] / 1e3) / 1e9, 1),
+                  "frac": round(step.bytes[name] / (per_op[name] / 1e3) / 1e9 / peak, 4)} for name in per_op}
+    dom = max(per_op, key=per_op.get)  # the op with the longest launches
+    traffic = None
+    try:
+        tr = json.load(open(PROFILE_TRAFFIC))
+        if tr.get("kernel_hash") == kernel_hash() and dom in tr.get("per_launch_bytes", {}):
+            traffic = tr["per_launch_bytes"][dom]
+    except Exception:
+        pass
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": ops[dom]["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": ops[dom]["frac"], "traffic": traffic, "peak_source": peak_src,
+                "note": "achieved = algorithmic bytes per launch / CUDA-event time of the call on its stream"}
+
+    e2e = None
+    if not args.no_e2e:
+        h2d, d2h = step.transfer_bytes()
+        for _ in range(2):
+            step.run(e2e=True)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(step.stream)
+        for _ in range(args.e2e_steps):
+            step.run(e2e=True)
+        b.record(step.stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e_el = aggregate_max(a.elapsed_time(b) / 1e3, world)
+        e2e = {"value": round(whole_job_rate(tokens_per_step * args.e2e_steps, world, e_el), 1),
+               "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps, "ms_per_step": round(e_el * 1e3 / args.e2e_steps, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, budget_s=10.0)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1) activations, logits and expert outputs)",
+                "config": {"workload": f"{WORKLOAD}: T=16384 (2 chunks x 8192), H=2048, E=128, top-8, dropless, "
+                                       f"page=64 tokens, pool={wl.num_pages} pages (1.1x live rows)",
+                           "tokens_per_step": tokens_per_step, "bytes_per_step": total_bytes,
+                           "hbm_gbs_step": round(total_bytes / (ms_per_step / 1e3) / 1e9, 1),
+                           "l2": "working set per step ~1.4 GB > 126 MB L2: no flush",
+                           "parallelism": f"replicas x{world}", "stream": "one high-priority stream"},
+                "roofline": roofline, "ops": ops, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": step.launches_per_step * args.steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------
+# the oracle (CPU baseline and reference arm)
+# ----------------------------------------------------------------------------------
+def oracle_step(wl, T_sample: int, seed: int = 0):
+    """One pass of the oracle over T_sample tokens per chunk; returns tokens processed."""
+    import oracle
+    from activation_paging_gb300 import inputs
+
+    pool = oracle.Pool(wl.page_tokens, wl.page_bytes, max(8, int(wl.num_pages * T_sample / wl.T) + wl.E * 2),
+                       1, 4, wl.E, 1 << 20, 0, keep_bytes=True)
+    plans = []
+    for c in range(wl.chunks):
+        logits = inputs.router_logits(seed + c, T_sample, wl.E)
+        x = inputs.normal_bf16(seed + c, inputs.X_STREAM, (T_sample, wl.H))
+        y = inputs.normal_bf16(seed + c, inputs.Y_STREAM, (T_sample * wl.k, wl.H))
+        plans.append((logits, x, y))
+    t0 = time.perf_counter()
+    kept = []
+    for logits, x, y in plans:
+        idx, w = oracle.route_topk(logits, wl.k)
+        plan = oracle.dispatch(x, idx, wl.E, 0, False)
+        pool.push(0, [plan["xd"]], plan["rows"], plan["seg_off"], plan["live"])
+        kept.append((plan, w, y))
+    for plan, w, y in kept:
+        dst = np.empty_like(plan["xd"])
+        pool.pop(0, [dst], plan["rows"])
+        oracle.combine(y, plan["dest"], w)
+    dt = time.perf_counter() - t0
+    pool.close()
+    return T_sample * wl.chunks, dt
+
+
+def cpu_baseline(wl, budget_s: float):
+    import oracle
+    oracle.build()
+    n, dt = oracle_step(wl, 512)
+    per_tok = dt / n
+    T_sample = int(min(wl.T, max(256, budget_s / 2 / per_tok / wl.chunks)))
+    tokens, secs = 0, 0.0
+    reps = 0
+    while secs < budget_s and reps < 4:
+        n, dt = oracle_step(wl, T_sample, seed=reps)
+        tokens += n
+        secs += dt
+        reps += 1
+    return {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} oracle passes of {T_sample} tokens per chunk x {wl.chunks} chunks "
+                      f"(route, dispatch, byte-exact stash push/pop, combine), single-threaded C",
+            "seconds": round(secs, 2)}
+
+
+def reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from activation_paging_gb300 import inputs
+    oracle.build()
+    wl = inputs.WORKLOADS[WORKLOAD]
+    n, dt = oracle_step(wl, 256)
+    per_tok = dt / n
+    budget = 150.0 / max(args.steps + max(args.warmup, 3), 1)
+    T_sample = int(min(wl.T, max(64, budget / per_tok / wl.chunks)))
+    for i in range(max(args.warmup, 3)):
+        oracle_step(wl, T_sample, seed=i)
+    tokens, secs = 0, 0.0
+    for i in range(args.steps):
+        n, dt = oracle_step(wl, T_sample, seed=100 + i)
+        tokens += n
+        secs += dt
+    value = tokens / secs
+    sample = (f"{T_sample} tokens per chunk x {wl.chunks} chunks per step of the {WORKLOAD} workload "
+              f"(the full step is {wl.T} per chunk), single-threaded C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(secs * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, logits and expert outputs)",
+            "config": {"workload": f"{WORKLOAD}: T=16384 (2 chunks x 8192), H=2048, E=128, top-8, dropless, "
+                                   f"page=64 tokens", "sample_tokens_per_step": T_sample * wl.chunks},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "kind": "oracle", "cores": 1,
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,311 @@
+/*
+ * ap.h - C ABI of the GB300 token-movement library for a top-k MoE layer with
+ * a paged activation stash (libap.so).
+ *
+ * The path: route_topk -> dispatch_permute -> stash_push ... stash_pop ->
+ * combine_unpermute, all on one GPU.  Every call is asynchronous on the CUDA
+ * stream it is given (passed as `void *`, a cudaStream_t; NULL = legacy
+ * default stream) and launches only this library's kernels.  No call
+ * allocates device memory: the caller owns every buffer (device pointers
+ * unless marked "host").  No call synchronises the host except the explicit
+ * read-out calls at the end of this header.
+ *
+ * Errors: every call returns an ap_status.  Argument and queue errors are
+ * detected on the host and returned before anything is launched.  Conditions
+ * only the GPU can see (pool overflow, lost spill pages, out-of-range counts
+ * or indices) never fault and never stop the stream: the kernel skips the
+ * offending copy and ORs a bit into a sticky device status word, read later
+ * (the deferred overflow handling of torchtitan pull 5541, AI-Generated
+ * Details, last paragraph).
+ *
+ * Sources (web pages) cited below:
+ *   torchtitan pull 5541 - HybridEP eager scheduling with a paged activation
+ *     stash, "AI-Generated Details" and "Verification";
+ *   torchtitan pull 5542 - "[graph_trainer] Overlap HybridEP and paging
+ *     across combined PP graphs";
+ *   Megatron-LM pull 7342 - token-wise ChunkedEP for Qwen3 MoE, "Summary",
+ *     "Validation and performance";
+ *   OpenPipe/ART pull 971 - "Price HybridEP recompute outputs at the live
+ *     communication extent".
+ */
+#ifndef AP_H_
+#define AP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------- */
+typedef int32_t ap_status;
+#define AP_OK 0
+#define AP_EINVAL (-1)     /* bad argument (size, pointer, layout)             */
+#define AP_EEMPTY (-2)     /* stash_pop on a slot with no record               */
+#define AP_EQFULL (-3)     /* stash_push on a slot whose record queue is full  */
+#define AP_ECUDA (-4)      /* a CUDA runtime call failed (see ap_last_error)   */
+#define AP_ESTREAM (-5)    /* pool call on a stream other than the paging one  */
+#define AP_ENOTSUP (-6)    /* configuration not supported by this build        */
+
+/* ---- sticky device status bits --------------------------------------------- */
+#define AP_FLAG_POOL_OVERFLOW 0x1u   /* device pages ran out; the excess spilled */
+#define AP_FLAG_SPILL_OVERFLOW 0x2u  /* spill pages ran out too; pages lost      */
+#define AP_FLAG_RECORD_OVERFLOW 0x4u /* a record needed > max_pages_per_record   */
+#define AP_FLAG_BAD_COUNT 0x8u       /* a segment lay outside the given rows     */
+#define AP_FLAG_BAD_INDEX 0x10u      /* an expert id or row index out of range   */
+#define AP_FLAG_CORRUPT 0x20u        /* a page id read back out of range         */
+
+/* payload types of dispatch_permute */
+#define AP_DTYPE_BF16 0
+#define AP_DTYPE_E4M3 1
+
+/* Human-readable name of a status code (static string). */
+const char *ap_status_str(ap_status s);
+/* Last error message of the calling thread (static per thread, never NULL). */
+const char *ap_last_error(void);
+/* Library version, e.g. "0.1.0". */
+const char *ap_version(void);
+
+/* ============================================================================
+ * route_topk
+ *
+ * Router of a top-k MoE layer: per token, p = softmax(logits) over the E
+ * experts, the k largest logits are selected in descending order (an equal
+ * logit goes to the lower expert id; j = 0 is the top choice), and the
+ * selected probabilities are renormalised, w_j = p_j / sum_sel p.  Since the
+ * softmax denominator cancels, w_j = exp(l_j - m) / sum_sel exp(l_i - m) with
+ * m the row maximum, computed in single precision.  Top-k routing with k = 8:
+ * Megatron-LM pull 7342, "Validation and performance".
+ *
+ *   logits  [T, E] float32, row-major (device, read)
+ *   idx     [T, k] int32 (device, written): expert ids
+ *   w       [T, k] float32 (device, written): renormalised weights
+ * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), 0 <= T < 2^31.  Logits must
+ * be finite.  Returns AP_EINVAL on a bad size or NULL pointer with T > 0.
+ * ========================================================================== */
+ap_status ap_route_topk(const float *logits, int64_t T, int32_t E, int32_t k,
+                        int32_t *idx, float *w, void *stream);
+
+/* ============================================================================
+ * dispatch_permute
+ *
+ * Expert-major, capacity-bounded permutation of token rows (dispatch into
+ * expert buffers, Megatron-LM pull 7342 "Summary"; capacity-shaped buffers,
+ * torchtitan pull 5541 "AI-Generated Details" and pull 5542).
+ *
+ * Pairs (t, j) are ranked in t-then-j order within their expert: the rank of
+ * a pair is the number of earlier pairs routed to the same expert.  A pair is
+ * kept iff capacity <= 0 (dropless) or rank < capacity; dropped pairs get
+ * dest = -1.  live[e] = kept rows of expert e.  Layout: padded (padded = 1,
+ * needs capacity > 0): seg_off[e] = e * capacity, xd has E*capacity rows;
+ * compact: seg_off = exclusive prefix sum of live, xd has sum(live) <= T*k
+ * rows.  Row dest(t, j) of xd receives row t of x:
+ *   AP_DTYPE_BF16: the H BF16 values, byte for byte;
+ *   AP_DTYPE_E4M3: per token amax = max|x[t]|, scale = amax/448,
+ *     q = e4m3_rn_satfinite(x * (448/amax)) (scale = 1 and q = e4m3(x) when
+ *     amax = 0); xd row = H code bytes, xd_scale[row] = scale.
+ * Rows of xd not written (padding, drops) keep their previous contents.
+ *
+ *   x        [T, H] bf16 (device, read)
+ *   idx      [T, k] int32 expert ids (device, read); ids outside [0, E) are
+ *            skipped (dest -1) and set AP_FLAG_BAD_INDEX in *d_status
+ *   xd       [xd_rows, H] bf16 or uint8 (device, written)
+ *   xd_scale [xd_rows] float32 (device, written; E4M3 only, else NULL)
+ *   counts, live, seg_off  [E] int32 (device, written)
+ *   dest     [T, k] int32 (device, written)
+ *   src_tok  [xd_rows] int32 (device, written for kept rows only; may be NULL)
+ *   scratch  device work space of ap_dispatch_scratch_bytes() bytes, 16-byte
+ *            aligned; its contents need no initialisation
+ *   d_status device uint32 word, bits ORed in (may be NULL)
+ * xd_rows must be >= E*capacity (padded) or >= T*k (compact), so no write can
+ * leave the buffer.  Limits: 1 <= E <= 1024, 1 <= k <= 32, H >= 1,
+ * T*k < 2^31.
+ * ========================================================================== */
+ap_status ap_dispatch_scratch_bytes(int64_t T, int32_t k, int32_t E,
+                                    int64_t *bytes);
+ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H,
+                              const int32_t *idx, int32_t k, int32_t E,
+                              int32_t capacity, int32_t padded,
+                              int32_t out_dtype, void *xd, float *xd_scale,
+                              int64_t xd_rows, int32_t *counts, int32_t *live,
+                              int32_t *seg_off, int32_t *dest,
+                              int32_t *src_tok, void *scratch,
+                              int64_t scratch_bytes, uint32_t *d_status,
+                              void *stream);
+
+/* ============================================================================
+ * combine_unpermute
+ *
+ * Top-k weighted un-permute back to a dense BF16 [T, H] output (combine with
+ * un-permute writing a fresh dense BF16 output: OpenPipe/ART pull 971,
+ * description and review).  Per token and column:
+ *   acc = 0 (float32); for j = 0..k-1 with dest[t, j] >= 0:
+ *     acc = acc + w[t, j] * y[dest[t, j]]   (separately rounded mul and add)
+ *   out[t] = bf16_round_nearest_even(acc)
+ * A token whose rows were all dropped gets +0.  A row index >= y_rows is
+ * skipped and sets AP_FLAG_BAD_INDEX in *d_status (may be NULL).
+ *
+ *   y     [y_rows, H] bf16 (device, read)
+ *   dest  [T, k] int32, w [T, k] float32 (device, read)
+ *   out   [T, H] bf16 (device, written; exactly T rows)
+ * Limits: H >= 1, 1 <= k <= 32.
+ * ========================================================================== */
+ap_status ap_combine_unpermute(const void *y, int64_t y_rows, int32_t H,
+                               const int32_t *dest, const float *w, int64_t T,
+                               int32_t k, void *out, uint32_t *d_status,
+                               void *stream);
+
+/* ============================================================================
+ * Paged activation stash (torchtitan pull 5541, "AI-Generated Details":
+ * binding live counts to sources, one high-priority paging stream that
+ * serialises free-list changes, FIFO records per slot, page-aligned
+ * multi-token copy tiles with one page resolved per tile and only the page's
+ * first tile recording or recycling it, live-prefix and page-tail masks,
+ * 64-bit addressing, host spill, sticky overflow, a grid bound that changes
+ * neither capacity nor the rows copied; "Verification": wrapped allocation
+ * and recycling, changing device counts, BF16/FP8 payloads, host spill).
+ *
+ * A pool is N pages of page_bytes bytes of device memory plus spill_pages
+ * pages of mapped pinned host memory.  Free pages form a ring: pages are
+ * taken from its head and returned to its tail.  A push copies the live
+ * prefix of each of nseg segments (rows seg_off[s] .. seg_off[s]+live[s]-1
+ * of every plane; live and seg_off are read on the device, so they may
+ * change between CUDA-graph replays) into ceil(live[s]/P) pages, segment by
+ * segment; each page takes the next free device page, else the next free
+ * spill page (AP_FLAG_POOL_OVERFLOW), else it is lost and not copied
+ * (AP_FLAG_SPILL_OVERFLOW).  Inside a page, plane 0 rows are dense at
+ * r * row_bytes[0]; plane 1 (e.g. FP8 scales) starts at
+ * roundup16(P * row_bytes[0]).  Bytes past a page's live rows are untouched.
+ * A pop takes the slot's oldest record, copies every page back to the same
+ * rows of the destination planes (rows outside the live prefixes are not
+ * touched) and returns the pages to the free ring in page order.
+ * "Exactly full" is not an overflow.  Flags stay set until ap_pool_reset.
+ * ========================================================================== */
+typedef struct ap_pool ap_pool; /* opaque host object */
+
+typedef struct {
+    int32_t page_tokens;          /* P: rows per page, >= 1                    */
+    int32_t num_slots;            /* S: independent FIFO record queues         */
+    int64_t page_bytes;           /* bytes per page, multiple of 16            */
+    int64_t num_pages;            /* N: device pages, 1 .. 2^31-1              */
+    int64_t spill_pages;          /* host spill pages, >= 0                    */
+    int32_t max_records_per_slot; /* queue depth of each slot                  */
+    int32_t max_segments;         /* largest nseg of a push                    */
+    int64_t max_pages_per_record; /* page-table entries per record             */
+    int32_t max_ctas;             /* copy grid bound; 0: environment variable
+                                     AP_STASH_MAX_CTAS if set, else 2048       */
+    int32_t reserved;             /* must be 0                                 */
+} ap_pool_config;
+
+/* Device state word block at the start of the metadata buffer (read-only for
+ * users; counters grow monotonically, ring positions are counter mod size). */
+typedef struct {
+    uint64_t head, tail;             /* free device ring: free = tail - head   */
+    uint64_t spill_head, spill_tail; /* free spill ring                        */
+    uint32_t flags;                  /* sticky AP_FLAG_* bits                  */
+    uint32_t pad0;
+    int64_t high_water;              /* most device pages ever in use          */
+    int64_t spill_high_water;        /* most spill pages ever in use           */
+    int64_t pad1;
+} ap_pool_state;
+
+/* Per-record summary returned by ap_pool_read_record. */
+typedef struct {
+    uint64_t record_id;
+    int32_t slot, nseg;
+    int64_t npages, ndev, nspill, nlost;
+} ap_record_info;
+
+/* Sizes the caller must provide: device pool bytes (N * page_bytes),
+ * device metadata bytes, and host spill bytes (spill_pages * page_bytes). */
+ap_status ap_pool_required_bytes(const ap_pool_config *cfg,
+                                 int64_t *dev_pool_bytes,
+                                 int64_t *dev_meta_bytes,
+                                 int64_t *host_spill_bytes);
+
+/* Create a pool over caller-owned memory.  dev_pool: device, 256-byte aligned,
+ * dev_pool_bytes.  dev_meta: device, 256-byte aligned, dev_meta_bytes.
+ * host_spill: pinned host memory (cudaHostAlloc / torch pin_memory) of
+ * host_spill_bytes, mapped into the device address space; NULL iff
+ * spill_pages == 0.  paging_stream: the one stream every later push, pop and
+ * reset of this pool must use (create it with high priority).  Enqueues the
+ * reset of the metadata on that stream; allocates only the host object and a
+ * few bytes of pinned host memory for read-outs. */
+ap_status ap_pool_init(ap_pool **out, const ap_pool_config *cfg,
+                       void *dev_pool, void *dev_meta, void *host_spill,
+                       void *paging_stream);
+/* Asynchronously return every page, clear flags and statistics, and empty
+ * the record queues.  Pool bytes are not touched. */
+ap_status ap_pool_reset(ap_pool *pool, void *stream);
+/* Free the host object (not the caller's buffers). */
+ap_status ap_pool_destroy(ap_pool *pool);
+/* Resolved copy-grid bound of the pool (max_ctas after the environment). */
+ap_status ap_pool_max_ctas(const ap_pool *pool, int32_t *max_ctas);
+
+/* Push one record into `slot`.
+ *   nplanes      1 or 2
+ *   src_planes   host array of nplanes device pointers, each [src_rows, rb]
+ *   row_bytes    host array of nplanes row sizes in bytes
+ *   src_rows     rows of every source plane (bounds every copy)
+ *   nseg         segments, 0 .. max_segments
+ *   d_seg_off, d_live  [nseg] int32 (device, read at execution time and
+ *                snapshotted into the record); a segment with live < 0,
+ *                seg_off < 0 or seg_off + live > src_rows is not copied and
+ *                sets AP_FLAG_BAD_COUNT
+ *   record_id    (host, written) monotonically increasing id, first is 1
+ * Returns AP_EQFULL when the slot queue is full, AP_ESTREAM when `stream` is
+ * not the paging stream, AP_EINVAL when the planes do not fit a page. */
+ap_status ap_stash_push(ap_pool *pool, int32_t slot, int32_t nplanes,
+                        const void *const *src_planes,
+                        const int64_t *row_bytes, int64_t src_rows,
+                        int32_t nseg, const int32_t *d_seg_off,
+                        const int32_t *d_live, uint64_t *record_id,
+                        void *stream);
+
+/* Pop the oldest record of `slot` into dst_planes (host array of nplanes
+ * device pointers, each [dst_rows, row_bytes of the push]).  A page whose
+ * rows fall outside dst_rows is not copied (AP_FLAG_BAD_COUNT) but still
+ * recycled.  record_id (host, may be NULL) receives the popped id.  Returns
+ * AP_EEMPTY when the slot has no record. */
+ap_status ap_stash_pop(ap_pool *pool, int32_t slot, int32_t nplanes,
+                       void *const *dst_planes, int64_t dst_rows,
+                       uint64_t *record_id, void *stream);
+
+/* Records queued in a slot (host-side count, no synchronisation). */
+ap_status ap_pool_queue_len(const ap_pool *pool, int32_t slot, int32_t *len);
+
+/* Device address of the sticky flag word (uint32), for device-side consumers
+ * such as an optimizer step that skips itself on overflow. */
+ap_status ap_pool_flags_device_ptr(const ap_pool *pool, uint32_t **d_flags);
+
+/* ---- read-outs: these synchronise the paging stream ----------------------- */
+/* Sticky flags (the only call meant for the training loop).  wait = 1
+ * synchronises the paging stream and returns the current flags; wait = 0
+ * returns the flags captured by the previous wait = 1 call (or 0). */
+ap_status ap_overflow_query(ap_pool *pool, uint32_t *flags, int32_t wait);
+/* Whole state block (synchronises). */
+ap_status ap_pool_read_state(ap_pool *pool, ap_pool_state *state);
+/* Free rings: ring [num_pages] int32 and spill_ring [spill_pages] int32
+ * (host, written; spill_ring may be NULL).  Synchronises. */
+ap_status ap_pool_read_rings(ap_pool *pool, int32_t *ring,
+                             int32_t *spill_ring);
+/* Record at queue position qpos (0 = oldest) of a slot: its summary and up
+ * to cap page-table entries (device page p -> p, spill page s -> N + s,
+ * lost -> -1), first rows and row counts (host arrays, each may be NULL).
+ * Synchronises. */
+ap_status ap_pool_read_record(ap_pool *pool, int32_t slot, int32_t qpos,
+                              ap_record_info *info, int32_t *page_table,
+                              int64_t *row0, int32_t *nrows, int64_t cap);
+
+/* ============================================================================
+ * E4M3 conversion used by the FP8 dispatch, exposed for testing the format:
+ * out[i] = e4m3_rn_satfinite(in[i]) (round to nearest even, finite overflow
+ * saturates to +-448, NaN -> 0x7F).  in: device float32 [n], out: device
+ * uint8 [n].
+ * ========================================================================== */
+ap_status ap_cast_e4m3(const float *in, uint8_t *out, int64_t n, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AP_H_ */
