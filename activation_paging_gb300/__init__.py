@@ -212,8 +212,21 @@ class Pool:
             rb[i] = (t.numel() // rows) * t.element_size() if rows else t[0:0].element_size()
         return ptrs, rb, rows
 
+    def _order_after_caller(self, tensors):
+        """Make the paging stream wait for the caller's current stream, and tell
+        the caching allocator that the tensors are used on the paging stream."""
+        cur = torch.cuda.current_stream(self.device)
+        if cur != self.stream:
+            self.stream.wait_stream(cur)
+            for t in tensors:
+                if t is not None and t.is_cuda:
+                    t.record_stream(self.stream)
+
     def push(self, slot: int, planes, seg_off: torch.Tensor, live: torch.Tensor) -> int:
-        """Stash the live prefixes of every segment of ``planes`` (list of 1-2 tensors)."""
+        """Stash the live prefixes of every segment of ``planes`` (list of 1-2 tensors).
+
+        The paging stream first waits for the caller's current stream."""
+        self._order_after_caller(list(planes) + [seg_off, live])
         ptrs, rb, rows = self._planes(planes)
         rid = ctypes.c_uint64()
         nseg = seg_off.numel()
@@ -222,7 +235,11 @@ class Pool:
         return rid.value
 
     def pop(self, slot: int, planes) -> int:
-        """Reload the slot's oldest record into ``planes`` (same rows as pushed)."""
+        """Reload the slot's oldest record into ``planes`` (same rows as pushed).
+
+        The paging stream first waits for the caller's current stream; the
+        caller orders later reads after ``self.stream``."""
+        self._order_after_caller(list(planes))
         ptrs, _, rows = self._planes(planes)
         rid = ctypes.c_uint64()
         check(self.lib.ap_stash_pop(self.handle, slot, len(planes), ptrs, rows, ctypes.byref(rid),

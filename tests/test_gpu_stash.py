@@ -153,7 +153,7 @@ def test_two_planes_fp8_layout_odd_rows():
 
 
 def test_spill_exhausted_lost_pages_and_reset():
-    t = Twin(4, (16,), N=3, S=1, R=4, segs=2, SP=2)
+    t = Twin(4, (16,), N=3, S=1, R=4, segs=2, SP=2, maxp=16)
     src = rows_np(1, 40, 16)
     t.push(0, [src], [0, 20], [13, 11])  # 4 + 3 pages: 3 device, 2 spill, 2 lost
     t.check(images=True)
