@@ -15,6 +15,10 @@ void set_error(const char *fmt, ...);
 ap_status fail(ap_status s, const char *fmt, ...);
 ap_status cuda_fail(cudaError_t e, const char *what);
 int sm_count();
+// Blocks of `kernel` (launched with `threads` threads and `smem` dynamic shared
+// bytes) that fit on the whole GPU at once: SMs x resident blocks per SM.
+// Grid-stride kernels launched with this grid run in exactly one wave.
+int resident_grid(const void *kernel, int threads, size_t smem = 0);
 
 #define AP_CHECK_LAUNCH(what)                                   \
     do {                                                        \

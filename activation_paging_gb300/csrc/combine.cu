@@ -1,9 +1,9 @@
 // Combine / un-permute: out[t] = bf16(sum_j w[t, j] * y[dest[t, j]]).
 //
 // The dense BF16 [T, H] output of combine with un-permute (OpenPipe/ART pull
-// 971, description and review).  One warp per token; each lane owns VE
-// consecutive columns per step and gathers the k expert rows of its columns,
-// all k loads in flight before the accumulation.  Accumulation is single
+// 971, description and review).  One warp per (token, column chunk); each
+// lane owns VE consecutive columns per step and gathers the k expert rows of
+// its columns, all k loads in flight before the accumulation.  Accumulation is single
 // precision with separately rounded multiply and add, j ascending (no FMA),
 // then one round-to-nearest-even conversion to BF16.
 #include <cuda_bf16.h>
@@ -49,6 +49,8 @@ __device__ __forceinline__ typename Vec<VE>::T pack(const float *f)
     return v;
 }
 
+// Work item = (token, column chunk of U*32 lane steps); items are strided over
+// all resident warps so every warp gets the same share (no partial last wave).
 // U column steps are unrolled so that U*k row loads are in flight per lane.
 template <int VE, int U>
 __global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ y, int64_t y_rows, int H,
@@ -59,51 +61,64 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ y,
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int nstep = H / VE;
-    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+    const int chunks = (nstep + U * kWarp - 1) / (U * kWarp);
+    const int64_t items = T * chunks;
+    for (int64_t it = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; it < items; it += warps) {
+        const int64_t t = it / chunks;
+        const int s0 = (int)(it - t * chunks) * U * kWarp;
         int32_t my_d = -1;
         float my_w = 0.f;
         if (lane < k) {
-            my_d = __ldcs(dest + t * k + lane);
-            my_w = __ldcs(w + t * k + lane);
+            my_d = dest[t * k + lane];
+            my_w = w[t * k + lane];
             if (my_d >= y_rows) {
-                if (d_status) atomicOr(d_status, AP_FLAG_BAD_INDEX);
+                if (d_status && s0 == 0) atomicOr(d_status, AP_FLAG_BAD_INDEX);
                 my_d = -1;
             }
         }
-        uint16_t *orow = out + t * H;
-        // warp-uniform loop over column steps
-        for (int s0 = 0; s0 < nstep; s0 += U * kWarp) {
-            float acc[U][VE];
+        float acc[U][VE];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-                for (int i = 0; i < VE; ++i) acc[u][i] = 0.f;
-            for (int j = 0; j < k; ++j) {
-                const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
-                const float wj = __shfl_sync(0xffffffffu, my_w, j);
-                if (d < 0) continue;
-                const V *yrow = reinterpret_cast<const V *>(y + (int64_t)d * H);
-                V v[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int s = s0 + u * kWarp + lane;
-                    if (s < nstep) v[u] = ld_stream(yrow + s);
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    float f[VE];
-                    unpack<VE>(v[u], f);
-#pragma unroll
-                    for (int i = 0; i < VE; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(wj, f[i]));
-                }
-            }
+            for (int i = 0; i < VE; ++i) acc[u][i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+            const float wj = __shfl_sync(0xffffffffu, my_w, j);
+            if (d < 0) continue;
+            const V *yrow = reinterpret_cast<const V *>(y + (int64_t)d * H);
+            V v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int s = s0 + u * kWarp + lane;
-                if (s < nstep) st_stream(reinterpret_cast<V *>(orow) + s, pack<VE>(acc[u]));
+                if (s < nstep) v[u] = ld_stream(yrow + s);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float f[VE];
+                unpack<VE>(v[u], f);
+#pragma unroll
+                for (int i = 0; i < VE; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(wj, f[i]));
             }
         }
+        uint16_t *orow = out + t * H;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + u * kWarp + lane;
+            if (s < nstep) st_stream(reinterpret_cast<V *>(orow) + s, pack<VE>(acc[u]));
+        }
     }
+}
+
+template <int VE, int U>
+void launch_combine(const uint16_t *y, int64_t y_rows, int H, const int32_t *dest, const float *w, int64_t T, int k,
+                    uint16_t *out, uint32_t *d_status, cudaStream_t st)
+{
+    static const int resident = resident_grid((const void *)k_combine<VE, U>, 256);
+    const int nstep = H / VE;
+    const int64_t items = T * ((nstep + U * kWarp - 1) / (U * kWarp));
+    const int64_t want = (items + 7) / 8;
+    const int grid = (int)(want < resident ? want : resident);
+    k_combine<VE, U><<<grid, 256, 0, st>>>(y, y_rows, H, dest, w, T, k, out, d_status);
 }
 
 } // namespace
@@ -118,20 +133,17 @@ extern "C" ap_status ap_combine_unpermute(const void *y, int64_t y_rows, int32_t
     if (T == 0) return AP_OK;
     if (!dest || !w || !out || (!y && y_rows > 0)) return fail(AP_EINVAL, "combine_unpermute: NULL pointer");
     cudaStream_t st = (cudaStream_t)stream;
-    const int64_t want = (T + 7) / 8;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    const int grid = (int)(want < cap ? want : cap);
     const uint16_t *yy = static_cast<const uint16_t *>(y);
     uint16_t *oo = static_cast<uint16_t *>(out);
     const uintptr_t al = reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(out);
     if (H % 8 == 0 && (al & 15) == 0)
-        k_combine<8, 2><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+        launch_combine<8, 1>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
     else if (H % 4 == 0 && (al & 7) == 0)
-        k_combine<4, 2><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+        launch_combine<4, 2>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
     else if (H % 2 == 0 && (al & 3) == 0)
-        k_combine<2, 4><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+        launch_combine<2, 4>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
     else
-        k_combine<1, 4><<<grid, 256, 0, st>>>(yy, y_rows, H, dest, w, T, k, oo, d_status);
+        launch_combine<1, 4>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
     AP_CHECK_LAUNCH("combine launch");
     return AP_OK;
 }

@@ -39,6 +39,16 @@ int sm_count()
     return n;
 }
 
+int resident_grid(const void *kernel, int threads, size_t smem)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+    }
+    return per_sm * sm_count();
+}
+
 } // namespace ap
 
 extern "C" const char *ap_status_str(ap_status s)

@@ -9,9 +9,10 @@
 //                 offsets), counts, live = min(count, C), segment offsets;
 //   3. k_rank   - per block: warp-level stable ranks (match_any + popc over
 //                 32 pairs at a time, pairs in t-then-j order) -> dest, src_tok;
-//   4. k_copy_* - one warp per token: the row is read once and written to its
-//                 k destinations with 16-byte vectors (BF16), or quantised
-//                 once to E4M3 with a per-row scale and written k times.
+//   4. k_copy_* - BF16: one warp per (token, row chunk), the chunk read once
+//                 and written to its k destinations with 16-byte vectors;
+//                 E4M3: one warp per token, the row quantised once with a
+//                 per-row scale and written k times.
 // The ranks are deterministic: no global atomics decide any order.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -21,7 +22,7 @@
 namespace ap {
 namespace {
 
-constexpr int kTokPerBlk = 256; // tokens per count/rank block
+constexpr int kTokPerBlk = 64; // tokens per count/rank block
 constexpr int kRankThreads = 256;
 constexpr int kRankWarps = kRankThreads / kWarp;
 
@@ -43,34 +44,66 @@ __global__ void __launch_bounds__(256) k_count(const int32_t *__restrict__ idx, 
 }
 
 // One CTA of 1024 threads.  blk[b][e] -> exclusive base over b (in place).
+// Thread (e, part) owns expert e over a contiguous range of blocks: it sums
+// its range, adds the sums of the earlier parts, then rewrites its range as
+// running bases.  Then counts, live = min(count, C) and segment offsets.
 __global__ void __launch_bounds__(1024) k_scan(int32_t *__restrict__ blk, int nblk, int E, int capacity,
                                                 int padded, int32_t *__restrict__ counts,
                                                 int32_t *__restrict__ live, int32_t *__restrict__ seg_off)
 {
+    __shared__ int32_t s_tot[1024];
     __shared__ int32_t s_warp[32];
-    const int e = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int parts = blockDim.x / E; // >= 1 since E <= 1024
+    const int e = tid % E, part = tid / E;
+    const bool active = part < parts;
+    const int per = (nblk + parts - 1) / parts;
+    const int b0 = part * per;
+    const int b1 = (b0 + per < nblk) ? b0 + per : nblk;
+    int32_t sum = 0;
+    if (active) {
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
+            int32_t c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sum += c[u];
+        }
+        for (; b < b1; ++b) sum += blk[(int64_t)b * E + e];
+    }
+    s_tot[tid] = active ? sum : 0;
+    __syncthreads();
     int32_t total = 0;
-    if (e < E) {
-        int b = 0;
-        for (; b + 8 <= nblk; b += 8) {
+    if (active) {
+        int32_t run = 0;
+        for (int p = 0; p < parts; ++p) {
+            if (p == part) run = total;
+            total += s_tot[p * E + e];
+        }
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
             int32_t c[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                blk[(int64_t)(b + u) * E + e] = total;
-                total += c[u];
+                blk[(int64_t)(b + u) * E + e] = run;
+                run += c[u];
             }
         }
-        for (; b < nblk; ++b) {
+        for (; b < b1; ++b) {
             const int32_t c = blk[(int64_t)b * E + e];
-            blk[(int64_t)b * E + e] = total;
-            total += c;
+            blk[(int64_t)b * E + e] = run;
+            run += c;
         }
-        counts[e] = total;
     }
-    const int32_t l = (e < E) ? ((capacity > 0 && total > capacity) ? capacity : total) : 0;
-    if (e < E) live[e] = l;
+    // threads tid < E (part 0) own expert tid's totals
+    const int32_t l = (tid < E) ? ((capacity > 0 && total > capacity) ? capacity : total) : 0;
+    if (tid < E) {
+        counts[tid] = total;
+        live[tid] = l;
+    }
     // exclusive scan of live over experts (compact layout)
     int32_t x = l;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -92,7 +125,7 @@ __global__ void __launch_bounds__(1024) k_scan(int32_t *__restrict__ blk, int nb
     }
     __syncthreads();
     const int32_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
-    if (e < E) seg_off[e] = padded ? e * capacity : incl - l;
+    if (tid < E) seg_off[tid] = padded ? tid * capacity : incl - l;
 }
 
 // Stable ranks.  The block's pairs are split into kRankWarps contiguous
@@ -160,8 +193,10 @@ __global__ void __launch_bounds__(kRankThreads) k_rank(const int32_t *__restrict
     if (bad && d_status) atomicOr(d_status, AP_FLAG_BAD_INDEX);
 }
 
-// ---- BF16 row copy: one warp per token, row read once, written k times ------
-template <typename V>
+// ---- BF16 row copy: one warp per (token, row chunk) ---------------------------
+// The chunk of the row is read once and written to the token's k destination
+// rows.  Items are strided over all resident warps (one wave, equal shares).
+template <typename V, int U>
 __global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x, int64_t T, int64_t rb,
                                                    const int32_t *__restrict__ dest, int k,
                                                    uint8_t *__restrict__ xd)
@@ -169,27 +204,27 @@ __global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int64_t nvec = rb / (int64_t)sizeof(V);
-    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
-        const int32_t my_d = (lane < k) ? __ldcs(dest + t * k + lane) : -1;
+    const int64_t chunks = (nvec + U * kWarp - 1) / (U * kWarp);
+    const int64_t items = T * chunks;
+    for (int64_t it = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; it < items; it += warps) {
+        const int64_t t = it / chunks;
+        const int64_t base = (it - t * chunks) * U * kWarp;
+        const int32_t my_d = (lane < k) ? dest[t * k + lane] : -1;
         const V *src = reinterpret_cast<const V *>(x + t * rb);
-        constexpr int U = 4;
-        // warp-uniform loop: every lane reaches the shuffles below
-        for (int64_t base = 0; base < nvec; base += U * kWarp) {
-            V r[U];
+        V r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = base + u * kWarp + lane;
+            if (v < nvec) r[u] = ld_stream(src + v);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+            if (d < 0) continue;
+            V *dst = reinterpret_cast<V *>(xd + (int64_t)d * rb);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = base + u * kWarp + lane;
-                if (v < nvec) r[u] = ld_stream(src + v);
-            }
-            for (int j = 0; j < k; ++j) {
-                const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
-                if (d < 0) continue;
-                V *dst = reinterpret_cast<V *>(xd + (int64_t)d * rb);
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t v = base + u * kWarp + lane;
-                    if (v < nvec) dst[v] = r[u];
-                }
+                if (v < nvec) dst[v] = r[u];
             }
         }
     }
@@ -295,11 +330,23 @@ __global__ void k_cast_e4m3(const float *__restrict__ in, uint8_t *__restrict__ 
 
 int64_t nblocks(int64_t T) { return (T + kTokPerBlk - 1) / kTokPerBlk; }
 
-int copy_grid(int64_t T)
+template <typename V, int U>
+void launch_copy(const uint8_t *x, int64_t T, int64_t rb, const int32_t *dest, int k, uint8_t *xd, cudaStream_t st)
 {
-    const int64_t want = (T + 7) / 8; // 8 warps (tokens) per block
-    const int64_t cap = (int64_t)sm_count() * 8;
-    return (int)(want < cap ? want : cap);
+    static const int resident = resident_grid((const void *)k_copy_rows<V, U>, 256);
+    const int64_t nvec = rb / (int64_t)sizeof(V);
+    const int64_t items = T * ((nvec + U * kWarp - 1) / (U * kWarp));
+    const int64_t want = (items + 7) / 8; // 8 warps per block
+    k_copy_rows<V, U><<<(int)(want < resident ? want : resident), 256, 0, st>>>(x, T, rb, dest, k, xd);
+}
+
+template <int VE>
+void launch_e4m3(const uint16_t *x, int64_t T, int H, const int32_t *dest, int k, uint8_t *xd, float *xd_scale,
+                 cudaStream_t st)
+{
+    static const int resident = resident_grid((const void *)k_copy_rows_e4m3<VE>, 256);
+    const int64_t want = (T + 7) / 8; // one warp per token
+    k_copy_rows_e4m3<VE><<<(int)(want < resident ? want : resident), 256, 0, st>>>(x, T, H, dest, k, xd, xd_scale);
 }
 
 } // namespace
@@ -352,32 +399,31 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
     k_rank<<<(unsigned)nb, kRankThreads, rank_smem, st>>>(idx, T, k, E, capacity, blk, seg_off, dest, src_tok,
                                                          d_status);
     AP_CHECK_LAUNCH("dispatch rank launch");
-    const int grid = copy_grid(T);
     if (out_dtype == AP_DTYPE_BF16) {
         const int64_t rb = (int64_t)H * 2;
         const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xd) | (uintptr_t)rb;
         const uint8_t *xs = static_cast<const uint8_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         if ((al & 15) == 0)
-            k_copy_rows<int4><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+            launch_copy<int4, 2>(xs, T, rb, dest, k, xo, st);
         else if ((al & 7) == 0)
-            k_copy_rows<int2><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+            launch_copy<int2, 4>(xs, T, rb, dest, k, xo, st);
         else if ((al & 3) == 0)
-            k_copy_rows<int><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+            launch_copy<int, 4>(xs, T, rb, dest, k, xo, st);
         else
-            k_copy_rows<short><<<grid, 256, 0, st>>>(xs, T, rb, dest, k, xo);
+            launch_copy<short, 4>(xs, T, rb, dest, k, xo, st);
     } else {
         const uint16_t *xs = static_cast<const uint16_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         const uintptr_t ax = reinterpret_cast<uintptr_t>(x), ao = reinterpret_cast<uintptr_t>(xd);
         if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0)
-            k_copy_rows_e4m3<8><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+            launch_e4m3<8>(xs, T, H, dest, k, xo, xd_scale, st);
         else if (H % 4 == 0 && (ax & 7) == 0 && (ao & 3) == 0)
-            k_copy_rows_e4m3<4><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+            launch_e4m3<4>(xs, T, H, dest, k, xo, xd_scale, st);
         else if (H % 2 == 0 && (ax & 3) == 0 && (ao & 1) == 0)
-            k_copy_rows_e4m3<2><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+            launch_e4m3<2>(xs, T, H, dest, k, xo, xd_scale, st);
         else
-            k_copy_rows_e4m3<1><<<grid, 256, 0, st>>>(xs, T, H, dest, k, xo, xd_scale);
+            launch_e4m3<1>(xs, T, H, dest, k, xo, xd_scale, st);
     }
     AP_CHECK_LAUNCH("dispatch copy launch");
     return AP_OK;

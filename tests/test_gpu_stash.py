@@ -213,8 +213,8 @@ def test_max_ctas_environment(monkeypatch):
 
 
 def test_flags_device_pointer_is_the_sticky_word():
-    t = Twin(4, (16,), N=2, S=1, R=2, segs=1, SP=1)
-    t.push(0, [rows_np(1, 16, 16)], [0], [16])
+    t = Twin(4, (16,), N=2, S=1, R=2, segs=1, SP=1, maxp=8)
+    t.push(0, [rows_np(1, 16, 16)], [0], [16])  # 4 pages: 2 device, 1 spill, 1 lost
     ptr = t.g.flags_device_ptr()
     assert ptr == t.g.meta.data_ptr() + 32
     word = t.g.meta[32:36].view(torch.int32)
