@@ -39,6 +39,7 @@ SIGNATURES = {
     "ap_route_topk": (i32, [P, i64, i32, i32, P, P, P]),
     "ap_dispatch_scratch_bytes": (i32, [i64, i32, i32, P]),
     "ap_dispatch_permute": (i32, [P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P, i64, P, P]),
+    "ap_dispatch_permute_noalloc": (i32, [P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P, P]),
     "ap_combine_unpermute": (i32, [P, i64, i32, P, P, i64, i32, P, P, P]),
     "ap_pool_required_bytes": (i32, [P, P, P, P]),
     "ap_pool_init": (i32, [P, P, P, P, P, P]),

@@ -134,6 +134,40 @@ ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H,
                               void *stream);
 
 /* ============================================================================
+ * dispatch_permute_noalloc
+ *
+ * No counterpart on the pages: a convenience for callers that cannot allocate
+ * device memory.  Such callers include code running where another allocator
+ * already holds every byte of the GPU, replay or real-time loops that must not
+ * enter cudaMalloc (it can synchronise the device and takes a global lock),
+ * and embedders with a memory budget fixed at start-up.
+ *
+ * Same arguments, results and errors as ap_dispatch_permute, without the
+ * scratch arguments: the work space is a fixed array of
+ * AP_DISPATCH_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
+ * that loads the library holds until the process exits.  Sizes whose work
+ * space (ap_dispatch_scratch_bytes) exceeds it are rejected with AP_EINVAL
+ * before anything is launched.  The call allocates nothing.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  All calls share the one array, so calls that overlap on the GPU
+ * (on different streams without ordering between them) race: order them on
+ * one stream or with events.  Contents left by a previous call do not matter;
+ * every entry a call reads is first written by that call.
+ * ========================================================================== */
+#define AP_DISPATCH_NOALLOC_SCRATCH_BYTES (1 << 20)
+ap_status ap_dispatch_permute_noalloc(const void *x, int64_t T, int32_t H,
+                                      const int32_t *idx, int32_t k, int32_t E,
+                                      int32_t capacity, int32_t padded,
+                                      int32_t out_dtype, void *xd,
+                                      float *xd_scale, int64_t xd_rows,
+                                      int32_t *counts, int32_t *live,
+                                      int32_t *seg_off, int32_t *dest,
+                                      int32_t *src_tok, uint32_t *d_status,
+                                      void *stream);
+
+/* ============================================================================
  * combine_unpermute
  *
  * Top-k weighted un-permute back to a dense BF16 [T, H] output (combine with
