@@ -28,8 +28,8 @@ FLAG_BAD_INDEX = 0x10
 FLAG_CORRUPT = 0x20
 DTYPE_BF16, DTYPE_E4M3 = 0, 1
 
-__all__ = ["route_topk", "dispatch_permute", "dispatch_scratch_bytes", "combine_unpermute", "cast_e4m3", "Pool",
-           "APError", "lib"]
+__all__ = ["route_topk", "dispatch_permute", "dispatch_scratch_bytes", "combine_unpermute", "combine_backward",
+           "dispatch_backward", "cast_e4m3", "Pool", "APError", "lib"]
 
 
 def lib():
@@ -124,6 +124,39 @@ def combine_unpermute(y: torch.Tensor, dest: torch.Tensor, w: torch.Tensor, out:
     return out
 
 
+def combine_backward(dout: torch.Tensor, y: torch.Tensor, dest: torch.Tensor, w: torch.Tensor,
+                     dy: torch.Tensor | None = None, dw: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None, stream=None):
+    """dy [rows, H] bf16 (rows no pair maps to are left as given) and dw [T, k] f32."""
+    _need(dout, torch.bfloat16, "dout")
+    _need(y, torch.bfloat16, "y")
+    _need(dest, torch.int32, "dest")
+    _need(w, torch.float32, "w")
+    T, k = dest.shape
+    H = y.shape[1]
+    if dy is None:
+        dy = torch.zeros_like(y)
+    if dw is None:
+        dw = torch.empty((T, k), dtype=torch.float32, device=y.device)
+    check(lib().ap_combine_backward(_p(dout), _p(y), y.shape[0], H, _p(dest), _p(w), T, k, _p(dy), _p(dw),
+                                    _p(status), _stream(stream)), "combine_backward")
+    return dy, dw
+
+
+def dispatch_backward(dxd: torch.Tensor, dest: torch.Tensor, dx: torch.Tensor | None = None,
+                      status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dx [T, H] bf16 = sum_j dxd[dest[t, j]] (FP32 accumulation)."""
+    _need(dxd, torch.bfloat16, "dxd")
+    _need(dest, torch.int32, "dest")
+    T, k = dest.shape
+    H = dxd.shape[1]
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.bfloat16, device=dxd.device)
+    check(lib().ap_dispatch_backward(_p(dxd), dxd.shape[0], H, _p(dest), T, k, _p(dx), _p(status),
+                                     _stream(stream)), "dispatch_backward")
+    return dx
+
+
 def cast_e4m3(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     _need(x, torch.float32, "x")
     if out is None:
@@ -198,6 +231,10 @@ class Pool:
         v = ctypes.c_int32()
         check(self.lib.ap_pool_max_ctas(self.handle, ctypes.byref(v)), "pool_max_ctas")
         return v.value
+
+    @max_ctas.setter
+    def max_ctas(self, value: int):
+        check(self.lib.ap_pool_set_max_ctas(self.handle, int(value)), "pool_set_max_ctas")
 
     # -- data path ----------------------------------------------------------
     @staticmethod

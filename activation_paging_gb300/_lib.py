@@ -41,11 +41,14 @@ SIGNATURES = {
     "ap_dispatch_permute": (i32, [P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P, i64, P, P]),
     "ap_dispatch_permute_noalloc": (i32, [P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P, P]),
     "ap_combine_unpermute": (i32, [P, i64, i32, P, P, i64, i32, P, P, P]),
+    "ap_combine_backward": (i32, [P, P, i64, i32, P, P, i64, i32, P, P, P, P]),
+    "ap_dispatch_backward": (i32, [P, i64, i32, P, i64, i32, P, P, P]),
     "ap_pool_required_bytes": (i32, [P, P, P, P]),
     "ap_pool_init": (i32, [P, P, P, P, P, P]),
     "ap_pool_reset": (i32, [P, P]),
     "ap_pool_destroy": (i32, [P]),
     "ap_pool_max_ctas": (i32, [P, P]),
+    "ap_pool_set_max_ctas": (i32, [P, i32]),
     "ap_stash_push": (i32, [P, i32, i32, P, P, i64, i32, P, P, P, P]),
     "ap_stash_pop": (i32, [P, i32, i32, P, i64, P, P]),
     "ap_pool_queue_len": (i32, [P, i32, P]),

@@ -51,8 +51,9 @@ __device__ __forceinline__ typename Vec<VE>::T pack(const float *f)
 
 // Work item = (token, column chunk of U*32 lane steps); items are strided over
 // all resident warps so every warp gets the same share (no partial last wave).
-// U column steps are unrolled so that U*k row loads are in flight per lane.
-template <int VE, int U>
+// U column steps are unrolled and KB rows are gathered per batch, so U*KB row
+// loads are in flight per lane.
+template <int VE, int U, int KB>
 __global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ y, int64_t y_rows, int H,
                                                  const int32_t *__restrict__ dest, const float *__restrict__ w,
                                                  int64_t T, int k, uint16_t *__restrict__ out, uint32_t *d_status)
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ y,
         float my_w = 0.f;
         if (lane < k) {
             my_d = dest[t * k + lane];
-            my_w = w[t * k + lane];
+            my_w = w ? w[t * k + lane] : 1.0f; // no weights: the dispatch backward (unit weights)
             if (my_d >= y_rows) {
                 if (d_status && s0 == 0) atomicOr(d_status, AP_FLAG_BAD_INDEX);
                 my_d = -1;
@@ -81,23 +82,37 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ y,
         for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int i = 0; i < VE; ++i) acc[u][i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
-            const float wj = __shfl_sync(0xffffffffu, my_w, j);
-            if (d < 0) continue;
-            const V *yrow = reinterpret_cast<const V *>(y + (int64_t)d * H);
-            V v[U];
+        // KB rows per batch: every load of the batch is issued before the first
+        // add, then the adds run in j order
+        for (int j0 = 0; j0 < k; j0 += KB) {
+            int32_t d[KB];
+            float wj[KB];
+            V v[KB][U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int s = s0 + u * kWarp + lane;
-                if (s < nstep) v[u] = ld_stream(yrow + s);
+            for (int jj = 0; jj < KB; ++jj) {
+                const int j = j0 + jj;
+                d[jj] = __shfl_sync(0xffffffffu, my_d, j & (kWarp - 1));
+                wj[jj] = __shfl_sync(0xffffffffu, my_w, j & (kWarp - 1));
+                if (j >= k) d[jj] = -1;
+                if (d[jj] >= 0) {
+                    const V *yrow = reinterpret_cast<const V *>(y + (int64_t)d[jj] * H);
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int s = s0 + u * kWarp + lane;
+                        if (s < nstep) v[jj][u] = ld_stream(yrow + s);
+                    }
+                }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float f[VE];
-                unpack<VE>(v[u], f);
+            for (int jj = 0; jj < KB; ++jj) {
+                if (d[jj] < 0) continue;
 #pragma unroll
-                for (int i = 0; i < VE; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(wj, f[i]));
+                for (int u = 0; u < U; ++u) {
+                    float f[VE];
+                    unpack<VE>(v[jj][u], f);
+#pragma unroll
+                    for (int i = 0; i < VE; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(wj[jj], f[i]));
+                }
             }
         }
         uint16_t *orow = out + t * H;
@@ -113,16 +128,131 @@ template <int VE, int U>
 void launch_combine(const uint16_t *y, int64_t y_rows, int H, const int32_t *dest, const float *w, int64_t T, int k,
                     uint16_t *out, uint32_t *d_status, cudaStream_t st)
 {
-    static const int resident = resident_grid((const void *)k_combine<VE, U>, 256);
+    constexpr int KB = (VE * U >= 8) ? 8 : 4;
+    static const int resident = resident_grid((const void *)k_combine<VE, U, KB>, 256);
     const int nstep = H / VE;
     const int64_t items = T * ((nstep + U * kWarp - 1) / (U * kWarp));
     const int64_t want = (items + 7) / 8;
     const int grid = (int)(want < resident ? want : resident);
-    k_combine<VE, U><<<grid, 256, 0, st>>>(y, y_rows, H, dest, w, T, k, out, d_status);
+    k_combine<VE, U, KB><<<grid, 256, 0, st>>>(y, y_rows, H, dest, w, T, k, out, d_status);
+}
+
+// Backward of combine, one warp per token (a deterministic dot product):
+//   dy[dest(t,j)] = bf16(w[t,j] * dout[t]),  dw[t,j] = <dout[t], y[dest(t,j)]>.
+// Each lane accumulates its columns in order, then a fixed butterfly sums the
+// lanes.  dout[t] is re-read for every j from L1.
+template <int VE>
+__global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t *__restrict__ dout,
+                                                     const uint16_t *__restrict__ y, int64_t y_rows, int H,
+                                                     const int32_t *__restrict__ dest, const float *__restrict__ w,
+                                                     int64_t T, int k, uint16_t *__restrict__ dy,
+                                                     float *__restrict__ dw, uint32_t *d_status)
+{
+    using V = typename Vec<VE>::T;
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int nstep = H / VE;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        int32_t my_d = -1;
+        float my_w = 0.f;
+        if (lane < k) {
+            my_d = dest[t * k + lane];
+            my_w = w[t * k + lane];
+            if (my_d >= y_rows) {
+                if (d_status) atomicOr(d_status, AP_FLAG_BAD_INDEX);
+                my_d = -1;
+            }
+        }
+        const V *grow = reinterpret_cast<const V *>(dout + t * H);
+        for (int j = 0; j < k; ++j) {
+            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+            const float wj = __shfl_sync(0xffffffffu, my_w, j);
+            if (d < 0) {
+                if (lane == 0) dw[t * k + j] = 0.f;
+                continue;
+            }
+            const V *yrow = reinterpret_cast<const V *>(y + (int64_t)d * H);
+            V *dyrow = reinterpret_cast<V *>(dy + (int64_t)d * H);
+            float dot = 0.f;
+            for (int s = lane; s < nstep; s += kWarp) {
+                float g[VE], yv[VE], o[VE];
+                unpack<VE>(grow[s], g);
+                unpack<VE>(ld_stream(yrow + s), yv);
+#pragma unroll
+                for (int i = 0; i < VE; ++i) {
+                    o[i] = __fmul_rn(wj, g[i]);
+                    dot = fmaf(g[i], yv[i], dot);
+                }
+                st_stream(dyrow + s, pack<VE>(o));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+            if (lane == 0) dw[t * k + j] = dot;
+        }
+    }
+}
+
+template <int VE>
+void launch_combine_bwd(const uint16_t *dout, const uint16_t *y, int64_t y_rows, int H, const int32_t *dest,
+                        const float *w, int64_t T, int k, uint16_t *dy, float *dw, uint32_t *d_status,
+                        cudaStream_t st)
+{
+    static const int resident = resident_grid((const void *)k_combine_bwd<VE>, 256);
+    const int64_t want = (T + 7) / 8;
+    k_combine_bwd<VE><<<(int)(want < resident ? want : resident), 256, 0, st>>>(dout, y, y_rows, H, dest, w, T, k,
+                                                                              dy, dw, d_status);
 }
 
 } // namespace
 } // namespace ap
+
+extern "C" ap_status ap_combine_backward(const void *dout, const void *y, int64_t y_rows, int32_t H,
+                                         const int32_t *dest, const float *w, int64_t T, int32_t k, void *dy,
+                                         float *dw, uint32_t *d_status, void *stream)
+{
+    using namespace ap;
+    if (T < 0 || H < 1 || k < 1 || k > 32 || y_rows < 0)
+        return fail(AP_EINVAL, "combine_backward: bad sizes T=%lld H=%d k=%d", (long long)T, H, k);
+    if (T == 0) return AP_OK;
+    if (!dout || !dest || !w || !dw || (y_rows > 0 && (!y || !dy)))
+        return fail(AP_EINVAL, "combine_backward: NULL pointer");
+    cudaStream_t st = (cudaStream_t)stream;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(y) |
+                         reinterpret_cast<uintptr_t>(dy);
+    const uint16_t *g = static_cast<const uint16_t *>(dout);
+    const uint16_t *yy = static_cast<const uint16_t *>(y);
+    uint16_t *d = static_cast<uint16_t *>(dy);
+    if (H % 8 == 0 && (al & 15) == 0)
+        launch_combine_bwd<8>(g, yy, y_rows, H, dest, w, T, k, d, dw, d_status, st);
+    else
+        launch_combine_bwd<1>(g, yy, y_rows, H, dest, w, T, k, d, dw, d_status, st);
+    AP_CHECK_LAUNCH("combine_backward launch");
+    return AP_OK;
+}
+
+extern "C" ap_status ap_dispatch_backward(const void *dxd, int64_t rows, int32_t H, const int32_t *dest, int64_t T,
+                                          int32_t k, void *dx, uint32_t *d_status, void *stream)
+{
+    using namespace ap;
+    if (T < 0 || H < 1 || k < 1 || k > 32 || rows < 0)
+        return fail(AP_EINVAL, "dispatch_backward: bad sizes T=%lld H=%d k=%d", (long long)T, H, k);
+    if (T == 0) return AP_OK;
+    if (!dest || !dx || (!dxd && rows > 0)) return fail(AP_EINVAL, "dispatch_backward: NULL pointer");
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint16_t *yy = static_cast<const uint16_t *>(dxd);
+    uint16_t *oo = static_cast<uint16_t *>(dx);
+    const uintptr_t al = reinterpret_cast<uintptr_t>(dxd) | reinterpret_cast<uintptr_t>(dx);
+    if (H % 8 == 0 && (al & 15) == 0)
+        launch_combine<8, 1>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
+    else if (H % 4 == 0 && (al & 7) == 0)
+        launch_combine<4, 2>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
+    else if (H % 2 == 0 && (al & 3) == 0)
+        launch_combine<2, 4>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
+    else
+        launch_combine<1, 4>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
+    AP_CHECK_LAUNCH("dispatch_backward launch");
+    return AP_OK;
+}
 
 extern "C" ap_status ap_combine_unpermute(const void *y, int64_t y_rows, int32_t H, const int32_t *dest, const float *w,
                                           int64_t T, int32_t k, void *out, uint32_t *d_status, void *stream)

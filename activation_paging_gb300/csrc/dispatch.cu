@@ -9,10 +9,9 @@
 //                 offsets), counts, live = min(count, C), segment offsets;
 //   3. k_rank   - per block: warp-level stable ranks (match_any + popc over
 //                 32 pairs at a time, pairs in t-then-j order) -> dest, src_tok;
-//   4. k_copy_* - BF16: one warp per (token, row chunk), the chunk read once
-//                 and written to its k destinations with 16-byte vectors;
-//                 E4M3: one warp per token, the row quantised once with a
-//                 per-row scale and written k times.
+//   4. k_copy_* - one warp per token: the row is read once and written to its
+//                 k destinations with 16-byte vectors (BF16), or quantised
+//                 once to E4M3 with a per-row scale and written k times.
 // The ranks are deterministic: no global atomics decide any order.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -193,10 +192,8 @@ __global__ void __launch_bounds__(kRankThreads) k_rank(const int32_t *__restrict
     if (bad && d_status) atomicOr(d_status, AP_FLAG_BAD_INDEX);
 }
 
-// ---- BF16 row copy: one warp per (token, row chunk) ---------------------------
-// The chunk of the row is read once and written to the token's k destination
-// rows.  Items are strided over all resident warps (one wave, equal shares).
-template <typename V, int U>
+// ---- BF16 row copy: one warp per token, row read once, written k times ------
+template <typename V>
 __global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x, int64_t T, int64_t rb,
                                                    const int32_t *__restrict__ dest, int k,
                                                    uint8_t *__restrict__ xd)
@@ -204,27 +201,27 @@ __global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int64_t nvec = rb / (int64_t)sizeof(V);
-    const int64_t chunks = (nvec + U * kWarp - 1) / (U * kWarp);
-    const int64_t items = T * chunks;
-    for (int64_t it = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; it < items; it += warps) {
-        const int64_t t = it / chunks;
-        const int64_t base = (it - t * chunks) * U * kWarp;
-        const int32_t my_d = (lane < k) ? dest[t * k + lane] : -1;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        const int32_t my_d = (lane < k) ? __ldcs(dest + t * k + lane) : -1;
         const V *src = reinterpret_cast<const V *>(x + t * rb);
-        V r[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = base + u * kWarp + lane;
-            if (v < nvec) r[u] = ld_stream(src + v);
-        }
-        for (int j = 0; j < k; ++j) {
-            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
-            if (d < 0) continue;
-            V *dst = reinterpret_cast<V *>(xd + (int64_t)d * rb);
+        constexpr int U = 4;
+        // warp-uniform loop: every lane reaches the shuffles below
+        for (int64_t base = 0; base < nvec; base += U * kWarp) {
+            V r[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = base + u * kWarp + lane;
-                if (v < nvec) dst[v] = r[u];
+                if (v < nvec) r[u] = ld_stream(src + v);
+            }
+            for (int j = 0; j < k; ++j) {
+                const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+                if (d < 0) continue;
+                V *dst = reinterpret_cast<V *>(xd + (int64_t)d * rb);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = base + u * kWarp + lane;
+                    if (v < nvec) dst[v] = r[u];
+                }
             }
         }
     }
@@ -330,14 +327,13 @@ __global__ void k_cast_e4m3(const float *__restrict__ in, uint8_t *__restrict__ 
 
 int64_t nblocks(int64_t T) { return (T + kTokPerBlk - 1) / kTokPerBlk; }
 
-template <typename V, int U>
+template <typename V>
 void launch_copy(const uint8_t *x, int64_t T, int64_t rb, const int32_t *dest, int k, uint8_t *xd, cudaStream_t st)
 {
-    static const int resident = resident_grid((const void *)k_copy_rows<V, U>, 256);
-    const int64_t nvec = rb / (int64_t)sizeof(V);
-    const int64_t items = T * ((nvec + U * kWarp - 1) / (U * kWarp));
-    const int64_t want = (items + 7) / 8; // 8 warps per block
-    k_copy_rows<V, U><<<(int)(want < resident ? want : resident), 256, 0, st>>>(x, T, rb, dest, k, xd);
+    // one warp per token; blocks beyond the resident ones start as others retire
+    const int64_t want = (T + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    k_copy_rows<V><<<(int)(want < cap ? want : cap), 256, 0, st>>>(x, T, rb, dest, k, xd);
 }
 
 template <int VE>
@@ -405,13 +401,13 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
         const uint8_t *xs = static_cast<const uint8_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         if ((al & 15) == 0)
-            launch_copy<int4, 2>(xs, T, rb, dest, k, xo, st);
+            launch_copy<int4>(xs, T, rb, dest, k, xo, st);
         else if ((al & 7) == 0)
-            launch_copy<int2, 4>(xs, T, rb, dest, k, xo, st);
+            launch_copy<int2>(xs, T, rb, dest, k, xo, st);
         else if ((al & 3) == 0)
-            launch_copy<int, 4>(xs, T, rb, dest, k, xo, st);
+            launch_copy<int>(xs, T, rb, dest, k, xo, st);
         else
-            launch_copy<short, 4>(xs, T, rb, dest, k, xo, st);
+            launch_copy<short>(xs, T, rb, dest, k, xo, st);
     } else {
         const uint16_t *xs = static_cast<const uint16_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);

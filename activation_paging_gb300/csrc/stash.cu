@@ -248,65 +248,41 @@ struct Planes {
 
 constexpr int kCopyThreads = 256;
 
-// Metadata of one copy tile: its page's descriptor and resolved page id.
-struct TileMeta {
-    PageDesc d;
-    int64_t id;
-};
-
 __global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st, RecPtr rec,
-                                                                const int32_t *__restrict__ ring,
-                                                                const int32_t *__restrict__ spill_ring, int64_t N,
-                                                                int64_t SP, uint8_t *pool, uint8_t *spill,
-                                                                int64_t page_bytes, Planes src, int rows_per_tile,
-                                                                int tiles_per_page)
+                                                             const int32_t *__restrict__ ring,
+                                                             const int32_t *__restrict__ spill_ring, int64_t N,
+                                                             int64_t SP, uint8_t *pool, uint8_t *spill,
+                                                             int64_t page_bytes, Planes src, int rows_per_tile,
+                                                             int tiles_per_page)
 {
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
     const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
     const int64_t tiles = npages * tiles_per_page;
-    // resolve a tile's page once: ring at head0 + ordinal, then the spill ring
-    auto meta = [&](int64_t tile) {
-        TileMeta m;
-        const int64_t ord = tile / tiles_per_page;
-        m.d = rec.desc[ord];
-        m.id = -1;
-        if (ord < ndev) m.id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
-        else if (ord < ndev + nspill) m.id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
-        return m;
-    };
-    int64_t tile = blockIdx.x;
-    TileMeta cur;
-    if (tile < tiles) cur = meta(tile);
-    while (tile < tiles) {
-        const int64_t next = tile + gridDim.x;
-        TileMeta nxt;
-        if (next < tiles) nxt = meta(next); // in flight during this tile's copy
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t ord = tile / tiles_per_page;
         const int sub = (int)(tile - ord * tiles_per_page);
-        const PageDesc d = cur.d;
-        int64_t id = cur.id;
+        const PageDesc d = rec.desc[ord];
         const int64_t r0 = (int64_t)sub * rows_per_tile;
-        if (r0 < d.nrows) {
-            const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
-            const bool ok = (ord < ndev) ? (id >= 0 && id < N)
-                                         : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
-            if (!ok) {
-                if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                id = -1;
-            }
-            if (sub == 0 && threadIdx.x == 0) rec.page_table[ord] = (int32_t)id; // first tile records the page
-            if (id >= 0) {
-                uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
-#pragma unroll
-                for (int p = 0; p < 2; ++p)
-                    if (p < src.n)
-                        block_copy(page + src.page_off[p] + r0 * src.rb[p], src.p[p] + (d.row0 + r0) * src.rb[p],
-                                   nr * src.rb[p]);
-            }
+        if (r0 >= d.nrows) continue;
+        const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
+        // resolve this tile's page once
+        int64_t id = -1;
+        if (ord < ndev) id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
+        else if (ord < ndev + nspill) id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
+        const bool ok = (ord < ndev) ? (id >= 0 && id < N) : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+            id = -1;
         }
-        tile = next;
-        cur = nxt;
+        if (sub == 0 && threadIdx.x == 0) rec.page_table[ord] = (int32_t)id; // first tile records the page
+        if (id < 0) continue;
+        uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+            if (p < src.n)
+                block_copy(page + src.page_off[p] + r0 * src.rb[p], src.p[p] + (d.row0 + r0) * src.rb[p],
+                           nr * src.rb[p]);
     }
 }
 
@@ -321,61 +297,43 @@ __global__ void k_pop_plan(ap_pool_state *st, RecHdr *hdr)
 }
 
 __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st, RecPtr rec, int32_t *ring,
-                                                               int32_t *spill_ring, int64_t N, int64_t SP,
-                                                               const uint8_t *pool, const uint8_t *spill,
-                                                               int64_t page_bytes, Planes dst, int64_t dst_rows,
-                                                               int rows_per_tile, int tiles_per_page)
+                                                            int32_t *spill_ring, int64_t N, int64_t SP,
+                                                            const uint8_t *pool, const uint8_t *spill,
+                                                            int64_t page_bytes, Planes dst, int64_t dst_rows,
+                                                            int rows_per_tile, int tiles_per_page)
 {
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
     const uint64_t tail0 = rec.hdr->tail0, stail0 = rec.hdr->spill_tail0;
     const int64_t tiles = npages * tiles_per_page;
-    auto meta = [&](int64_t tile) {
-        TileMeta m;
-        const int64_t ord = tile / tiles_per_page;
-        m.d = rec.desc[ord];
-        m.id = rec.page_table[ord];
-        return m;
-    };
-    int64_t tile = blockIdx.x;
-    TileMeta cur;
-    if (tile < tiles) cur = meta(tile);
-    while (tile < tiles) {
-        const int64_t next = tile + gridDim.x;
-        TileMeta nxt;
-        if (next < tiles) nxt = meta(next); // in flight during this tile's copy
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t ord = tile / tiles_per_page;
         const int sub = (int)(tile - ord * tiles_per_page);
-        const PageDesc d = cur.d;
-        const int64_t id = cur.id;
+        const PageDesc d = rec.desc[ord];
         const int64_t r0 = (int64_t)sub * rows_per_tile;
-        if (r0 < d.nrows) {
-            const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
-            const bool ok = (ord < ndev) ? (id >= 0 && id < N)
-                                         : (ord < ndev + nspill) ? (id >= N && id < N + SP) : (id == -1);
-            if (!ok) {
-                if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-            } else {
-                if (sub == 0 && threadIdx.x == 0) { // first tile recycles the page
-                    if (ord < ndev) ring[(tail0 + (uint64_t)ord) % (uint64_t)N] = (int32_t)id;
-                    else if (id >= 0) spill_ring[(stail0 + (uint64_t)(ord - ndev)) % (uint64_t)SP] = (int32_t)(id - N);
-                }
-                if (id >= 0) {
-                    if (d.row0 + d.nrows > dst_rows) {
-                        if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
-                    } else {
-                        const uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
-#pragma unroll
-                        for (int p = 0; p < 2; ++p)
-                            if (p < dst.n)
-                                block_copy(dst.p[p] + (d.row0 + r0) * dst.rb[p], page + dst.page_off[p] + r0 * dst.rb[p],
-                                           nr * dst.rb[p]);
-                    }
-                }
-            }
+        if (r0 >= d.nrows) continue;
+        const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
+        int64_t id = rec.page_table[ord];
+        const bool ok = (ord < ndev) ? (id >= 0 && id < N) : (ord < ndev + nspill) ? (id >= N && id < N + SP) : (id == -1);
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+            continue;
         }
-        tile = next;
-        cur = nxt;
+        if (sub == 0 && threadIdx.x == 0) { // first tile recycles the page
+            if (ord < ndev) ring[(tail0 + (uint64_t)ord) % (uint64_t)N] = (int32_t)id;
+            else if (id >= 0) spill_ring[(stail0 + (uint64_t)(ord - ndev)) % (uint64_t)SP] = (int32_t)(id - N);
+        }
+        if (id < 0) continue;
+        if (d.row0 + d.nrows > dst_rows) {
+            if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
+            continue;
+        }
+        const uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+            if (p < dst.n)
+                block_copy(dst.p[p] + (d.row0 + r0) * dst.rb[p], page + dst.page_off[p] + r0 * dst.rb[p],
+                           nr * dst.rb[p]);
     }
 }
 
@@ -579,6 +537,13 @@ extern "C" ap_status ap_pool_max_ctas(const ap_pool *p, int32_t *max_ctas)
     return AP_OK;
 }
 
+extern "C" ap_status ap_pool_set_max_ctas(ap_pool *p, int32_t max_ctas)
+{
+    if (!p || max_ctas < 0) return fail(AP_EINVAL, "pool_set_max_ctas: bad argument");
+    p->max_ctas = resolve_max_ctas(max_ctas);
+    return AP_OK;
+}
+
 extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, const void *const *src_planes,
                                    const int64_t *row_bytes, int64_t src_rows, int32_t nseg,
                                    const int32_t *d_seg_off, const int32_t *d_live, uint64_t *record_id,
@@ -631,10 +596,8 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
         pl.page_off[i] = page_off[i];
     }
     pl.n = nplanes;
-    static const int resident_push = ap::resident_grid((const void *)ap::k_push_copy, ap::kCopyThreads);
     int64_t grid = bound * h.tiles_per_page;
     if (grid > p->max_ctas) grid = p->max_ctas;
-    if (grid > resident_push) grid = resident_push;
     if (grid < 1) grid = 1;
     ap::k_push_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(
         st, rec, reinterpret_cast<const int32_t *>(p->dev_meta + p->M.ring),
@@ -673,10 +636,8 @@ extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, voi
         pl.page_off[i] = page_off[i];
     }
     pl.n = nplanes;
-    static const int resident_pop = ap::resident_grid((const void *)ap::k_pop_copy, ap::kCopyThreads);
     int64_t grid = h.bound_pages * h.tiles_per_page;
     if (grid > p->max_ctas) grid = p->max_ctas;
-    if (grid > resident_pop) grid = resident_pop;
     if (grid < 1) grid = 1;
     ap::k_pop_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(
         st, rec, reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),

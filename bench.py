@@ -4,9 +4,12 @@ One step is the whole path over one batch of the Qwen3-MoE-like layer
 (T = 16384 tokens as 2 chunks of 8192, H = 2048, E = 128, top-8, dropless,
 64-token pages, pool = 1.1x the live rows): for each chunk route -> dispatch
 -> stash push; then for each chunk stash pop -> combine of the expert outputs.
-All calls go through the C ABI on one high-priority stream.  Inputs are
-seeded synthetic tensors resident in HBM; the step's working set (~1.4 GB)
-is larger than L2, so no flush is needed between steps.
+All calls go through the C ABI on one high-priority stream; the timed region
+replays one CUDA graph of the step (``--eager`` launches the calls one by one
+instead), and a second, eager pass with CUDA events around every call gives
+the per-call times behind ``ops`` and ``roofline``.  Inputs are seeded
+synthetic tensors resident in HBM; the step's working set (~1.4 GB) is larger
+than L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -43,6 +46,10 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA-graph replay")
+    ap.add_argument("--op-steps", type=int, default=100, help="eager steps with per-call events (ops, roofline)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="also measure reload (pop) overlapped with a bf16 GEMM on another stream")
     return ap.parse_args(argv)
 
 
@@ -180,7 +187,7 @@ class Step:
         self.bytes = op_bytes(wl, self.R)
         self.launches_per_step = wl.chunks * (1 + 4 + 2 + 2 + 1)
 
-    def run(self, events=None, e2e=False):
+    def run(self, events=None):
         """Enqueue one step.  events: dict op -> list of (start, end) event pairs."""
         torch, ap, wl, s = self.torch, self.ap, self.wl, self.stream
 
@@ -196,20 +203,28 @@ class Step:
             events.setdefault(name, []).append((a, b))
 
         with torch.cuda.stream(s):
-            for c, (h, d) in enumerate(self.chunks):
-                if e2e:
-                    d["logits"].copy_(h["logits"], non_blocking=True)
-                    d["x"].copy_(h["x"], non_blocking=True)
-                    d["y"].copy_(h["y"], non_blocking=True)
+            for h, d in self.chunks:
                 rec("route", lambda: ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=s))
                 rec("dispatch", lambda: ap.dispatch_permute(d["x"], d["idx"], wl.E, out=d["disp"], stream=s))
                 rec("push", lambda: self.pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"], d["disp"]["live"]))
-            for c, (h, d) in enumerate(self.chunks):
+            for h, d in self.chunks:
                 rec("pop", lambda: self.pool.pop(0, [d["dst"]]))
                 rec("combine", lambda: ap.combine_unpermute(d["y"], d["disp"]["dest"], d["w"], out=d["out"],
                                                             stream=s))
-                if e2e:
-                    h["out"].copy_(d["out"], non_blocking=True)
+
+    def upload(self):
+        """Copy every chunk's inputs from pinned host memory (on the step's stream)."""
+        with self.torch.cuda.stream(self.stream):
+            for h, d in self.chunks:
+                d["logits"].copy_(h["logits"], non_blocking=True)
+                d["x"].copy_(h["x"], non_blocking=True)
+                d["y"].copy_(h["y"], non_blocking=True)
+
+    def download(self):
+        """Copy every chunk's combined output back to pinned host memory."""
+        with self.torch.cuda.stream(self.stream):
+            for h, d in self.chunks:
+                h["out"].copy_(d["out"], non_blocking=True)
 
     def transfer_bytes(self):
         h2d = sum(h["logits"].nbytes + h["x"].nbytes + h["y"].nbytes for h, _ in self.chunks)
@@ -217,13 +232,86 @@ class Step:
         return h2d, d2h
 
 
+def overlap_report(step, device, grid_bounds=(64, 152, 608, 2048), reps=10):
+    """Exposed reload time when the pops of one step run on the high-priority
+    paging stream while a bf16 GEMM (cuBLAS, 8192 x 2304 x 8192) runs on a
+    normal-priority compute stream; the reloads are issued first and waited
+    on last (early launch, late wait).  Swept over the copy-grid bound."""
+    import torch
+    compute = torch.cuda.Stream(device=device, priority=0)
+    paging = step.stream
+    g = torch.Generator(device=device).manual_seed(0)
+    a = torch.randn((8192, 2304), device=device, dtype=torch.bfloat16, generator=g)
+    b = torch.randn((2304, 8192), device=device, dtype=torch.bfloat16, generator=g)
+    c = torch.empty((8192, 8192), device=device, dtype=torch.bfloat16)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def gemm():
+        with torch.cuda.stream(compute):
+            torch.matmul(a, b, out=c)
+
+    def push_all():
+        with torch.cuda.stream(paging):
+            for h, d in step.chunks:
+                step.pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"], d["disp"]["live"])
+
+    def pop_all():
+        with torch.cuda.stream(paging):
+            for h, d in step.chunks:
+                step.pool.pop(0, [d["dst"]])
+
+    saved = step.pool.max_ctas
+    gemm()
+    torch.cuda.synchronize(device)
+    out = {"gemm": "bf16 8192x2304 @ 2304x8192 on a normal-priority stream",
+           "reload": f"{len(step.chunks)} pops of the step on the high-priority paging stream", "by_grid_bound": {}}
+    for gb in grid_bounds:
+        step.pool.max_ctas = gb
+        t_gemm, t_pop, t_both = [], [], []
+        for _ in range(reps):
+            s0, s1 = ev(), ev()
+            s0.record(compute)
+            gemm()
+            s1.record(compute)
+            push_all()
+            torch.cuda.synchronize(device)
+            p0, p1 = ev(), ev()
+            p0.record(paging)
+            pop_all()
+            p1.record(paging)
+            push_all()
+            torch.cuda.synchronize(device)
+            b0, done, b1 = ev(), ev(), ev()
+            b0.record(compute)
+            paging.wait_event(b0)
+            pop_all()              # early launch of the reloads
+            done.record(paging)
+            gemm()
+            compute.wait_event(done)  # late wait
+            b1.record(compute)
+            torch.cuda.synchronize(device)
+            t_gemm.append(s0.elapsed_time(s1))
+            t_pop.append(p0.elapsed_time(p1))
+            t_both.append(b0.elapsed_time(b1))
+        mg, mp, mb = (statistics.median(v) for v in (t_gemm, t_pop, t_both))
+        out["by_grid_bound"][str(gb)] = {"gemm_ms": round(mg, 4), "reload_ms": round(mp, 4),
+                                         "both_ms": round(mb, 4), "exposed_ms": round(mb - mg, 4),
+                                         "hidden_frac": round(1 - (mb - mg) / mp, 3) if mp > 0 else None}
+    step.pool.max_ctas = saved
+    torch.cuda.synchronize(device)
+    return out
+
+
 def kernel_hash() -> str:
-    path = os.path.join(ROOT, "activation_paging_gb300", "csrc", "stash.cu")
-    common = os.path.join(ROOT, "activation_paging_gb300", "csrc", "ap_common.cuh")
-    h = hashlib.sha256()
-    for p in (path, common):
-        h.update(open(p, "rb").read())
-    return h.hexdigest()[:16]
+    """Hash of the stash copy kernels' device source (their kernels and the
+    shared device copy helper), so recorded ncu traffic is used only while
+    the kernels it was taken from are unchanged."""
+    csrc = os.path.join(ROOT, "activation_paging_gb300", "csrc")
+    stash = open(os.path.join(csrc, "stash.cu")).read()
+    common = open(os.path.join(csrc, "ap_common.cuh")).read()
+    dev = stash[stash.index("// ---- kernels"):stash.index("// ---- host runtime")]
+    dev += common[common.index("// ---- device helpers"):]
+    return hashlib.sha256(dev.encode()).hexdigest()[:16]
 
 
 def measured_peaks():
@@ -252,8 +340,26 @@ def native(args):
         step.run()
     torch.cuda.synchronize(device)
 
-    # timed region: K steps, events around every call on the launching stream
-    events = {}
+    # one step captured as a CUDA graph: live counts, offsets and pages stay on
+    # the device, so every replay re-routes from the current inputs
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=step.stream):
+            step.run()
+        for _ in range(3):
+            with torch.cuda.stream(step.stream):
+                graph.replay()
+        torch.cuda.synchronize(device)
+
+    def one_step(events=None):
+        if graph is not None and events is None:
+            with torch.cuda.stream(step.stream):
+                graph.replay()
+        else:
+            step.run(events)
+
+    # timed region: K steps, bracketed by events on the launching stream
     sampler = ClockSampler(local)
     time.sleep(0.3)
     barrier(world)
@@ -262,7 +368,7 @@ def native(args):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(step.stream)
     for _ in range(args.steps):
-        step.run(events)
+        one_step()
     t1.record(step.stream)
     torch.cuda.synchronize(device)
     barrier(world)
@@ -270,6 +376,13 @@ def native(args):
     elapsed = t0.elapsed_time(t1) / 1e3
     max_elapsed = aggregate_max(elapsed, world)
     value = whole_job_rate(tokens_per_step * args.steps, world, max_elapsed)
+
+    # per-call times: eager steps with CUDA events around every call
+    events = {}
+    op_steps = max(1, min(args.op_steps, args.steps))
+    for _ in range(op_steps):
+        step.run(events)
+    torch.cuda.synchronize(device)
 
     per_op = {}
     for name, pairs in events.items():
@@ -293,20 +406,28 @@ def native(args):
         pass
     roofline = {"bound": "hbm", "kernel": dom, "achieved": ops[dom]["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": ops[dom]["frac"], "traffic": traffic, "peak_source": peak_src,
-                "note": "achieved = algorithmic bytes per launch / CUDA-event time of the call on its stream"}
+                "note": (f"achieved = algorithmic bytes per launch / mean CUDA-event time of the call on its stream "
+                         f"over {op_steps} eager steps (the call includes its small plan kernel)")}
 
     e2e = None
     if not args.no_e2e:
+        # the public path end to end: pinned host inputs in, step, output back
         h2d, d2h = step.transfer_bytes()
+
+        def e2e_step():
+            step.upload()
+            one_step()
+            step.download()
+
         for _ in range(2):
-            step.run(e2e=True)
+            e2e_step()
         torch.cuda.synchronize(device)
         barrier(world)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(step.stream)
         for _ in range(args.e2e_steps):
-            step.run(e2e=True)
+            e2e_step()
         b.record(step.stream)
         torch.cuda.synchronize(device)
         barrier(world)
@@ -314,6 +435,8 @@ def native(args):
         e2e = {"value": round(whole_job_rate(tokens_per_step * args.e2e_steps, world, e_el), 1),
                "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps, "ms_per_step": round(e_el * 1e3 / args.e2e_steps, 4)}
+
+    overlap = overlap_report(step, device) if args.overlap else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -329,8 +452,9 @@ def native(args):
                            "tokens_per_step": tokens_per_step, "bytes_per_step": total_bytes,
                            "hbm_gbs_step": round(total_bytes / (ms_per_step / 1e3) / 1e9, 1),
                            "l2": "working set per step ~1.4 GB > 126 MB L2: no flush",
-                           "parallelism": f"replicas x{world}", "stream": "one high-priority stream"},
-                "roofline": roofline, "ops": ops, "cpu_baseline": cpu, "e2e": e2e,
+                           "parallelism": f"replicas x{world}", "stream": "one high-priority stream",
+                           "launch": "eager" if graph is None else "CUDA graph of one step, replayed"},
+                "roofline": roofline, "ops": ops, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
                 "gpu_launches": step.launches_per_step * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -190,6 +190,34 @@ ap_status ap_combine_unpermute(const void *y, int64_t y_rows, int32_t H,
                                void *stream);
 
 /* ============================================================================
+ * Backward of combine and of dispatch (the backward primitives of the token
+ * movement: Megatron-LM pull 7342, "Summary").  The pages give no formulas;
+ * these are the derivatives of the forward definitions above.
+ *
+ * ap_combine_backward: for every kept pair (t, j) with row r = dest[t, j]:
+ *   dy[r]   = bf16_round_nearest_even(w[t, j] * dout[t])  (one float multiply)
+ *   dw[t,j] = sum_h dout[t, h] * y[r, h]   (float32; per-lane partial sums in
+ *             column order, then a fixed butterfly over the 32 lanes)
+ * A dropped pair gets dw = 0.  Rows of dy that no pair maps to are not
+ * written.  A row index >= y_rows is skipped (dw = 0) and sets
+ * AP_FLAG_BAD_INDEX in *d_status (may be NULL).
+ *   dout [T, H] bf16, y [y_rows, H] bf16, dest/w [T, k] (device, read)
+ *   dy [y_rows, H] bf16, dw [T, k] float32 (device, written)
+ *
+ * ap_dispatch_backward: dx[t] = bf16(sum_j dxd[dest[t, j]]) with a float32
+ * accumulator, j ascending, dropped pairs skipped (the combine with unit
+ * weights).  dxd [rows, H] bf16, dest [T, k], dx [T, H] bf16 (device).
+ * Limits of both: H >= 1, 1 <= k <= 32.
+ * ========================================================================== */
+ap_status ap_combine_backward(const void *dout, const void *y, int64_t y_rows,
+                              int32_t H, const int32_t *dest, const float *w,
+                              int64_t T, int32_t k, void *dy, float *dw,
+                              uint32_t *d_status, void *stream);
+ap_status ap_dispatch_backward(const void *dxd, int64_t rows, int32_t H,
+                               const int32_t *dest, int64_t T, int32_t k,
+                               void *dx, uint32_t *d_status, void *stream);
+
+/* ============================================================================
  * Paged activation stash (torchtitan pull 5541, "AI-Generated Details":
  * binding live counts to sources, one high-priority paging stream that
  * serialises free-list changes, FIFO records per slot, page-aligned
@@ -275,6 +303,11 @@ ap_status ap_pool_reset(ap_pool *pool, void *stream);
 ap_status ap_pool_destroy(ap_pool *pool);
 /* Resolved copy-grid bound of the pool (max_ctas after the environment). */
 ap_status ap_pool_max_ctas(const ap_pool *pool, int32_t *max_ctas);
+/* Change the copy-grid bound for later pushes and pops (>= 1; 0 re-reads the
+ * environment / default).  Like the bound itself, it changes neither the
+ * capacity nor the rows copied, only how many CTAs the copy kernels occupy,
+ * and so how much of the GPU stays free for concurrent compute. */
+ap_status ap_pool_set_max_ctas(ap_pool *pool, int32_t max_ctas);
 
 /* Push one record into `slot`.
  *   nplanes      1 or 2

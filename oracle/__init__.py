@@ -71,6 +71,8 @@ def _load():
             "or_quantize_rows_e4m3": (None, [P, i64, i32, P, P]),
             "or_permute_rows_fp8": (None, [P, P, i64, i32, P, i32, P, P]),
             "or_combine": (None, [P, i64, i32, P, P, i64, i32, P, P]),
+            "or_combine_backward": (None, [P, P, i64, i32, P, P, i64, i32, P, P, P]),
+            "or_dispatch_backward": (None, [P, i64, i32, P, i64, i32, P, P]),
             "or_pool_new": (P, [i32, i64, i64, i32, i32, i32, i64, i64, i32, u8]),
             "or_pool_free": (None, [P]),
             "or_pool_reset": (None, [P]),
@@ -204,6 +206,35 @@ def combine(y_bf16: np.ndarray, dest: np.ndarray, w: np.ndarray):
     status = np.zeros(1, np.uint32)
     _load().or_combine(_ptr(y), y.shape[0], H, _ptr(dest), _ptr(w), T, k, _ptr(out), _ptr(status))
     return out, int(status[0])
+
+
+def combine_backward(dout_bf16: np.ndarray, y_bf16: np.ndarray, dest: np.ndarray, w: np.ndarray,
+                     dy_fill: int = 0xA5):
+    """dy rows (BF16(w * dout), canary elsewhere), dw [T, k] f32 and status."""
+    dout = np.ascontiguousarray(dout_bf16, dtype=np.uint16)
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    dest = np.ascontiguousarray(dest, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    T, k = dest.shape
+    H = y.shape[1]
+    dy = np.frombuffer(np.full(y.size * 2, dy_fill, np.uint8).tobytes(), np.uint16).reshape(y.shape).copy()
+    dw = np.empty((T, k), np.float32)
+    status = np.zeros(1, np.uint32)
+    _load().or_combine_backward(_ptr(dout), _ptr(y), y.shape[0], H, _ptr(dest), _ptr(w), T, k, _ptr(dy), _ptr(dw),
+                                _ptr(status))
+    return dy, dw, int(status[0])
+
+
+def dispatch_backward(dxd_bf16: np.ndarray, dest: np.ndarray):
+    """dx[t] = BF16(sum_j dxd[dest[t, j]]) with single-precision accumulation."""
+    dxd = np.ascontiguousarray(dxd_bf16, dtype=np.uint16)
+    dest = np.ascontiguousarray(dest, dtype=np.int32)
+    T, k = dest.shape
+    H = dxd.shape[1]
+    dx = np.empty((T, H), np.uint16)
+    status = np.zeros(1, np.uint32)
+    _load().or_dispatch_backward(_ptr(dxd), dxd.shape[0], H, _ptr(dest), T, k, _ptr(dx), _ptr(status))
+    return dx, int(status[0])
 
 
 def dispatch(x_bf16: np.ndarray, idx: np.ndarray, E: int, capacity: int, padded: bool,

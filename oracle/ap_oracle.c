@@ -357,6 +357,70 @@ void or_combine(const uint16_t *y, int64_t y_rows, int32_t H,
 }
 
 /* ------------------------------------------------------------------------- */
+/* (7) Backward of combine and of dispatch.                                   */
+/*   [MG7342] "Summary": forward, backward and fused forward/backward         */
+/*   primitives of the token movement.  The pages give no formulas; these are */
+/*   the derivatives of the forward definitions above:                        */
+/*     out[t] = sum_j w[t,j] * y[dest(t,j)]   and   xd[dest(t,j)] = x[t].     */
+/*   Combine backward: dy[dest(t,j)] = BF16(w[t,j] * dout[t]) (one single     */
+/*   multiply, nearest-even), dw[t,j] = <dout[t], y[dest(t,j)]> summed in     */
+/*   double and rounded once to single; a dropped pair gets dw = 0 and        */
+/*   writes no row.  Dispatch backward: dx[t] = BF16(sum_j dxd[dest(t,j)])    */
+/*   with a single-precision accumulator, j ascending (the combine with unit  */
+/*   weights).                                                                */
+/* ------------------------------------------------------------------------- */
+void or_combine_backward(const uint16_t *dout, const uint16_t *y, int64_t y_rows,
+                         int32_t H, const int32_t *dest, const float *w,
+                         int64_t T, int32_t k, uint16_t *dy, float *dw,
+                         uint32_t *status)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t r = dest[t * k + j];
+            dw[t * k + j] = 0.0f;
+            if (r < 0)
+                continue;
+            if (r >= y_rows) {
+                if (status)
+                    *status |= OR_FLAG_BAD_INDEX;
+                continue;
+            }
+            double dot = 0.0;
+            for (int32_t h = 0; h < H; ++h) {
+                float g = or_bf16_to_f32(dout[t * H + h]);
+                float prod = w[t * k + j] * g;
+                dy[(int64_t)r * H + h] = or_f32_to_bf16(prod);
+                dot += (double)g * (double)or_bf16_to_f32(y[(int64_t)r * H + h]);
+            }
+            dw[t * k + j] = (float)dot;
+        }
+    }
+}
+
+void or_dispatch_backward(const uint16_t *dxd, int64_t rows, int32_t H,
+                          const int32_t *dest, int64_t T, int32_t k, uint16_t *dx,
+                          uint32_t *status)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int32_t j = 0; j < k; ++j) {
+                int32_t r = dest[t * k + j];
+                if (r < 0)
+                    continue;
+                if (r >= rows) {
+                    if (status)
+                        *status |= OR_FLAG_BAD_INDEX;
+                    continue;
+                }
+                acc = acc + or_bf16_to_f32(dxd[(int64_t)r * H + h]);
+            }
+            dx[t * H + h] = or_f32_to_bf16(acc);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* (4)-(5) Paged stash: fixed page pool, free list, spill, per-slot FIFO.     */
 /*   [TT5541] "AI-Generated Details": one high-priority paging stream         */
 /*   serialises free-list changes; per-slot records stay FIFO; copy loops in  */

@@ -209,7 +209,12 @@ def test_max_ctas_environment(monkeypatch):
     assert pool.max_ctas == 37
     monkeypatch.delenv("AP_STASH_MAX_CTAS")
     assert ap.Pool(4, 64, 8).max_ctas == 2048
-    assert ap.Pool(4, 64, 8, max_ctas=5).max_ctas == 5
+    p5 = ap.Pool(4, 64, 8, max_ctas=5)
+    assert p5.max_ctas == 5
+    p5.max_ctas = 64
+    assert p5.max_ctas == 64
+    p5.max_ctas = 0
+    assert p5.max_ctas == 2048
 
 
 def test_flags_device_pointer_is_the_sticky_word():
