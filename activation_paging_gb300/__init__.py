@@ -271,6 +271,37 @@ class Pool:
                                      ctypes.byref(rid), self.stream.cuda_stream), "stash_push")
         return rid.value
 
+    def dispatch_stash(self, slot: int, x: torch.Tensor, idx: torch.Tensor, E: int, capacity: int = 0,
+                       padded: bool = False, out: dict | None = None, status: torch.Tensor | None = None):
+        """Fused dispatch (BF16) + push into ``slot``: returns the dispatch
+        dict (as ``dispatch_permute``) with the record id under ``record_id``."""
+        _need(x, torch.bfloat16, "x")
+        _need(idx, torch.int32, "idx")
+        T, H = x.shape
+        k = idx.shape[1]
+        dev = x.device
+        rows = E * capacity if padded else T * k
+        o = dict(out) if out is not None else {}
+        if "xd" not in o:
+            o["xd"] = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        for name, shape in (("counts", (E,)), ("live", (E,)), ("seg_off", (E,)), ("dest", (T, k))):
+            if name not in o:
+                o[name] = torch.empty(shape, dtype=torch.int32, device=dev)
+        if "src_tok" not in o:
+            o["src_tok"] = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+        sb = dispatch_scratch_bytes(T, k, E)
+        if "scratch" not in o or o["scratch"].numel() < sb:
+            o["scratch"] = torch.empty(sb, dtype=torch.uint8, device=dev)
+        self._order_after_caller([x, idx, status] + [v for v in o.values() if isinstance(v, torch.Tensor)])
+        rid = ctypes.c_uint64()
+        xd = o["xd"]
+        check(self.lib.ap_dispatch_stash(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity, int(padded), _p(xd),
+                                         xd.shape[0], _p(o["counts"]), _p(o["live"]), _p(o["seg_off"]),
+                                         _p(o["dest"]), _p(o["src_tok"]), _p(o["scratch"]), o["scratch"].numel(),
+                                         _p(status), ctypes.byref(rid), self.stream.cuda_stream), "dispatch_stash")
+        o["record_id"] = rid.value
+        return o
+
     def pop(self, slot: int, planes) -> int:
         """Reload the slot's oldest record into ``planes`` (same rows as pushed).
 

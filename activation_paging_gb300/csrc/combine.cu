@@ -52,9 +52,11 @@ __device__ __forceinline__ typename Vec<VE>::T pack(const float *f)
 // Work item = (token, column chunk of U*32 lane steps); items are strided over
 // all resident warps so every warp gets the same share (no partial last wave).
 // U column steps are unrolled and KB rows are gathered per batch, so U*KB row
-// loads are in flight per lane.
+// loads are in flight per lane; each warp reads U*32*16 contiguous bytes of a
+// row (1 KB for BF16 rows with U = 2), which a sweep on GB300 found faster
+// than narrower pieces or deeper batches with fewer resident warps.
 template <int VE, int U, int KB>
-__global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ y, int64_t y_rows, int H,
+__global__ void __launch_bounds__(256, 4) k_combine(const uint16_t *__restrict__ y, int64_t y_rows, int H,
                                                  const int32_t *__restrict__ dest, const float *__restrict__ w,
                                                  int64_t T, int k, uint16_t *__restrict__ out, uint32_t *d_status)
 {
@@ -128,7 +130,7 @@ template <int VE, int U>
 void launch_combine(const uint16_t *y, int64_t y_rows, int H, const int32_t *dest, const float *w, int64_t T, int k,
                     uint16_t *out, uint32_t *d_status, cudaStream_t st)
 {
-    constexpr int KB = (VE * U >= 8) ? 8 : 4;
+    constexpr int KB = 2;
     static const int resident = resident_grid((const void *)k_combine<VE, U, KB>, 256);
     const int nstep = H / VE;
     const int64_t items = T * ((nstep + U * kWarp - 1) / (U * kWarp));
@@ -243,9 +245,9 @@ extern "C" ap_status ap_dispatch_backward(const void *dxd, int64_t rows, int32_t
     uint16_t *oo = static_cast<uint16_t *>(dx);
     const uintptr_t al = reinterpret_cast<uintptr_t>(dxd) | reinterpret_cast<uintptr_t>(dx);
     if (H % 8 == 0 && (al & 15) == 0)
-        launch_combine<8, 1>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
+        launch_combine<8, 2>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
     else if (H % 4 == 0 && (al & 7) == 0)
-        launch_combine<4, 2>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
+        launch_combine<4, 4>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
     else if (H % 2 == 0 && (al & 3) == 0)
         launch_combine<2, 4>(yy, rows, H, dest, nullptr, T, k, oo, d_status, st);
     else
@@ -267,9 +269,9 @@ extern "C" ap_status ap_combine_unpermute(const void *y, int64_t y_rows, int32_t
     uint16_t *oo = static_cast<uint16_t *>(out);
     const uintptr_t al = reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(out);
     if (H % 8 == 0 && (al & 15) == 0)
-        launch_combine<8, 1>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
+        launch_combine<8, 2>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
     else if (H % 4 == 0 && (al & 7) == 0)
-        launch_combine<4, 2>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
+        launch_combine<4, 4>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
     else if (H % 2 == 0 && (al & 3) == 0)
         launch_combine<2, 4>(yy, y_rows, H, dest, w, T, k, oo, d_status, st);
     else

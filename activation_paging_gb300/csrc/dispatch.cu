@@ -357,31 +357,33 @@ extern "C" ap_status ap_dispatch_scratch_bytes(int64_t T, int32_t k, int32_t E, 
     return AP_OK;
 }
 
-extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, const int32_t *idx, int32_t k,
-                                         int32_t E, int32_t capacity, int32_t padded, int32_t out_dtype, void *xd,
-                                         float *xd_scale, int64_t xd_rows, int32_t *counts, int32_t *live,
-                                         int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
-                                         int64_t scratch_bytes, uint32_t *d_status, void *stream)
+namespace ap {
+
+ap_status dispatch_check(const char *who, const void *x, int64_t T, int32_t H, const int32_t *idx, int32_t k,
+                         int32_t E, int32_t capacity, int32_t padded, const void *xd, int64_t xd_rows,
+                         const int32_t *counts, const int32_t *live, const int32_t *seg_off, const int32_t *dest,
+                         const void *scratch, int64_t scratch_bytes)
 {
-    using namespace ap;
     if (T < 0 || H < 1 || k < 1 || k > 32 || E < 1 || E > 1024 || T * (int64_t)k >= (int64_t(1) << 31))
-        return fail(AP_EINVAL, "dispatch_permute: bad sizes T=%lld H=%d k=%d E=%d", (long long)T, H, k, E);
-    if (padded && capacity <= 0) return fail(AP_EINVAL, "dispatch_permute: padded layout needs capacity > 0");
-    if (out_dtype != AP_DTYPE_BF16 && out_dtype != AP_DTYPE_E4M3)
-        return fail(AP_EINVAL, "dispatch_permute: unknown out_dtype %d", out_dtype);
+        return fail(AP_EINVAL, "%s: bad sizes T=%lld H=%d k=%d E=%d", who, (long long)T, H, k, E);
+    if (padded && capacity <= 0) return fail(AP_EINVAL, "%s: padded layout needs capacity > 0", who);
     const int64_t need_rows = padded ? (int64_t)E * capacity : T * (int64_t)k;
     if (xd_rows < need_rows)
-        return fail(AP_EINVAL, "dispatch_permute: xd_rows %lld < %lld", (long long)xd_rows, (long long)need_rows);
+        return fail(AP_EINVAL, "%s: xd_rows %lld < %lld", who, (long long)xd_rows, (long long)need_rows);
     int64_t need_scratch = 0;
     ap_dispatch_scratch_bytes(T, k, E, &need_scratch);
     if (scratch_bytes < need_scratch)
-        return fail(AP_EINVAL, "dispatch_permute: scratch %lld < %lld bytes", (long long)scratch_bytes,
+        return fail(AP_EINVAL, "%s: scratch %lld < %lld bytes", who, (long long)scratch_bytes,
                     (long long)need_scratch);
     if (!counts || !live || !seg_off || !scratch || (T > 0 && (!x || !idx || !dest || !xd)))
-        return fail(AP_EINVAL, "dispatch_permute: NULL pointer");
-    if (out_dtype == AP_DTYPE_E4M3 && T > 0 && !xd_scale)
-        return fail(AP_EINVAL, "dispatch_permute: E4M3 needs xd_scale");
-    cudaStream_t st = (cudaStream_t)stream;
+        return fail(AP_EINVAL, "%s: NULL pointer", who);
+    return AP_OK;
+}
+
+ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
+                            int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, int32_t *src_tok,
+                            void *scratch, uint32_t *d_status, cudaStream_t st)
+{
     int32_t *blk = static_cast<int32_t *>(scratch);
     const int64_t nb = nblocks(T);
     if (nb > 0) {
@@ -395,6 +397,28 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
     k_rank<<<(unsigned)nb, kRankThreads, rank_smem, st>>>(idx, T, k, E, capacity, blk, seg_off, dest, src_tok,
                                                          d_status);
     AP_CHECK_LAUNCH("dispatch rank launch");
+    return AP_OK;
+}
+
+} // namespace ap
+
+extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, const int32_t *idx, int32_t k,
+                                         int32_t E, int32_t capacity, int32_t padded, int32_t out_dtype, void *xd,
+                                         float *xd_scale, int64_t xd_rows, int32_t *counts, int32_t *live,
+                                         int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
+                                         int64_t scratch_bytes, uint32_t *d_status, void *stream)
+{
+    using namespace ap;
+    if (out_dtype != AP_DTYPE_BF16 && out_dtype != AP_DTYPE_E4M3)
+        return fail(AP_EINVAL, "dispatch_permute: unknown out_dtype %d", out_dtype);
+    ap_status s = dispatch_check("dispatch_permute", x, T, H, idx, k, E, capacity, padded, xd, xd_rows, counts, live,
+                                 seg_off, dest, scratch, scratch_bytes);
+    if (s != AP_OK) return s;
+    if (out_dtype == AP_DTYPE_E4M3 && T > 0 && !xd_scale)
+        return fail(AP_EINVAL, "dispatch_permute: E4M3 needs xd_scale");
+    cudaStream_t st = (cudaStream_t)stream;
+    s = dispatch_metadata(T, idx, k, E, capacity, padded, counts, live, seg_off, dest, src_tok, scratch, d_status, st);
+    if (s != AP_OK || T == 0) return s;
     if (out_dtype == AP_DTYPE_BF16) {
         const int64_t rb = (int64_t)H * 2;
         const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xd) | (uintptr_t)rb;

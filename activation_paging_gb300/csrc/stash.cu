@@ -337,6 +337,86 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
     }
 }
 
+// Fused dispatch + push: one warp per token reads its BF16 row once and writes
+// it both to the dispatch buffer row dest(t, j) and, for a kept pair, to row
+// (rank mod P) of page pg_base[e] + rank / P of the record (rank = the pair's
+// row within its expert segment).  The pair that holds row 0 of a page records
+// the page.  Same bytes, page table and flags as a dispatch followed by a push.
+template <typename V>
+__global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__restrict__ x, int64_t T, int64_t rb,
+                                                             const int32_t *__restrict__ idx,
+                                                             const int32_t *__restrict__ dest, int k, int E,
+                                                             uint8_t *__restrict__ xd, ap_pool_state *st, RecPtr rec,
+                                                             const int32_t *__restrict__ ring,
+                                                             const int32_t *__restrict__ spill_ring, int64_t N,
+                                                             int64_t SP, uint8_t *pool, uint8_t *spill,
+                                                             int64_t page_bytes, int P)
+{
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int64_t nvec = rb / (int64_t)sizeof(V);
+    const int64_t npages = rec.hdr->npages;
+    const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
+    const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        int32_t my_d = -1;
+        uint8_t *my_page = nullptr; // where this lane's pair lands in the pool (row start), or null
+        if (lane < k) {
+            my_d = dest[t * k + lane];
+            const int e = idx[t * k + lane];
+            if (my_d >= 0 && e >= 0 && e < E) {
+                const int64_t r = (int64_t)my_d - rec.seg_off[e]; // row within the expert segment
+                if (r >= 0 && r < rec.live[e]) {
+                    const int64_t ord = rec.pg_base[e] + r / P;
+                    if (ord < npages) {
+                        int64_t id = -1;
+                        if (ord < ndev) id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
+                        else if (ord < ndev + nspill)
+                            id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
+                        const bool ok = (ord < ndev) ? (id >= 0 && id < N)
+                                                     : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
+                        if (!ok) {
+                            atomicOr(&st->flags, AP_FLAG_CORRUPT);
+                            id = -1;
+                        }
+                        if (r % P == 0) rec.page_table[ord] = (int32_t)id; // row 0 of the page records it
+                        if (id >= 0) {
+                            uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+                            my_page = page + (r % P) * rb;
+                        }
+                    }
+                }
+            }
+        }
+        const V *src = reinterpret_cast<const V *>(x + t * rb);
+        constexpr int U = 4;
+        for (int64_t base = 0; base < nvec; base += U * kWarp) { // warp-uniform
+            V r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = base + u * kWarp + lane;
+                if (v < nvec) r[u] = ld_stream(src + v);
+            }
+            for (int j = 0; j < k; ++j) {
+                const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+                const unsigned long long pg =
+                    __shfl_sync(0xffffffffu, (unsigned long long)reinterpret_cast<uintptr_t>(my_page), j);
+                if (d < 0) continue;
+                V *dst = reinterpret_cast<V *>(xd + (int64_t)d * rb);
+                V *pdst = reinterpret_cast<V *>(static_cast<uintptr_t>(pg));
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = base + u * kWarp + lane;
+                    if (v < nvec) {
+                        dst[v] = r[u];
+                        if (pdst) st_stream(pdst + v, r[u]);
+                    }
+                }
+            }
+        }
+    }
+}
+
 } // namespace
 } // namespace ap
 
@@ -604,6 +684,84 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
         reinterpret_cast<const int32_t *>(p->dev_meta + p->M.spill_ring), p->cfg.num_pages, p->cfg.spill_pages,
         p->dev_pool, p->spill_dev, p->cfg.page_bytes, pl, h.rows_per_tile, h.tiles_per_page);
     AP_CHECK_LAUNCH("stash push copy launch");
+    p->next_id += 1;
+    p->q_count[slot] += 1;
+    if (record_id) *record_id = h.id;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, int64_t T, int32_t H,
+                                       const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
+                                       void *xd, int64_t xd_rows, int32_t *counts, int32_t *live, int32_t *seg_off,
+                                       int32_t *dest, int32_t *src_tok, void *scratch, int64_t scratch_bytes,
+                                       uint32_t *d_status, uint64_t *record_id, void *stream)
+{
+    using namespace ap;
+    if (!p) return fail(AP_EINVAL, "dispatch_stash: NULL pool");
+    if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "dispatch_stash: not the paging stream");
+    if (slot < 0 || slot >= p->cfg.num_slots) return fail(AP_EINVAL, "dispatch_stash: slot %d out of range", slot);
+    ap_status s = dispatch_check("dispatch_stash", x, T, H, idx, k, E, capacity, padded, xd, xd_rows, counts, live,
+                                 seg_off, dest, scratch, scratch_bytes);
+    if (s != AP_OK) return s;
+    if (E > p->cfg.max_segments)
+        return fail(AP_EINVAL, "dispatch_stash: E=%d segments > max_segments %d", E, p->cfg.max_segments);
+    int64_t rb[2] = {(int64_t)H * 2, 0};
+    int64_t page_off[2];
+    if (!plane_fit(p, 1, rb, page_off)) return fail(AP_EINVAL, "dispatch_stash: a BF16 row of H=%d does not fit", H);
+    if (p->q_count[slot] >= p->cfg.max_records_per_slot)
+        return fail(AP_EQFULL, "dispatch_stash: slot %d queue full", slot);
+    const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xd) |
+                         reinterpret_cast<uintptr_t>(p->dev_pool) | reinterpret_cast<uintptr_t>(p->spill_dev) |
+                         (uintptr_t)rb[0] | (uintptr_t)p->cfg.page_bytes;
+    if (T > 0 && (al & 15) != 0 && (al & 7) != 0)
+        return fail(AP_ENOTSUP, "dispatch_stash: rows must be 8-byte aligned (H %% 4 == 0)");
+    cudaStream_t st = p->stream;
+    s = dispatch_metadata(T, idx, k, E, capacity, padded, counts, live, seg_off, dest, src_tok, scratch, d_status, st);
+    if (s != AP_OK) return s;
+
+    const int32_t pos = (p->q_head[slot] + p->q_count[slot]) % p->cfg.max_records_per_slot;
+    const int64_t index = (int64_t)slot * p->cfg.max_records_per_slot + pos;
+    HostRec &h = p->q[index];
+    h.id = p->next_id;
+    h.index = index;
+    h.nplanes = 1;
+    h.rb[0] = rb[0];
+    h.rb[1] = 0;
+    const int64_t P = p->cfg.page_tokens;
+    int64_t rpt = 32768 / rb[0];
+    if (rpt < 1) rpt = 1;
+    if (rpt > P) rpt = P;
+    h.rows_per_tile = (int32_t)rpt;
+    h.tiles_per_page = (int32_t)((P + rpt - 1) / rpt);
+    int64_t bound = E + (xd_rows + P - 1) / P;
+    if (bound > p->cfg.max_pages_per_record) bound = p->cfg.max_pages_per_record;
+    h.bound_pages = bound;
+    ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
+    ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
+    ap::k_push_plan<<<1, ap::kPlanThreads, 0, st>>>(stt, rec, E, seg_off, live, xd_rows, p->cfg.page_tokens,
+                                                    p->cfg.max_pages_per_record, p->cfg.num_pages,
+                                                    p->cfg.spill_pages);
+    AP_CHECK_LAUNCH("dispatch_stash plan launch");
+    if (T > 0) {
+        const int64_t want = (T + 7) / 8;
+        const int64_t cap = (int64_t)sm_count() * 16;
+        const int grid = (int)(want < cap ? want : cap);
+        const int32_t *ring = reinterpret_cast<const int32_t *>(p->dev_meta + p->M.ring);
+        const int32_t *sring = reinterpret_cast<const int32_t *>(p->dev_meta + p->M.spill_ring);
+        const uint8_t *xs = static_cast<const uint8_t *>(x);
+        uint8_t *xo = static_cast<uint8_t *>(xd);
+        if ((al & 15) == 0)
+            ap::k_dispatch_stash_copy<int4><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, xo, stt, rec, ring,
+                                                                  sring, p->cfg.num_pages, p->cfg.spill_pages,
+                                                                  p->dev_pool, p->spill_dev, p->cfg.page_bytes,
+                                                                  p->cfg.page_tokens);
+        else
+            ap::k_dispatch_stash_copy<int2><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, xo, stt, rec, ring,
+                                                                  sring, p->cfg.num_pages, p->cfg.spill_pages,
+                                                                  p->dev_pool, p->spill_dev, p->cfg.page_bytes,
+                                                                  p->cfg.page_tokens);
+        AP_CHECK_LAUNCH("dispatch_stash copy launch");
+    }
     p->next_id += 1;
     p->q_count[slot] += 1;
     if (record_id) *record_id = h.id;

@@ -4,6 +4,10 @@ One step is the whole path over one batch of the Qwen3-MoE-like layer
 (T = 16384 tokens as 2 chunks of 8192, H = 2048, E = 128, top-8, dropless,
 64-token pages, pool = 1.1x the live rows): for each chunk route -> dispatch
 -> stash push; then for each chunk stash pop -> combine of the expert outputs.
+By default dispatch and push are the one fused call (the dispatched rows are
+written to the dispatch buffer and to their pages in one pass); ``--unfused``
+times the two separate calls, and the other variant is always timed too
+(``alt`` in the output).
 All calls go through the C ABI on one high-priority stream; the timed region
 replays one CUDA graph of the step (``--eager`` launches the calls one by one
 instead), and a second, eager pass with CUDA events around every call gives
@@ -48,6 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA-graph replay")
     ap.add_argument("--op-steps", type=int, default=100, help="eager steps with per-call events (ops, roofline)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time the step with separate dispatch and push calls (default: the fused call)")
+    ap.add_argument("--no-alt", action="store_true", help="skip timing the other step variant")
     ap.add_argument("--overlap", action="store_true",
                     help="also measure reload (pop) overlapped with a bf16 GEMM on another stream")
     return ap.parse_args(argv)
@@ -147,6 +154,8 @@ def op_bytes(wl, R):
         "push": 2 * R * rb,
         "pop": 2 * R * rb,
         "combine": R * H * 2 + T * H * 2 + T * k * 8,
+        # fused dispatch + push: x read once, dispatch rows and page rows written
+        "dispatch_stash": T * H * 2 + 2 * R * rb + T * k * 8 + R * 4,
     }
 
 
@@ -186,9 +195,11 @@ class Step:
         self.R = wl.rows
         self.bytes = op_bytes(wl, self.R)
         self.launches_per_step = wl.chunks * (1 + 4 + 2 + 2 + 1)
+        self.launches_per_step_fused = wl.chunks * (1 + 5 + 2 + 1)
 
-    def run(self, events=None):
-        """Enqueue one step.  events: dict op -> list of (start, end) event pairs."""
+    def run(self, events=None, fused=False):
+        """Enqueue one step.  events: dict op -> list of (start, end) event pairs.
+        fused: one fused dispatch + push call per chunk instead of two calls."""
         torch, ap, wl, s = self.torch, self.ap, self.wl, self.stream
 
         def rec(name, fn):
@@ -205,8 +216,12 @@ class Step:
         with torch.cuda.stream(s):
             for h, d in self.chunks:
                 rec("route", lambda: ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=s))
-                rec("dispatch", lambda: ap.dispatch_permute(d["x"], d["idx"], wl.E, out=d["disp"], stream=s))
-                rec("push", lambda: self.pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"], d["disp"]["live"]))
+                if fused:
+                    rec("dispatch_stash", lambda: self.pool.dispatch_stash(0, d["x"], d["idx"], wl.E, out=d["disp"]))
+                else:
+                    rec("dispatch", lambda: ap.dispatch_permute(d["x"], d["idx"], wl.E, out=d["disp"], stream=s))
+                    rec("push", lambda: self.pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"],
+                                                       d["disp"]["live"]))
             for h, d in self.chunks:
                 rec("pop", lambda: self.pool.pop(0, [d["dst"]]))
                 rec("combine", lambda: ap.combine_unpermute(d["y"], d["disp"]["dest"], d["w"], out=d["out"],
@@ -232,7 +247,7 @@ class Step:
         return h2d, d2h
 
 
-def overlap_report(step, device, grid_bounds=(64, 152, 608, 2048), reps=10):
+def overlap_report(step, device, grid_bounds=(64, 152, 304, 608, 1216, 2048), reps=15):
     """Exposed reload time when the pops of one step run on the high-priority
     paging stream while a bf16 GEMM (cuBLAS, 8192 x 2304 x 8192) runs on a
     normal-priority compute stream; the reloads are issued first and waited
@@ -264,11 +279,15 @@ def overlap_report(step, device, grid_bounds=(64, 152, 608, 2048), reps=10):
     gemm()
     torch.cuda.synchronize(device)
     out = {"gemm": "bf16 8192x2304 @ 2304x8192 on a normal-priority stream",
-           "reload": f"{len(step.chunks)} pops of the step on the high-priority paging stream", "by_grid_bound": {}}
-    for gb in grid_bounds:
-        step.pool.max_ctas = gb
-        t_gemm, t_pop, t_both = [], [], []
-        for _ in range(reps):
+           "reload": f"{len(step.chunks)} pops of the step on the high-priority paging stream",
+           "method": f"median of {reps} rounds; each round measures every grid bound in turn: the GEMM alone, "
+                     "the reloads alone, then both with the reloads launched first and waited on last",
+           "by_grid_bound": {}}
+    samples = {gb: ([], [], []) for gb in grid_bounds}
+    for _ in range(reps):
+        for gb in grid_bounds:
+            step.pool.max_ctas = gb
+            t_gemm, t_pop, t_both = samples[gb]
             s0, s1 = ev(), ev()
             s0.record(compute)
             gemm()
@@ -293,6 +312,8 @@ def overlap_report(step, device, grid_bounds=(64, 152, 608, 2048), reps=10):
             t_gemm.append(s0.elapsed_time(s1))
             t_pop.append(p0.elapsed_time(p1))
             t_both.append(b0.elapsed_time(b1))
+    for gb in grid_bounds:
+        t_gemm, t_pop, t_both = samples[gb]
         mg, mp, mb = (statistics.median(v) for v in (t_gemm, t_pop, t_both))
         out["by_grid_bound"][str(gb)] = {"gemm_ms": round(mg, 4), "reload_ms": round(mp, 4),
                                          "both_ms": round(mb, 4), "exposed_ms": round(mb - mg, 4),
@@ -336,28 +357,32 @@ def native(args):
     step = Step(wl, device, seed_base=1000 * rank)
     tokens_per_step = wl.T * wl.chunks
 
+    fused_main = not args.unfused
+
+    def capture(fused):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=step.stream):
+            step.run(fused=fused)
+        for _ in range(3):
+            with torch.cuda.stream(step.stream):
+                g.replay()
+        torch.cuda.synchronize(device)
+        return g
+
     for _ in range(max(args.warmup, 3)):
-        step.run()
+        step.run(fused=fused_main)
     torch.cuda.synchronize(device)
 
     # one step captured as a CUDA graph: live counts, offsets and pages stay on
     # the device, so every replay re-routes from the current inputs
-    graph = None
-    if not args.eager:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=step.stream):
-            step.run()
-        for _ in range(3):
-            with torch.cuda.stream(step.stream):
-                graph.replay()
-        torch.cuda.synchronize(device)
+    graph = None if args.eager else capture(fused_main)
 
-    def one_step(events=None):
-        if graph is not None and events is None:
+    def one_step():
+        if graph is not None:
             with torch.cuda.stream(step.stream):
                 graph.replay()
         else:
-            step.run(events)
+            step.run(fused=fused_main)
 
     # timed region: K steps, bracketed by events on the launching stream
     sampler = ClockSampler(local)
@@ -381,14 +406,34 @@ def native(args):
     events = {}
     op_steps = max(1, min(args.op_steps, args.steps))
     for _ in range(op_steps):
-        step.run(events)
+        step.run(events, fused=fused_main)
     torch.cuda.synchronize(device)
+
+    # the other step variant (fused <-> separate dispatch and push), for comparison
+    alt = None
+    if not args.eager and not args.no_alt:
+        g2 = capture(not fused_main)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(step.stream)
+        for _ in range(args.steps):
+            with torch.cuda.stream(step.stream):
+                g2.replay()
+        a1.record(step.stream)
+        torch.cuda.synchronize(device)
+        a_el = aggregate_max(a0.elapsed_time(a1) / 1e3, world)
+        alt = {"step": "separate dispatch and push calls" if fused_main else "fused dispatch + push",
+               "value": round(whole_job_rate(tokens_per_step * args.steps, world, a_el), 1),
+               "ms_per_step": round(a_el * 1e3 / args.steps, 5)}
+        del g2
 
     per_op = {}
     for name, pairs in events.items():
         ms = [a.elapsed_time(b) for a, b in pairs]
         per_op[name] = sum(ms) / len(ms)  # per launch (per chunk)
-    total_bytes = sum(step.bytes.values()) * wl.chunks
+    step_ops = (("route", "dispatch_stash", "pop", "combine") if fused_main
+                else ("route", "dispatch", "push", "pop", "combine"))
+    total_bytes = sum(step.bytes[o] for o in step_ops) * wl.chunks
     ms_per_step = max_elapsed * 1e3 / args.steps
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
@@ -453,9 +498,12 @@ def native(args):
                            "hbm_gbs_step": round(total_bytes / (ms_per_step / 1e3) / 1e9, 1),
                            "l2": "working set per step ~1.4 GB > 126 MB L2: no flush",
                            "parallelism": f"replicas x{world}", "stream": "one high-priority stream",
-                           "launch": "eager" if graph is None else "CUDA graph of one step, replayed"},
-                "roofline": roofline, "ops": ops, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
-                "gpu_launches": step.launches_per_step * args.steps, "clocks": clocks}
+                           "launch": "eager" if graph is None else "CUDA graph of one step, replayed",
+                           "step": ("route, fused dispatch + push, pop, combine per chunk" if fused_main
+                                    else "route, dispatch, push, pop, combine per chunk")},
+                "roofline": roofline, "ops": ops, "alt": alt, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
+                "gpu_launches": (step.launches_per_step_fused if fused_main else step.launches_per_step) * args.steps,
+                "clocks": clocks}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

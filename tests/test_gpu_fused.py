@@ -1,0 +1,107 @@
+"""GPU parity: the fused dispatch + push against the oracle's dispatch and push.
+
+The fused call must leave exactly what a dispatch followed by a push leaves:
+dispatch outputs, the record and its page table, rings, counters, flags and
+every pool / spill byte (compared with the oracle's byte-exact pool), and the
+pop of the record must give the dispatched rows back."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_paging_gb300 import inputs
+from gpu_util import bf16_to_dev, bf16_to_host, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+ap = pytest.importorskip("activation_paging_gb300")
+FILL = 0xA5
+
+
+@pytest.mark.parametrize("T,H,E,k,C,padded,P,N,SP", [
+    (512, 128, 8, 2, 160, True, 16, 80, 0),       # padded, exactly enough pages
+    (1000, 264, 16, 4, 0, False, 32, 150, 0),     # compact, 8-byte rows path, page tails
+    (777, 2056, 32, 6, 0, False, 64, 40, 64),     # odd hidden size; pool overflows into spill
+    (300, 64, 8, 2, 0, False, 8, 10, 5),          # spill exhausted: lost pages
+])
+def test_fused_matches_oracle_dispatch_then_push(T, H, E, k, C, padded, P, N, SP):
+    rb = H * 2
+    page_bytes = ap.page_bytes_for(P, (rb,))
+    g = ap.Pool(P, page_bytes, N, 2, 4, E, N + SP + E, SP, fill=FILL)
+    o = oracle.Pool(P, page_bytes, N, 2, 4, E, N + SP + E, SP, keep_bytes=True, fill=FILL)
+    for rep in range(2):
+        logits = inputs.router_logits(T + rep, T, E)
+        x = inputs.normal_bf16(T + rep, inputs.X_STREAM, (T, H))
+        idx, _ = oracle.route_topk(logits, k)
+        plan = oracle.dispatch(x, idx, E, C, padded)
+        rid_o = o.push(rep, [plan["xd"].view(np.uint8).reshape(plan["rows"], rb)], plan["rows"], plan["seg_off"],
+                       plan["live"])
+        xd_dev = torch.full((plan["rows"], H), 0xA5A5 - 0x10000, dtype=torch.int16, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(g.stream):
+            d = g.dispatch_stash(rep, bf16_to_dev(x), to_dev(idx), E, C, padded,
+                                 out={"xd": xd_dev.view(torch.bfloat16)})
+        torch.cuda.synchronize()
+        assert d["record_id"] == rid_o
+        for key in ("counts", "live", "seg_off", "dest"):
+            assert np.array_equal(host(d[key]), plan[key]), key
+        assert np.array_equal(bf16_to_host(d["xd"]), plan["xd"])
+        assert g.state() == o.state()
+        a, b = g.record(rep, 0), o.record(rep, 0)
+        for key in ("id", "npages", "ndev", "nspill", "nlost"):
+            assert a[key] == b[key], key
+        for key in ("page_table", "row0", "nrows"):
+            assert np.array_equal(a[key], b[key]), key
+    assert np.array_equal(host(g.pool), o.pool_bytes())
+    if SP:
+        assert np.array_equal(g.spill.numpy(), o.spill_bytes())
+    rg, sg = g.rings()
+    ro, so = o.rings()
+    assert np.array_equal(rg, ro) and np.array_equal(sg, so)
+    # pops give the rows back (lost pages leave the canary)
+    for rep in range(2):
+        rec = o.record(rep, 0)
+        rows = int(max(rec["row0"] + rec["nrows"])) + 1 if rec["npages"] else 1
+        dst_np = [np.full((rows, rb), 0x3C, np.uint8)]
+        dst = to_dev(dst_np[0])
+        torch.cuda.synchronize()
+        g.pop(rep, [dst])
+        o.pop(rep, dst_np, rows)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(dst), dst_np[0])
+    assert g.state() == o.state()
+
+
+def test_fused_equals_unfused_on_the_gpu():
+    wl = inputs.WORKLOADS["qwen3_moe"]
+    logits = torch.from_numpy(inputs.router_logits(5, wl.T, wl.E)).cuda()
+    x = bf16_to_dev(inputs.normal_bf16(5, inputs.X_STREAM, (wl.T, wl.H)))
+    idx, _ = ap.route_topk(logits, wl.k)
+    a = ap.Pool(wl.page_tokens, wl.page_bytes, wl.num_pages, 1, 2, wl.E, fill=0)
+    b = ap.Pool(wl.page_tokens, wl.page_bytes, wl.num_pages, 1, 2, wl.E, fill=0)
+    d1 = ap.dispatch_permute(x, idx, wl.E)
+    a.push(0, [d1["xd"]], d1["seg_off"], d1["live"])
+    with torch.cuda.stream(b.stream):
+        b.stream.wait_stream(torch.cuda.default_stream())
+        d2 = b.dispatch_stash(0, x, idx, wl.E)
+    torch.cuda.synchronize()
+    for key in ("counts", "live", "seg_off", "dest", "xd"):
+        assert torch.equal(d1[key].view(torch.int16) if key == "xd" else d1[key],
+                           d2[key].view(torch.int16) if key == "xd" else d2[key]), key
+    assert a.state() == b.state()
+    ra, rb_ = a.record(0), b.record(0)
+    assert np.array_equal(ra["page_table"], rb_["page_table"])
+    assert torch.equal(a.pool, b.pool)
+
+
+def test_fused_host_errors():
+    g = ap.Pool(8, ap.page_bytes_for(8, (2 * 6,)), 16, 1, 1, 4)
+    x = torch.zeros((16, 6), dtype=torch.bfloat16, device="cuda")  # 12-byte rows: not 8-byte aligned
+    idx = torch.zeros((16, 2), dtype=torch.int32, device="cuda")
+    with pytest.raises(ap.APError) as e:
+        with torch.cuda.stream(g.stream):
+            g.dispatch_stash(0, x, idx, 4)
+    assert e.value.status == -6
+    rc = g.lib.ap_dispatch_stash(g.handle, 0, None, 0, 8, None, 2, 4, 0, 0, None, 0, None, None, None, None, None,
+                                 None, 0, None, None, torch.cuda.Stream().cuda_stream)
+    assert rc == -5  # not the paging stream
