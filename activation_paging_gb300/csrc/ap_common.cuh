@@ -21,15 +21,21 @@ int sm_count();
 int resident_grid(const void *kernel, int threads, size_t smem = 0);
 
 // Dispatch stages shared by the dispatch entry points (dispatch.cu): argument
-// checks, then the count / scan / rank launches that produce counts, live,
-// seg_off, dest and src_tok.
+// checks, then the count/rank and scan launches that produce counts, live,
+// seg_off and the in-block ranks the copy kernels turn into dest and src_tok.
 ap_status dispatch_check(const char *who, const void *x, int64_t T, int32_t H, const int32_t *idx, int32_t k,
                          int32_t E, int32_t capacity, int32_t padded, const void *xd, int64_t xd_rows,
                          const int32_t *counts, const int32_t *live, const int32_t *seg_off, const int32_t *dest,
                          const void *scratch, int64_t scratch_bytes);
 ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
-                            int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, int32_t *src_tok,
-                            void *scratch, uint32_t *d_status, cudaStream_t st);
+                            int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, void *scratch,
+                            uint32_t *d_status, cudaStream_t st);
+// The count/rank stage alone (block histograms into scratch, in-block ranks
+// into dest), and the number of count/rank blocks; the fused dispatch + stash
+// runs its own scan (see dispatch_scan.cuh).
+ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
+                              uint32_t *d_status, cudaStream_t st);
+int dispatch_blocks(int64_t T);
 
 #define AP_CHECK_LAUNCH(what)                                   \
     do {                                                        \

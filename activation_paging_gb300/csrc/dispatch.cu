@@ -2,139 +2,48 @@
 //
 // Expert-major, capacity-shaped dispatch buffers (Megatron-LM pull 7342,
 // "Summary"; torchtitan pull 5541, "AI-Generated Details": the capacity shape
-// that reload restores).  Four launches on the caller's stream:
-//   1. k_count  - per block of kTokPerBlk tokens, a shared-memory histogram of
-//                 expert ids -> blk[b][e];
+// that reload restores).  Three launches on the caller's stream:
+//   1. k_count_rank - per block of kTokPerBlk tokens: the expert histogram
+//                 -> blk[b][e], and each pair's stable rank inside the block
+//                 (warp match_any + popc over 32 pairs at a time, pairs in
+//                 t-then-j order) -> dest (temporarily);
 //   2. k_scan   - one CTA: exclusive scan of blk over b per expert (block base
 //                 offsets), counts, live = min(count, C), segment offsets;
-//   3. k_rank   - per block: warp-level stable ranks (match_any + popc over
-//                 32 pairs at a time, pairs in t-then-j order) -> dest, src_tok;
-//   4. k_copy_* - one warp per token: the row is read once and written to its
-//                 k destinations with 16-byte vectors (BF16), or quantised
-//                 once to E4M3 with a per-row scale and written k times.
+//   3. k_copy_* - one warp per token: lanes j < k finish their pair's row
+//                 (block base + in-block rank, capacity test) -> dest, src_tok;
+//                 the row is read once and written to its k destinations with
+//                 16-byte vectors (BF16), or quantised once to E4M3 with a
+//                 per-row scale and written k times.
 // The ranks are deterministic: no global atomics decide any order.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
-#include "ap_common.cuh"
+#include "dispatch_scan.cuh"
 
 namespace ap {
 namespace {
 
-constexpr int kTokPerBlk = 64; // tokens per count/rank block
 constexpr int kRankThreads = 256;
 constexpr int kRankWarps = kRankThreads / kWarp;
 
-__global__ void __launch_bounds__(256) k_count(const int32_t *__restrict__ idx, int64_t T, int k, int E,
-                                               int32_t *__restrict__ blk)
-{
-    extern __shared__ int32_t hist[];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-    __syncthreads();
-    const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
-    int64_t p1 = p0 + (int64_t)kTokPerBlk * k;
-    if (p1 > T * k) p1 = T * k;
-    for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-        const int e = idx[p];
-        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) blk[(int64_t)blockIdx.x * E + e] = hist[e];
-}
-
-// One CTA of 1024 threads.  blk[b][e] -> exclusive base over b (in place).
-// Thread (e, part) owns expert e over a contiguous range of blocks: it sums
-// its range, adds the sums of the earlier parts, then rewrites its range as
-// running bases.  Then counts, live = min(count, C) and segment offsets.
+// One CTA of 1024 threads: the expert scan (dispatch_scan.cuh).
 __global__ void __launch_bounds__(1024) k_scan(int32_t *__restrict__ blk, int nblk, int E, int capacity,
                                                 int padded, int32_t *__restrict__ counts,
                                                 int32_t *__restrict__ live, int32_t *__restrict__ seg_off)
 {
-    __shared__ int32_t s_tot[1024];
-    __shared__ int32_t s_warp[32];
-    const int tid = threadIdx.x;
-    const int parts = blockDim.x / E; // >= 1 since E <= 1024
-    const int e = tid % E, part = tid / E;
-    const bool active = part < parts;
-    const int per = (nblk + parts - 1) / parts;
-    const int b0 = part * per;
-    const int b1 = (b0 + per < nblk) ? b0 + per : nblk;
-    int32_t sum = 0;
-    if (active) {
-        int b = b0;
-        for (; b + 8 <= b1; b += 8) {
-            int32_t c[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) sum += c[u];
-        }
-        for (; b < b1; ++b) sum += blk[(int64_t)b * E + e];
-    }
-    s_tot[tid] = active ? sum : 0;
-    __syncthreads();
-    int32_t total = 0;
-    if (active) {
-        int32_t run = 0;
-        for (int p = 0; p < parts; ++p) {
-            if (p == part) run = total;
-            total += s_tot[p * E + e];
-        }
-        int b = b0;
-        for (; b + 8 <= b1; b += 8) {
-            int32_t c[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                blk[(int64_t)(b + u) * E + e] = run;
-                run += c[u];
-            }
-        }
-        for (; b < b1; ++b) {
-            const int32_t c = blk[(int64_t)b * E + e];
-            blk[(int64_t)b * E + e] = run;
-            run += c;
-        }
-    }
-    // threads tid < E (part 0) own expert tid's totals
-    const int32_t l = (tid < E) ? ((capacity > 0 && total > capacity) ? capacity : total) : 0;
-    if (tid < E) {
-        counts[tid] = total;
-        live[tid] = l;
-    }
-    // exclusive scan of live over experts (compact layout)
-    int32_t x = l;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
-    }
-    if (lane == 31) s_warp[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-        int32_t v = s_warp[lane];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, v, off);
-            if (lane >= off) v += y;
-        }
-        s_warp[lane] = v;
-    }
-    __syncthreads();
-    const int32_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
-    if (tid < E) seg_off[tid] = padded ? tid * capacity : incl - l;
+    scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off);
 }
 
-// Stable ranks.  The block's pairs are split into kRankWarps contiguous
-// ranges; each warp counts its range, a per-expert scan over warps gives each
-// warp's base, then each warp walks its range 32 pairs at a time in order.
-__global__ void __launch_bounds__(kRankThreads) k_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
-                                                       int capacity, const int32_t *__restrict__ blk_base,
-                                                       const int32_t *__restrict__ seg_off,
-                                                       int32_t *__restrict__ dest, int32_t *__restrict__ src_tok,
-                                                       uint32_t *d_status)
+// Block histograms and stable in-block ranks, in one pass over idx.  The
+// block's pairs are split into kRankWarps contiguous ranges; each warp counts
+// its range, a per-expert scan over warps gives each warp's base inside the
+// block (the block's totals go to blk[b][e]), then each warp walks its range
+// 32 pairs at a time in order (match_any + popc).  dest[p] temporarily holds
+// the pair's rank inside its block (-1 for an invalid id); the copy kernels
+// add the block's base from the scan and write the final row.
+__global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
+                                                             int32_t *__restrict__ blk, int32_t *__restrict__ dest,
+                                                             uint32_t *d_status)
 {
     extern __shared__ int32_t cnt[]; // [kRankWarps][E]
     const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
@@ -155,15 +64,16 @@ __global__ void __launch_bounds__(kRankThreads) k_rank(const int32_t *__restrict
         else bad = true;
     }
     __syncthreads();
-    // phase 2: per expert, exclusive scan over warps starting at the block base
+    // phase 2: per expert, exclusive scan over warps; the block total is the block's count
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int32_t run = blk_base[(int64_t)blockIdx.x * E + e];
+        int32_t run = 0;
 #pragma unroll
         for (int w2 = 0; w2 < kRankWarps; ++w2) {
             const int32_t c = cnt[w2 * E + e];
             cnt[w2 * E + e] = run;
             run += c;
         }
+        blk[(int64_t)blockIdx.x * E + e] = run;
     }
     __syncthreads();
     // phase 3: ordered walk, 32 pairs per step
@@ -174,17 +84,8 @@ __global__ void __launch_bounds__(kRankThreads) k_rank(const int32_t *__restrict
         const bool valid = in && e >= 0 && e < E;
         if (!valid) e = -1 - (int)(in ? 0 : 1); // -1: bad id, -2: past the end
         const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (valid) {
-            const int32_t r = my[e] + __popc(peers & lanemask_lt());
-            int32_t d = -1;
-            if (capacity <= 0 || r < capacity) {
-                d = seg_off[e] + r;
-                if (src_tok) src_tok[d] = (int32_t)(p / k);
-            }
-            dest[p] = d;
-        } else if (in) {
-            dest[p] = -1;
-        }
+        if (valid) dest[p] = my[e] + __popc(peers & lanemask_lt());
+        else if (in) dest[p] = -1;
         __syncwarp();
         if (valid && (peers & lanemask_lt()) == 0) my[e] += __popc(peers);
         __syncwarp();
@@ -195,14 +96,17 @@ __global__ void __launch_bounds__(kRankThreads) k_rank(const int32_t *__restrict
 // ---- BF16 row copy: one warp per token, row read once, written k times ------
 template <typename V>
 __global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x, int64_t T, int64_t rb,
-                                                   const int32_t *__restrict__ dest, int k,
-                                                   uint8_t *__restrict__ xd)
+                                                   const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
+                                                   int k, int E, int capacity, const int32_t *__restrict__ blk,
+                                                   const int32_t *__restrict__ seg_off,
+                                                   int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd)
 {
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int64_t nvec = rb / (int64_t)sizeof(V);
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
-        const int32_t my_d = (lane < k) ? __ldcs(dest + t * k + lane) : -1;
+        const int32_t my_d =
+            (lane < k) ? finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity) : -1;
         const V *src = reinterpret_cast<const V *>(x + t * rb);
         constexpr int U = 4;
         // warp-uniform loop: every lane reaches the shuffles below
@@ -238,14 +142,18 @@ __device__ __forceinline__ uint8_t to_e4m3(float v)
 // VE bf16 elements per lane step: 8 (16-byte loads, 8-byte stores), 4, 2 or 1.
 template <int VE>
 __global__ void __launch_bounds__(256) k_copy_rows_e4m3(const uint16_t *__restrict__ x, int64_t T, int H,
-                                                        const int32_t *__restrict__ dest, int k,
-                                                        uint8_t *__restrict__ xd, float *__restrict__ xd_scale)
+                                                        const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
+                                                        int k, int E, int capacity, const int32_t *__restrict__ blk,
+                                                        const int32_t *__restrict__ seg_off,
+                                                        int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd,
+                                                        float *__restrict__ xd_scale)
 {
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int nstep = H / VE;
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
-        const int32_t my_d = (lane < k) ? __ldcs(dest + t * k + lane) : -1;
+        const int32_t my_d =
+            (lane < k) ? finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity) : -1;
         const uint16_t *row = x + t * H;
         // pass 1: amax
         float amax = 0.f;
@@ -327,22 +235,32 @@ __global__ void k_cast_e4m3(const float *__restrict__ in, uint8_t *__restrict__ 
 
 int64_t nblocks(int64_t T) { return (T + kTokPerBlk - 1) / kTokPerBlk; }
 
+// Arguments every copy kernel needs to finish the pairs' rows (finalize_dest).
+struct Ranks {
+    const int32_t *idx;
+    int32_t *dest;
+    int k, E, capacity;
+    const int32_t *blk, *seg_off;
+    int32_t *src_tok;
+};
+
 template <typename V>
-void launch_copy(const uint8_t *x, int64_t T, int64_t rb, const int32_t *dest, int k, uint8_t *xd, cudaStream_t st)
+void launch_copy(const uint8_t *x, int64_t T, int64_t rb, const Ranks &r, uint8_t *xd, cudaStream_t st)
 {
     // one warp per token; blocks beyond the resident ones start as others retire
     const int64_t want = (T + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * 16;
-    k_copy_rows<V><<<(int)(want < cap ? want : cap), 256, 0, st>>>(x, T, rb, dest, k, xd);
+    k_copy_rows<V><<<(int)(want < cap ? want : cap), 256, 0, st>>>(x, T, rb, r.idx, r.dest, r.k, r.E, r.capacity,
+                                                                   r.blk, r.seg_off, r.src_tok, xd);
 }
 
 template <int VE>
-void launch_e4m3(const uint16_t *x, int64_t T, int H, const int32_t *dest, int k, uint8_t *xd, float *xd_scale,
-                 cudaStream_t st)
+void launch_e4m3(const uint16_t *x, int64_t T, int H, const Ranks &r, uint8_t *xd, float *xd_scale, cudaStream_t st)
 {
     static const int resident = resident_grid((const void *)k_copy_rows_e4m3<VE>, 256);
     const int64_t want = (T + 7) / 8; // one warp per token
-    k_copy_rows_e4m3<VE><<<(int)(want < resident ? want : resident), 256, 0, st>>>(x, T, H, dest, k, xd, xd_scale);
+    k_copy_rows_e4m3<VE><<<(int)(want < resident ? want : resident), 256, 0, st>>>(
+        x, T, H, r.idx, r.dest, r.k, r.E, r.capacity, r.blk, r.seg_off, r.src_tok, xd, xd_scale);
 }
 
 } // namespace
@@ -380,23 +298,29 @@ ap_status dispatch_check(const char *who, const void *x, int64_t T, int32_t H, c
     return AP_OK;
 }
 
-ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
-                            int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, int32_t *src_tok,
-                            void *scratch, uint32_t *d_status, cudaStream_t st)
+ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
+                              uint32_t *d_status, cudaStream_t st)
 {
-    int32_t *blk = static_cast<int32_t *>(scratch);
     const int64_t nb = nblocks(T);
-    if (nb > 0) {
-        k_count<<<(unsigned)nb, 256, E * sizeof(int32_t), st>>>(idx, T, k, E, blk);
-        AP_CHECK_LAUNCH("dispatch count launch");
-    }
-    k_scan<<<1, 1024, 0, st>>>(blk, (int)nb, E, capacity, padded, counts, live, seg_off);
+    if (nb == 0) return AP_OK;
+    const size_t smem = (size_t)kRankWarps * E * sizeof(int32_t);
+    k_count_rank<<<(unsigned)nb, kRankThreads, smem, st>>>(idx, T, k, E, static_cast<int32_t *>(scratch), dest,
+                                                           d_status);
+    AP_CHECK_LAUNCH("dispatch count/rank launch");
+    return AP_OK;
+}
+
+int dispatch_blocks(int64_t T) { return (int)nblocks(T); }
+
+ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
+                            int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, void *scratch,
+                            uint32_t *d_status, cudaStream_t st)
+{
+    ap_status s = dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
+    if (s != AP_OK) return s;
+    k_scan<<<1, 1024, 0, st>>>(static_cast<int32_t *>(scratch), (int)nblocks(T), E, capacity, padded, counts, live,
+                               seg_off);
     AP_CHECK_LAUNCH("dispatch scan launch");
-    if (T == 0) return AP_OK;
-    const size_t rank_smem = (size_t)kRankWarps * E * sizeof(int32_t);
-    k_rank<<<(unsigned)nb, kRankThreads, rank_smem, st>>>(idx, T, k, E, capacity, blk, seg_off, dest, src_tok,
-                                                         d_status);
-    AP_CHECK_LAUNCH("dispatch rank launch");
     return AP_OK;
 }
 
@@ -417,33 +341,34 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
     if (out_dtype == AP_DTYPE_E4M3 && T > 0 && !xd_scale)
         return fail(AP_EINVAL, "dispatch_permute: E4M3 needs xd_scale");
     cudaStream_t st = (cudaStream_t)stream;
-    s = dispatch_metadata(T, idx, k, E, capacity, padded, counts, live, seg_off, dest, src_tok, scratch, d_status, st);
+    s = dispatch_metadata(T, idx, k, E, capacity, padded, counts, live, seg_off, dest, scratch, d_status, st);
     if (s != AP_OK || T == 0) return s;
+    const Ranks ranks{idx, dest, k, E, capacity, static_cast<const int32_t *>(scratch), seg_off, src_tok};
     if (out_dtype == AP_DTYPE_BF16) {
         const int64_t rb = (int64_t)H * 2;
         const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xd) | (uintptr_t)rb;
         const uint8_t *xs = static_cast<const uint8_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         if ((al & 15) == 0)
-            launch_copy<int4>(xs, T, rb, dest, k, xo, st);
+            launch_copy<int4>(xs, T, rb, ranks, xo, st);
         else if ((al & 7) == 0)
-            launch_copy<int2>(xs, T, rb, dest, k, xo, st);
+            launch_copy<int2>(xs, T, rb, ranks, xo, st);
         else if ((al & 3) == 0)
-            launch_copy<int>(xs, T, rb, dest, k, xo, st);
+            launch_copy<int>(xs, T, rb, ranks, xo, st);
         else
-            launch_copy<short>(xs, T, rb, dest, k, xo, st);
+            launch_copy<short>(xs, T, rb, ranks, xo, st);
     } else {
         const uint16_t *xs = static_cast<const uint16_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         const uintptr_t ax = reinterpret_cast<uintptr_t>(x), ao = reinterpret_cast<uintptr_t>(xd);
         if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0)
-            launch_e4m3<8>(xs, T, H, dest, k, xo, xd_scale, st);
+            launch_e4m3<8>(xs, T, H, ranks, xo, xd_scale, st);
         else if (H % 4 == 0 && (ax & 7) == 0 && (ao & 3) == 0)
-            launch_e4m3<4>(xs, T, H, dest, k, xo, xd_scale, st);
+            launch_e4m3<4>(xs, T, H, ranks, xo, xd_scale, st);
         else if (H % 2 == 0 && (ax & 3) == 0 && (ao & 1) == 0)
-            launch_e4m3<2>(xs, T, H, dest, k, xo, xd_scale, st);
+            launch_e4m3<2>(xs, T, H, ranks, xo, xd_scale, st);
         else
-            launch_e4m3<1>(xs, T, H, dest, k, xo, xd_scale, st);
+            launch_e4m3<1>(xs, T, H, ranks, xo, xd_scale, st);
     }
     AP_CHECK_LAUNCH("dispatch copy launch");
     return AP_OK;

@@ -1,0 +1,121 @@
+// Expert scan of the dispatch, shared by the dispatch kernels (dispatch.cu)
+// and the fused scan + stash plan kernel (stash.cu).
+#pragma once
+
+#include "ap_common.cuh"
+
+namespace ap {
+namespace {
+
+constexpr int kTokPerBlk = 64; // tokens per count/rank block
+
+// One CTA of 1024 threads.  blk[b][e] -> exclusive base over b (in place).
+// Thread (e, part) owns expert e over a contiguous range of blocks: it sums
+// its range, adds the sums of the earlier parts, then rewrites its range as
+// running bases.  Then counts, live = min(count, C) and segment offsets.
+__device__ __forceinline__ void scan_body(int32_t *__restrict__ blk, int nblk, int E, int capacity, int padded,
+                                          int32_t *__restrict__ counts, int32_t *__restrict__ live,
+                                          int32_t *__restrict__ seg_off)
+{
+    __shared__ int32_t s_tot[1024];
+    __shared__ int32_t s_warp[32];
+    const int tid = threadIdx.x;
+    const int parts = blockDim.x / E; // >= 1 since E <= 1024
+    const int e = tid % E, part = tid / E;
+    const bool active = part < parts;
+    const int per = (nblk + parts - 1) / parts;
+    const int b0 = part * per;
+    const int b1 = (b0 + per < nblk) ? b0 + per : nblk;
+    int32_t sum = 0;
+    if (active) {
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
+            int32_t c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sum += c[u];
+        }
+        for (; b < b1; ++b) sum += blk[(int64_t)b * E + e];
+    }
+    s_tot[tid] = active ? sum : 0;
+    __syncthreads();
+    int32_t total = 0;
+    if (active) {
+        int32_t run = 0;
+        for (int p = 0; p < parts; ++p) {
+            if (p == part) run = total;
+            total += s_tot[p * E + e];
+        }
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
+            int32_t c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                blk[(int64_t)(b + u) * E + e] = run;
+                run += c[u];
+            }
+        }
+        for (; b < b1; ++b) {
+            const int32_t c = blk[(int64_t)b * E + e];
+            blk[(int64_t)b * E + e] = run;
+            run += c;
+        }
+    }
+    // threads tid < E (part 0) own expert tid's totals
+    const int32_t l = (tid < E) ? ((capacity > 0 && total > capacity) ? capacity : total) : 0;
+    if (tid < E) {
+        counts[tid] = total;
+        live[tid] = l;
+    }
+    // exclusive scan of live over experts (compact layout)
+    int32_t x = l;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t v = s_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += y;
+        }
+        s_warp[lane] = v;
+    }
+    __syncthreads();
+    const int32_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
+    if (tid < E) seg_off[tid] = padded ? tid * capacity : incl - l;
+}
+
+// Row of pair (t, j) from its in-block rank (left in dest by k_count_rank) and
+// the block bases (left in blk by the scan): rank = base[b][e] + in-block
+// rank; kept iff capacity <= 0 or rank < capacity.  Writes the final dest and,
+// for a kept pair, src_tok; returns the row or -1.  Called once per pair.
+__device__ __forceinline__ int32_t finalize_dest(const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
+                                                 int32_t *__restrict__ src_tok, const int32_t *__restrict__ blk,
+                                                 const int32_t *__restrict__ seg_off, int64_t t, int j, int k, int E,
+                                                 int capacity)
+{
+    const int64_t p = t * k + j;
+    const int32_t lr = dest[p];
+    if (lr < 0) return -1; // invalid expert id: already -1
+    const int e = idx[p];
+    const int32_t r = blk[(t / kTokPerBlk) * E + e] + lr;
+    int32_t d = -1;
+    if (capacity <= 0 || r < capacity) {
+        d = seg_off[e] + r;
+        if (src_tok) src_tok[d] = (int32_t)t;
+    }
+    dest[p] = d;
+    return d;
+}
+
+} // namespace
+} // namespace ap

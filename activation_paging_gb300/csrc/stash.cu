@@ -29,7 +29,7 @@
 
 #include <new>
 
-#include "ap_common.cuh"
+#include "dispatch_scan.cuh"
 
 namespace ap {
 namespace {
@@ -132,15 +132,21 @@ __global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int32_t *sp
 }
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemSegs = 2048; // segments whose tables the plan keeps in shared memory
 
-__global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, RecPtr rec, int nseg,
-                                                             const int32_t *__restrict__ d_seg_off,
-                                                             const int32_t *__restrict__ d_live, int64_t src_rows,
-                                                             int P, int64_t max_pages, int64_t N, int64_t SP)
+__device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, int nseg,
+                                               const int32_t *__restrict__ d_seg_off,
+                                               const int32_t *__restrict__ d_live, int64_t src_rows, int P,
+                                               int64_t max_pages, int64_t N, int64_t SP)
 {
     __shared__ int64_t s_warp[kPlanThreads / kWarp];
     __shared__ int64_t s_carry;
     __shared__ uint32_t s_flags;
+    // segment tables in shared memory when they fit (the descriptor step
+    // below searches them once per page)
+    __shared__ int64_t s_base[kPlanSmemSegs + 1];
+    __shared__ int32_t s_off[kPlanSmemSegs], s_live[kPlanSmemSegs];
+    const bool in_smem = nseg <= kPlanSmemSegs;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) {
         s_carry = 0;
@@ -160,6 +166,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, R
             }
             rec.seg_off[s] = o;
             rec.live[s] = l;
+            if (in_smem) {
+                s_off[s] = o;
+                s_live[s] = l;
+            }
             n = ((int64_t)l + P - 1) / P;
         }
         int64_t x = n;
@@ -181,7 +191,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, R
         }
         __syncthreads();
         const int64_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
-        if (s < nseg) rec.pg_base[s] = s_carry + incl - n;
+        if (s < nseg) {
+            rec.pg_base[s] = s_carry + incl - n;
+            if (in_smem) s_base[s] = s_carry + incl - n;
+        }
         __syncthreads();
         if (tid == kPlanThreads - 1) s_carry += incl;
         __syncthreads();
@@ -191,19 +204,22 @@ __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, R
     const int64_t kept = total < max_pages ? total : max_pages;
     __syncthreads();
     // 2. one descriptor per page: segment by binary search over pg_base
+    const int64_t *pg_base = in_smem ? s_base : rec.pg_base;
+    const int32_t *seg_live = in_smem ? s_live : rec.live;
+    const int32_t *seg_offs = in_smem ? s_off : rec.seg_off;
     for (int64_t ord = tid; ord < kept; ord += kPlanThreads) {
         int lo = 0, hi = nseg - 1; // largest s with pg_base[s] <= ord
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (rec.pg_base[mid] <= ord) lo = mid;
+            if (pg_base[mid] <= ord) lo = mid;
             else hi = mid - 1;
         }
-        const int64_t pg = ord - rec.pg_base[lo];
+        const int64_t pg = ord - pg_base[lo];
         const int64_t r0 = pg * P;
-        int64_t nr = (int64_t)rec.live[lo] - r0;
+        int64_t nr = (int64_t)seg_live[lo] - r0;
         if (nr > P) nr = P;
         PageDesc d;
-        d.row0 = (int64_t)rec.seg_off[lo] + r0;
+        d.row0 = (int64_t)seg_offs[lo] + r0;
         d.nrows = (int32_t)nr;
         d.pad = 0;
         rec.desc[ord] = d;
@@ -237,6 +253,29 @@ __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, R
         if (s_use > st->spill_high_water) st->spill_high_water = s_use;
         st->flags |= f;
     }
+}
+
+__global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, RecPtr rec, int nseg,
+                                                             const int32_t *__restrict__ d_seg_off,
+                                                             const int32_t *__restrict__ d_live, int64_t src_rows,
+                                                             int P, int64_t max_pages, int64_t N, int64_t SP)
+{
+    push_plan_body(st, rec, nseg, d_seg_off, d_live, src_rows, P, max_pages, N, SP);
+}
+
+// Fused dispatch + stash: the dispatch's expert scan and the record's page
+// plan in one CTA (the plan reads the live counts and offsets the scan has
+// just written; __syncthreads makes them visible to the whole block).
+__global__ void __launch_bounds__(kPlanThreads) k_scan_plan(int32_t *__restrict__ blk, int nblk, int E, int capacity,
+                                                             int padded, int32_t *__restrict__ counts,
+                                                             int32_t *__restrict__ live,
+                                                             int32_t *__restrict__ seg_off, ap_pool_state *st,
+                                                             RecPtr rec, int64_t src_rows, int P, int64_t max_pages,
+                                                             int64_t N, int64_t SP)
+{
+    scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off);
+    __syncthreads();
+    push_plan_body(st, rec, E, seg_off, live, src_rows, P, max_pages, N, SP);
 }
 
 struct Planes {
@@ -345,7 +384,10 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
 template <typename V>
 __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__restrict__ x, int64_t T, int64_t rb,
                                                              const int32_t *__restrict__ idx,
-                                                             const int32_t *__restrict__ dest, int k, int E,
+                                                             int32_t *__restrict__ dest, int k, int E, int capacity,
+                                                             const int32_t *__restrict__ blk,
+                                                             const int32_t *__restrict__ seg_off,
+                                                             int32_t *__restrict__ src_tok,
                                                              uint8_t *__restrict__ xd, ap_pool_state *st, RecPtr rec,
                                                              const int32_t *__restrict__ ring,
                                                              const int32_t *__restrict__ spill_ring, int64_t N,
@@ -362,7 +404,7 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
         int32_t my_d = -1;
         uint8_t *my_page = nullptr; // where this lane's pair lands in the pool (row start), or null
         if (lane < k) {
-            my_d = dest[t * k + lane];
+            my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
             const int e = idx[t * k + lane];
             if (my_d >= 0 && e >= 0 && e < E) {
                 const int64_t r = (int64_t)my_d - rec.seg_off[e]; // row within the expert segment
@@ -716,7 +758,7 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
     if (T > 0 && (al & 15) != 0 && (al & 7) != 0)
         return fail(AP_ENOTSUP, "dispatch_stash: rows must be 8-byte aligned (H %% 4 == 0)");
     cudaStream_t st = p->stream;
-    s = dispatch_metadata(T, idx, k, E, capacity, padded, counts, live, seg_off, dest, src_tok, scratch, d_status, st);
+    s = dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
     if (s != AP_OK) return s;
 
     const int32_t pos = (p->q_head[slot] + p->q_count[slot]) % p->cfg.max_records_per_slot;
@@ -738,10 +780,11 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
     h.bound_pages = bound;
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
-    ap::k_push_plan<<<1, ap::kPlanThreads, 0, st>>>(stt, rec, E, seg_off, live, xd_rows, p->cfg.page_tokens,
-                                                    p->cfg.max_pages_per_record, p->cfg.num_pages,
-                                                    p->cfg.spill_pages);
-    AP_CHECK_LAUNCH("dispatch_stash plan launch");
+    ap::k_scan_plan<<<1, ap::kPlanThreads, 0, st>>>(static_cast<int32_t *>(scratch), dispatch_blocks(T), E, capacity,
+                                                    padded, counts, live, seg_off, stt, rec, xd_rows,
+                                                    p->cfg.page_tokens, p->cfg.max_pages_per_record,
+                                                    p->cfg.num_pages, p->cfg.spill_pages);
+    AP_CHECK_LAUNCH("dispatch_stash scan + plan launch");
     if (T > 0) {
         const int64_t want = (T + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 16;
@@ -750,16 +793,17 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
         const int32_t *sring = reinterpret_cast<const int32_t *>(p->dev_meta + p->M.spill_ring);
         const uint8_t *xs = static_cast<const uint8_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
+        const int32_t *blk = static_cast<const int32_t *>(scratch);
         if ((al & 15) == 0)
-            ap::k_dispatch_stash_copy<int4><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, xo, stt, rec, ring,
-                                                                  sring, p->cfg.num_pages, p->cfg.spill_pages,
-                                                                  p->dev_pool, p->spill_dev, p->cfg.page_bytes,
-                                                                  p->cfg.page_tokens);
+            ap::k_dispatch_stash_copy<int4><<<grid, 256, 0, st>>>(
+                xs, T, rb[0], idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, stt, rec, ring, sring,
+                p->cfg.num_pages, p->cfg.spill_pages, p->dev_pool, p->spill_dev, p->cfg.page_bytes,
+                p->cfg.page_tokens);
         else
-            ap::k_dispatch_stash_copy<int2><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, xo, stt, rec, ring,
-                                                                  sring, p->cfg.num_pages, p->cfg.spill_pages,
-                                                                  p->dev_pool, p->spill_dev, p->cfg.page_bytes,
-                                                                  p->cfg.page_tokens);
+            ap::k_dispatch_stash_copy<int2><<<grid, 256, 0, st>>>(
+                xs, T, rb[0], idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, stt, rec, ring, sring,
+                p->cfg.num_pages, p->cfg.spill_pages, p->dev_pool, p->spill_dev, p->cfg.page_bytes,
+                p->cfg.page_tokens);
         AP_CHECK_LAUNCH("dispatch_stash copy launch");
     }
     p->next_id += 1;
