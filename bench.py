@@ -194,8 +194,11 @@ class Step:
         torch.cuda.synchronize(device)
         self.R = wl.rows
         self.bytes = op_bytes(wl, self.R)
-        self.launches_per_step = wl.chunks * (1 + 4 + 2 + 2 + 1)
-        self.launches_per_step_fused = wl.chunks * (1 + 5 + 2 + 1)
+        # kernels per chunk: route 1; dispatch 3 (count/rank, scan, copy); push 2
+        # (plan, copy); pop 2 (plan, copy); combine 1.  Fused dispatch + push 3
+        # (count/rank, scan + plan, copy).
+        self.launches_per_step = wl.chunks * (1 + 3 + 2 + 2 + 1)
+        self.launches_per_step_fused = wl.chunks * (1 + 3 + 2 + 1)
 
     def run(self, events=None, fused=False):
         """Enqueue one step.  events: dict op -> list of (start, end) event pairs.

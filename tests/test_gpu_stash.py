@@ -224,3 +224,19 @@ def test_flags_device_pointer_is_the_sticky_word():
     assert ptr == t.g.meta.data_ptr() + 32
     word = t.g.meta[32:36].view(torch.int32)
     assert int(host(word)[0]) == t.o.state()["flags"] == ap.FLAG_POOL_OVERFLOW | ap.FLAG_SPILL_OVERFLOW
+
+
+def test_many_segments_plan_in_global_memory():
+    """More segments than the plan keeps in shared memory (2048): the plan
+    searches its tables in global memory; same results as the oracle."""
+    rng = np.random.default_rng(11)
+    nseg = 3000
+    live = rng.integers(0, 6, size=nseg).astype(np.int32)
+    seg_off = np.concatenate([[0], np.cumsum(live)[:-1]]).astype(np.int32)
+    rows = int(live.sum()) + 1
+    t = Twin(4, (16,), N=1200, S=1, R=2, segs=4096, maxp=4096)
+    src = rows_np(12, rows, 16)
+    t.push(0, [src], seg_off, live)
+    t.check(images=True)
+    t.pop(0, [(rows, 16)])
+    t.check(images=True)
