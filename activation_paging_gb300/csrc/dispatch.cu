@@ -227,6 +227,68 @@ __global__ void __launch_bounds__(256) k_copy_rows_e4m3(const uint16_t *__restri
     }
 }
 
+// E4M3 with the whole row held in registers (VE = 8 bf16 per 16-byte vector,
+// at most NR vectors per lane, i.e. H <= 256 * NR): one read of the row, amax
+// from registers, quantise once, store to every destination.  Same arithmetic
+// as k_copy_rows_e4m3.
+template <int NR>
+__global__ void __launch_bounds__(256) k_copy_rows_e4m3_reg(const uint16_t *__restrict__ x, int64_t T, int H,
+                                                            const int32_t *__restrict__ idx,
+                                                            int32_t *__restrict__ dest, int k, int E, int capacity,
+                                                            const int32_t *__restrict__ blk,
+                                                            const int32_t *__restrict__ seg_off,
+                                                            int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd,
+                                                            float *__restrict__ xd_scale)
+{
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int nstep = H / 8;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        const int32_t my_d =
+            (lane < k) ? finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity) : -1;
+        const int4 *row = reinterpret_cast<const int4 *>(x + t * H);
+        int4 v[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const int s = lane + i * kWarp;
+            v[i] = (s < nstep) ? ld_stream(row + s) : make_int4(0, 0, 0, 0);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            uint16_t e[8];
+            memcpy(e, &v[i], 16);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(e[q])));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+        const float inv = (amax == 0.f) ? 1.f : __fdiv_rn(448.f, amax);
+        if (lane < k && my_d >= 0) xd_scale[my_d] = scale;
+        // codes replace the values in place (8 code bytes in the vector's first half)
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            uint16_t e[8];
+            memcpy(e, &v[i], 16);
+            uint8_t q[8];
+#pragma unroll
+            for (int z = 0; z < 8; ++z) q[z] = to_e4m3(__fmul_rn(bf16_bits_to_f32(e[z]), inv));
+            memcpy(&v[i], q, 8);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+            if (d < 0) continue;
+            uint8_t *drow = xd + (int64_t)d * H;
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                const int s = lane + i * kWarp;
+                if (s < nstep) *reinterpret_cast<int2 *>(drow + (int64_t)s * 8) = make_int2(v[i].x, v[i].y);
+            }
+        }
+    }
+}
+
 __global__ void k_cast_e4m3(const float *__restrict__ in, uint8_t *__restrict__ out, int64_t n)
 {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
@@ -252,6 +314,16 @@ void launch_copy(const uint8_t *x, int64_t T, int64_t rb, const Ranks &r, uint8_
     const int64_t cap = (int64_t)sm_count() * 16;
     k_copy_rows<V><<<(int)(want < cap ? want : cap), 256, 0, st>>>(x, T, rb, r.idx, r.dest, r.k, r.E, r.capacity,
                                                                    r.blk, r.seg_off, r.src_tok, xd);
+}
+
+template <int NR>
+void launch_e4m3_reg(const uint16_t *x, int64_t T, int H, const Ranks &r, uint8_t *xd, float *xd_scale,
+                     cudaStream_t st)
+{
+    const int64_t want = (T + 7) / 8; // one warp per token
+    const int64_t cap = (int64_t)sm_count() * 16;
+    k_copy_rows_e4m3_reg<NR><<<(int)(want < cap ? want : cap), 256, 0, st>>>(
+        x, T, H, r.idx, r.dest, r.k, r.E, r.capacity, r.blk, r.seg_off, r.src_tok, xd, xd_scale);
 }
 
 template <int VE>
@@ -361,7 +433,13 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
         const uint16_t *xs = static_cast<const uint16_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         const uintptr_t ax = reinterpret_cast<uintptr_t>(x), ao = reinterpret_cast<uintptr_t>(xd);
-        if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0)
+        if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0 && H <= 256 * 4)
+            launch_e4m3_reg<4>(xs, T, H, ranks, xo, xd_scale, st);
+        else if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0 && H <= 256 * 8)
+            launch_e4m3_reg<8>(xs, T, H, ranks, xo, xd_scale, st);
+        else if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0 && H <= 256 * 9)
+            launch_e4m3_reg<9>(xs, T, H, ranks, xo, xd_scale, st);
+        else if (H % 8 == 0 && (ax & 15) == 0 && (ao & 7) == 0)
             launch_e4m3<8>(xs, T, H, ranks, xo, xd_scale, st);
         else if (H % 4 == 0 && (ax & 7) == 0 && (ao & 3) == 0)
             launch_e4m3<4>(xs, T, H, ranks, xo, xd_scale, st);

@@ -26,8 +26,17 @@ __device__ __forceinline__ void scan_body(int32_t *__restrict__ blk, int nblk, i
     const int per = (nblk + parts - 1) / parts;
     const int b0 = part * per;
     const int b1 = (b0 + per < nblk) ? b0 + per : nblk;
+    // short ranges stay in registers between the two passes (one round trip)
+    constexpr int kReg = 16;
+    const bool in_reg = per <= kReg;
+    int32_t cr[kReg];
     int32_t sum = 0;
-    if (active) {
+    if (active && in_reg) {
+#pragma unroll
+        for (int u = 0; u < kReg; ++u) cr[u] = (b0 + u < b1) ? blk[(int64_t)(b0 + u) * E + e] : 0;
+#pragma unroll
+        for (int u = 0; u < kReg; ++u) sum += cr[u];
+    } else if (active) {
         int b = b0;
         for (; b + 8 <= b1; b += 8) {
             int32_t c[8];
@@ -47,21 +56,29 @@ __device__ __forceinline__ void scan_body(int32_t *__restrict__ blk, int nblk, i
             if (p == part) run = total;
             total += s_tot[p * E + e];
         }
-        int b = b0;
-        for (; b + 8 <= b1; b += 8) {
-            int32_t c[8];
+        if (in_reg) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                blk[(int64_t)(b + u) * E + e] = run;
-                run += c[u];
+            for (int u = 0; u < kReg; ++u) {
+                if (b0 + u < b1) blk[(int64_t)(b0 + u) * E + e] = run;
+                run += cr[u];
             }
-        }
-        for (; b < b1; ++b) {
-            const int32_t c = blk[(int64_t)b * E + e];
-            blk[(int64_t)b * E + e] = run;
-            run += c;
+        } else {
+            int b = b0;
+            for (; b + 8 <= b1; b += 8) {
+                int32_t c[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) c[u] = blk[(int64_t)(b + u) * E + e];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    blk[(int64_t)(b + u) * E + e] = run;
+                    run += c[u];
+                }
+            }
+            for (; b < b1; ++b) {
+                const int32_t c = blk[(int64_t)b * E + e];
+                blk[(int64_t)b * E + e] = run;
+                run += c;
+            }
         }
     }
     // threads tid < E (part 0) own expert tid's totals

@@ -148,7 +148,13 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
     __shared__ int32_t s_off[kPlanSmemSegs], s_live[kPlanSmemSegs];
     const bool in_smem = nseg <= kPlanSmemSegs;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    // the free-ring counters, read early (only this kernel changes them now)
+    uint64_t head = 0, tail = 0, sh = 0, stl = 0;
     if (tid == 0) {
+        head = st->head;
+        tail = st->tail;
+        sh = st->spill_head;
+        stl = st->spill_tail;
         s_carry = 0;
         s_flags = 0;
     }
@@ -228,8 +234,6 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
     if (tid == 0) {
         uint32_t f = s_flags;
         if (total > max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
-        const uint64_t head = st->head, tail = st->tail;
-        const uint64_t sh = st->spill_head, stl = st->spill_tail;
         const int64_t avail = (int64_t)(tail - head);
         const int64_t savail = (int64_t)(stl - sh);
         const int64_t ndev = kept < avail ? kept : avail;
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
             }
         }
         const V *src = reinterpret_cast<const V *>(x + t * rb);
-        constexpr int U = 4;
+        constexpr int U = 8; // 8 vectors per lane in flight (a sweep on GB300 favoured 8 over 2 and 4)
         for (int64_t base = 0; base < nvec; base += U * kWarp) { // warp-uniform
             V r[U];
 #pragma unroll
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
                 for (int u = 0; u < U; ++u) {
                     const int64_t v = base + u * kWarp + lane;
                     if (v < nvec) {
-                        dst[v] = r[u];
+                        st_stream(dst + v, r[u]);
                         if (pdst) st_stream(pdst + v, r[u]);
                     }
                 }

@@ -55,6 +55,11 @@ def parse_args(argv=None):
     ap.add_argument("--unfused", action="store_true",
                     help="time the step with separate dispatch and push calls (default: the fused call)")
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other step variant")
+    ap.add_argument("--serial", action="store_true",
+                    help="capture the fused step on one stream (default: independent work on a second stream)")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["qwen3_moe", "skewed", "spill", "dsv2_lite_fp8", "dsv2_lite_fp8_h2056"],
+                    help="qwen3_moe (default) is the benchmark; the others time that workload's stash schedule")
     ap.add_argument("--overlap", action="store_true",
                     help="also measure reload (pop) overlapped with a bf16 GEMM on another stream")
     return ap.parse_args(argv)
@@ -172,6 +177,7 @@ class Step:
         self.pool = ap.Pool(wl.page_tokens, wl.page_bytes, wl.num_pages, wl.num_slots, 4, wl.E, wl.num_pages,
                             device=device)
         self.stream = self.pool.stream
+        self.side = torch.cuda.Stream(device=device, priority=-1)
         self.chunks = []
         for c in range(wl.chunks):
             seed = seed_base + c
@@ -229,6 +235,38 @@ class Step:
                 rec("pop", lambda: self.pool.pop(0, [d["dst"]]))
                 rec("combine", lambda: ap.combine_unpermute(d["y"], d["disp"]["dest"], d["w"], out=d["out"],
                                                             stream=s))
+
+    def run_concurrent(self):
+        """The fused step with its independent work forked to a second stream:
+        chunk 1's routing runs beside chunk 0's dispatch + push, and chunk 0's
+        combine beside chunk 1's pop.  Every pool call stays on the paging
+        stream.  Used for the captured graph (fork and join become graph edges)."""
+        torch, ap, wl, s = self.torch, self.ap, self.wl, self.stream
+        side = self.side
+        (h0, d0), (h1, d1) = self.chunks[0], self.chunks[1]
+        with torch.cuda.stream(s):
+            fork = torch.cuda.Event()
+            fork.record(s)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                ap.route_topk(d1["logits"], wl.k, d1["idx"], d1["w"], stream=side)
+                r1 = torch.cuda.Event()
+                r1.record(side)
+            ap.route_topk(d0["logits"], wl.k, d0["idx"], d0["w"], stream=s)
+            self.pool.dispatch_stash(0, d0["x"], d0["idx"], wl.E, out=d0["disp"])
+            s.wait_event(r1)
+            self.pool.dispatch_stash(0, d1["x"], d1["idx"], wl.E, out=d1["disp"])
+            self.pool.pop(0, [d0["dst"]])
+            p0 = torch.cuda.Event()
+            p0.record(s)
+            side.wait_event(p0)
+            with torch.cuda.stream(side):
+                ap.combine_unpermute(d0["y"], d0["disp"]["dest"], d0["w"], out=d0["out"], stream=side)
+                c0 = torch.cuda.Event()
+                c0.record(side)
+            self.pool.pop(0, [d1["dst"]])
+            ap.combine_unpermute(d1["y"], d1["disp"]["dest"], d1["w"], out=d1["out"], stream=s)
+            s.wait_event(c0)  # join
 
     def run_e2e_pipelined(self, state, fused=True):
         """One end-to-end step with host buffers: inputs are copied from pinned
@@ -383,6 +421,195 @@ def overlap_report(step, device, grid_bounds=(64, 152, 304, 608, 1216, 2048), re
     return out
 
 
+class ScheduleStep:
+    """One pass of another workload's stash schedule (skewed, spill, FP8 stack).
+
+    Every source (a chunk, a microbatch x layer, an interleaved F/B source)
+    is routed, dispatched and pushed into its slot; every pop reloads it and
+    the combine un-permutes the (synthetic) expert outputs.  BF16 sources use
+    the fused dispatch + push; the E4M3 stack dispatches, then pushes two
+    planes (codes and scales)."""
+
+    def __init__(self, wl, device):
+        import torch
+        import activation_paging_gb300 as ap
+        from activation_paging_gb300 import inputs
+
+        self.torch, self.ap, self.wl, self.device = torch, ap, wl, device
+        if wl.name.startswith("dsv2"):
+            srcs = [(f"m{m}l{l}", 1000 + m * wl.layers + l, l, 100 + m)
+                    for m in range(wl.microbatches) for l in range(wl.layers)]
+            sched = [("push", n) for n, *_ in srcs]
+            sched += [("pop", f"m{m}l{l}") for m in range(wl.microbatches) for l in reversed(range(wl.layers))]
+            records, maxp = wl.microbatches, 4096
+        elif wl.name == "spill":
+            srcs = [("a0", 0, 0, 0), ("b0", 1, 1, 1), ("a1", 2, 0, 2)]
+            sched = [("push", "a0"), ("push", "b0"), ("pop", "a0"), ("push", "a1"), ("pop", "b0"), ("pop", "a1")]
+            records, maxp = 2, 8192
+        else:
+            srcs = [("a", 0, 0, 0)]
+            sched = [("push", "a"), ("pop", "a")]
+            records, maxp = 2, wl.num_pages
+        self.sched = sched
+        self.pool = ap.Pool(wl.page_tokens, wl.page_bytes, wl.num_pages, max(wl.num_slots, 1), records, wl.E, maxp,
+                            wl.spill_pages, device=device)
+        self.stream = self.pool.stream
+        C = wl.capacity
+        xs = {}
+        self.src = {}
+        for name, lseed, slot, xseed in srcs:
+            if xseed not in xs:
+                x = inputs.normal_bf16(xseed, inputs.X_STREAM, (wl.T, wl.H))
+                xs[xseed] = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+            logits = torch.from_numpy(inputs.router_logits(lseed, wl.T, wl.E, wl.zipf_s, wl.zipf_beta)).to(device)
+            d = {"slot": slot, "x": xs[xseed], "logits": logits,
+                 "idx": torch.empty((wl.T, wl.k), dtype=torch.int32, device=device),
+                 "w": torch.empty((wl.T, wl.k), dtype=torch.float32, device=device)}
+            self.stream.wait_stream(torch.cuda.current_stream())
+            ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=self.stream)
+            d["disp"] = ap.dispatch_permute(d["x"], d["idx"], wl.E, C, wl.padded, fp8=wl.fp8, stream=self.stream)
+            self.src[name] = d
+        rows = wl.rows
+        y = inputs.normal_bf16(7, inputs.Y_STREAM, (rows, wl.H))
+        self.y = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).to(device)
+        self.out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device)
+        if wl.fp8:
+            self.dst = [torch.empty((rows, wl.H), dtype=torch.uint8, device=device),
+                        torch.empty(rows, dtype=torch.float32, device=device)]
+        else:
+            self.dst = [torch.empty((rows, wl.H), dtype=torch.bfloat16, device=device)]
+        torch.cuda.synchronize(device)
+        rb = wl.row_bytes
+        # algorithmic bytes use the rows actually kept (drops and padding move nothing)
+        kept = [int(d["disp"]["live"].sum()) for d in self.src.values()]
+        T, H, E, k, R = wl.T, wl.H, wl.E, wl.k, sum(kept) / len(kept)
+        plane_bytes = R * sum(rb)
+        self.bytes = {"route": T * E * 4 + T * k * 8,
+                      "dispatch": T * H * 2 + plane_bytes + T * k * 8 + R * 4,
+                      "push": 2 * plane_bytes,
+                      "dispatch_stash": T * H * 2 + 2 * plane_bytes + T * k * 8 + R * 4,
+                      "pop": 2 * plane_bytes,
+                      "combine": R * H * 2 + T * H * 2 + T * k * 8}
+        self.tokens = T * sum(1 for op, _ in sched if op == "push")
+        self.rows_kept = R
+        self.launches = sum((1 + (3 if not wl.fp8 else 5)) if op == "push" else 3 for op, _ in sched)
+
+    def spilled_bytes(self):
+        """Bytes one pass of the schedule sends over the host link: every
+        spilled page is written at its push and read back at its pop."""
+        torch = self.torch
+        total = 0
+        with torch.cuda.stream(self.stream):
+            for op, name in self.sched:
+                d = self.src[name]
+                if op == "push":
+                    self.run_one(op, name)
+                    torch.cuda.synchronize(self.device)
+                    rec = self.pool.record(d["slot"], self.pool.queue_len(d["slot"]) - 1)
+                    total += int(rec["nrows"][rec["ndev"]:rec["ndev"] + rec["nspill"]].sum()) * sum(self.wl.row_bytes)
+                else:
+                    self.run_one(op, name)
+        torch.cuda.synchronize(self.device)
+        return 2 * total
+
+    def run_one(self, op, name):
+        self.sched_backup, self.sched = self.sched, [(op, name)]
+        try:
+            self.run()
+        finally:
+            self.sched = self.sched_backup
+
+    def run(self, events=None):
+        torch, ap, wl, s = self.torch, self.ap, self.wl, self.stream
+
+        def rec(name, fn):
+            if events is None:
+                fn()
+                return
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            events.setdefault(name, []).append((a, b))
+
+        with torch.cuda.stream(s):
+            for op, name in self.sched:
+                d = self.src[name]
+                if op == "push":
+                    rec("route", lambda: ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=s))
+                    if wl.fp8:
+                        rec("dispatch", lambda: ap.dispatch_permute(d["x"], d["idx"], wl.E, wl.capacity, wl.padded,
+                                                                    fp8=True, out=d["disp"], stream=s))
+                        rec("push", lambda: self.pool.push(d["slot"], [d["disp"]["xd"], d["disp"]["xd_scale"]],
+                                                           d["disp"]["seg_off"], d["disp"]["live"]))
+                    else:
+                        rec("dispatch_stash", lambda: self.pool.dispatch_stash(d["slot"], d["x"], d["idx"], wl.E,
+                                                                               wl.capacity, wl.padded,
+                                                                               out=d["disp"]))
+                else:
+                    rec("pop", lambda: self.pool.pop(d["slot"], self.dst))
+                    rec("combine", lambda: ap.combine_unpermute(self.y, d["disp"]["dest"], d["w"], out=self.out,
+                                                                stream=s))
+
+
+def native_schedule(args):
+    """Time one other workload's schedule (graph replay) and its per-call rates."""
+    import torch
+    from activation_paging_gb300 import inputs, build as cuda_build
+
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    cuda_build.build()
+    wl = inputs.WORKLOADS[args.workload]
+    st = ScheduleStep(wl, device)
+    for _ in range(max(args.warmup, 3)):
+        st.run()
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st.stream):
+        st.run()
+    for _ in range(2):
+        with torch.cuda.stream(st.stream):
+            g.replay()
+    torch.cuda.synchronize(device)
+    steps = max(1, args.steps)
+    sampler = ClockSampler(0)
+    time.sleep(0.3)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st.stream)
+    for _ in range(steps):
+        with torch.cuda.stream(st.stream):
+            g.replay()
+    b.record(st.stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    el = a.elapsed_time(b) / 1e3
+    events = {}
+    for _ in range(max(1, min(args.op_steps, steps))):
+        st.run(events)
+    torch.cuda.synchronize(device)
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
+    ops = {}
+    for name, pairs in events.items():
+        ms = sum(x.elapsed_time(y) for x, y in pairs) / len(pairs)
+        gbs = st.bytes[name] / (ms / 1e3) / 1e9
+        ops[name] = {"ms": round(ms, 5), "bytes": st.bytes[name], "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    flags = st.pool.overflow()
+    link = st.spilled_bytes() if wl.spill_pages else 0
+    line = {"metric": METRIC, "workload": wl.name, "value": round(st.tokens * steps / el, 1), "unit": "tokens/s",
+            "rows_kept_per_record": round(st.rows_kept, 1), "host_link_bytes_per_step": link,
+            "ms_per_step": round(el * 1e3 / steps, 4), "steps": steps, "tokens_per_step": st.tokens,
+            "config": {"T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "capacity": wl.capacity, "padded": wl.padded,
+                       "fp8": wl.fp8, "page_tokens": wl.page_tokens, "num_pages": wl.num_pages,
+                       "spill_pages": wl.spill_pages, "schedule": [f"{op} {n}" for op, n in st.sched][:12]},
+            "ops": ops, "pool_flags": flags, "gpu_launches": st.launches * steps, "clocks": clocks,
+            "note": "ops: mean CUDA-event time per call over eager passes; pops of spilled records read host memory"}
+    print(json.dumps(line), flush=True)
+
+
 def kernel_hash() -> str:
     """Hash of the stash copy kernels' device source (their kernels and the
     shared device copy helper), so recorded ncu traffic is used only while
@@ -422,7 +649,10 @@ def native(args):
     def capture(fused):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=step.stream):
-            step.run(fused=fused)
+            if fused and wl.chunks == 2 and not args.serial:
+                step.run_concurrent()
+            else:
+                step.run(fused=fused)
         for _ in range(3):
             with torch.cuda.stream(step.stream):
                 g.replay()
@@ -562,7 +792,10 @@ def native(args):
                            "hbm_gbs_step": round(total_bytes / (ms_per_step / 1e3) / 1e9, 1),
                            "l2": "working set per step ~1.4 GB > 126 MB L2: no flush",
                            "parallelism": f"replicas x{world}", "stream": "one high-priority stream",
-                           "launch": "eager" if graph is None else "CUDA graph of one step, replayed",
+                           "launch": ("eager" if graph is None else
+                                      "CUDA graph of one step, replayed" + ("" if (args.serial or not fused_main)
+                                                                            else "; chunk 1 routing and chunk 0 "
+                                                                                 "combine on a second stream")),
                            "step": ("route, fused dispatch + push, pop, combine per chunk" if fused_main
                                     else "route, dispatch, push, pop, combine per chunk")},
                 "roofline": roofline, "ops": ops, "alt": alt, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
@@ -663,6 +896,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         reference(args)
+    elif args.workload != WORKLOAD:
+        native_schedule(args)
     else:
         native(args)
 
