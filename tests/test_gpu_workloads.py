@@ -62,7 +62,8 @@ def check_pages(g: "ap.Pool", rec: dict, planes, page_bytes, plane_off, nsample=
             assert torch.equal(page[off:off + nr * rb], want)
 
 
-def test_qwen3_moe_two_chunks():
+@pytest.mark.parametrize("fused", [False, True])
+def test_qwen3_moe_two_chunks(fused):
     wl = inputs.WORKLOADS["qwen3_moe"]
     rb = wl.row_bytes
     g = ap.Pool(wl.page_tokens, wl.page_bytes, wl.num_pages, 1, 4, wl.E, wl.num_pages, fill=0xA5)
@@ -74,14 +75,21 @@ def test_qwen3_moe_two_chunks():
         idx_o, w_o = oracle.route_topk(logits, wl.k)
         plan = oracle.dispatch(x, idx_o, wl.E, 0, False)
         idx, w = ap.route_topk(to_dev(logits), wl.k)
-        d = ap.dispatch_permute(bf16_to_dev(x), idx, wl.E)
+        if fused:
+            g.stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(g.stream):
+                d = g.dispatch_stash(0, bf16_to_dev(x), idx, wl.E)
+            torch.cuda.synchronize()
+        else:
+            d = ap.dispatch_permute(bf16_to_dev(x), idx, wl.E)
         assert np.array_equal(host(idx), idx_o)
         assert np.all(np.abs(host(w).astype(np.float64) - w_o) <= route_tolerance(logits, idx_o, w_o))
         for key in ("counts", "live", "seg_off", "dest"):
             assert np.array_equal(host(d[key]), plan[key]), key
         assert np.array_equal(bf16_to_host(d["xd"]), plan["xd"])
-        g.stream.wait_stream(torch.cuda.current_stream())
-        g.push(0, [d["xd"]], d["seg_off"], d["live"])
+        if not fused:
+            g.stream.wait_stream(torch.cuda.current_stream())
+            g.push(0, [d["xd"]], d["seg_off"], d["live"])
         o.push_rb(0, rb, plan["rows"], plan["seg_off"], plan["live"])
         chunks.append((d, w_o, plan))
     torch.cuda.synchronize()
@@ -195,9 +203,11 @@ def test_dsv2_lite_fp8_layer_stack(H):
     compare_pool(g, o, range(wl.layers))
 
 
-def test_spill_two_sources_interleaved():
+@pytest.mark.parametrize("fused", [False, True])
+def test_spill_two_sources_interleaved(fused):
     """Pool at 60% of two live records: the second source spills to pinned host
-    memory, the overflow flag stays set, reloads are byte-exact."""
+    memory, the overflow flag stays set, reloads are byte-exact.  With
+    ``fused`` every push is the fused dispatch + push call."""
     wl = inputs.WORKLOADS["spill"]
     rb = wl.row_bytes
     g = ap.Pool(wl.page_tokens, wl.page_bytes, wl.num_pages, 2, 2, wl.E, 8192, wl.spill_pages, fill=0xA5)
@@ -217,12 +227,20 @@ def test_spill_two_sources_interleaved():
         rows = np.random.default_rng(seed).choice(plan["rows"], 2048, replace=False)
         got = bf16_to_host(d["xd"][torch.from_numpy(rows).cuda()])
         assert np.array_equal(got, x[plan["src_tok"][rows]])
+        d["x_dev"], d["idx_dev"] = bf16_to_dev(x), idx
         data[name] = (d, plan, x, w_o)
 
     def push(slot, name):
         d, plan, _, _ = data[name]
         g.stream.wait_stream(torch.cuda.current_stream())
-        g.push(slot, [d["xd"]], d["seg_off"], d["live"])
+        if fused:
+            dest_before = d["dest"].clone()
+            with torch.cuda.stream(g.stream):
+                g.dispatch_stash(slot, d["x_dev"], d["idx_dev"], wl.E, out=d)
+            torch.cuda.synchronize()
+            assert torch.equal(d["dest"], dest_before)
+        else:
+            g.push(slot, [d["xd"]], d["seg_off"], d["live"])
         o.push_rb(slot, rb, plan["rows"], plan["seg_off"], plan["live"])
 
     def pop(slot, name):
