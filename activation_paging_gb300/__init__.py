@@ -272,9 +272,11 @@ class Pool:
         return rid.value
 
     def dispatch_stash(self, slot: int, x: torch.Tensor, idx: torch.Tensor, E: int, capacity: int = 0,
-                       padded: bool = False, out: dict | None = None, status: torch.Tensor | None = None):
-        """Fused dispatch (BF16) + push into ``slot``: returns the dispatch
-        dict (as ``dispatch_permute``) with the record id under ``record_id``."""
+                       padded: bool = False, fp8: bool = False, out: dict | None = None,
+                       status: torch.Tensor | None = None):
+        """Fused dispatch + push into ``slot`` (BF16 rows, or E4M3 codes and
+        row scales as two planes): returns the dispatch dict (as
+        ``dispatch_permute``) with the record id under ``record_id``."""
         _need(x, torch.bfloat16, "x")
         _need(idx, torch.int32, "idx")
         T, H = x.shape
@@ -283,7 +285,9 @@ class Pool:
         rows = E * capacity if padded else T * k
         o = dict(out) if out is not None else {}
         if "xd" not in o:
-            o["xd"] = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+            o["xd"] = torch.empty((rows, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+        if fp8 and "xd_scale" not in o:
+            o["xd_scale"] = torch.empty(rows, dtype=torch.float32, device=dev)
         for name, shape in (("counts", (E,)), ("live", (E,)), ("seg_off", (E,)), ("dest", (T, k))):
             if name not in o:
                 o[name] = torch.empty(shape, dtype=torch.int32, device=dev)
@@ -295,7 +299,8 @@ class Pool:
         self._order_after_caller([x, idx, status] + [v for v in o.values() if isinstance(v, torch.Tensor)])
         rid = ctypes.c_uint64()
         xd = o["xd"]
-        check(self.lib.ap_dispatch_stash(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity, int(padded), _p(xd),
+        check(self.lib.ap_dispatch_stash(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity, int(padded),
+                                         DTYPE_E4M3 if fp8 else DTYPE_BF16, _p(xd), _p(o.get("xd_scale") if fp8 else None),
                                          xd.shape[0], _p(o["counts"]), _p(o["live"]), _p(o["seg_off"]),
                                          _p(o["dest"]), _p(o["src_tok"]), _p(o["scratch"]), o["scratch"].numel(),
                                          _p(status), ctypes.byref(rid), self.stream.cuda_stream), "dispatch_stash")

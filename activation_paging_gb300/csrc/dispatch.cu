@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(1024) k_scan(int32_t *__restrict__ blk, int nb
                                                 int padded, int32_t *__restrict__ counts,
                                                 int32_t *__restrict__ live, int32_t *__restrict__ seg_off)
 {
-    scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off);
+    int32_t my_live, my_off;
+    scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off, my_live, my_off);
 }
 
 // Block histograms and stable in-block ranks, in one pass over idx.  The
@@ -132,12 +133,6 @@ __global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x
 }
 
 // ---- E4M3 quantise + copy: one warp per token -------------------------------
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-__device__ __forceinline__ uint8_t to_e4m3(float v)
-{
-    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-}
 
 // VE bf16 elements per lane step: 8 (16-byte loads, 8-byte stores), 4, 2 or 1.
 template <int VE>

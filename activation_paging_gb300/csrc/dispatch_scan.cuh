@@ -2,6 +2,8 @@
 // and the fused scan + stash plan kernel (stash.cu).
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "ap_common.cuh"
 
 namespace ap {
@@ -13,9 +15,11 @@ constexpr int kTokPerBlk = 64; // tokens per count/rank block
 // Thread (e, part) owns expert e over a contiguous range of blocks: it sums
 // its range, adds the sums of the earlier parts, then rewrites its range as
 // running bases.  Then counts, live = min(count, C) and segment offsets.
+// my_live / my_off: thread tid < E also returns expert tid's live count and
+// segment offset in registers (for a page plan run by the same CTA).
 __device__ __forceinline__ void scan_body(int32_t *__restrict__ blk, int nblk, int E, int capacity, int padded,
                                           int32_t *__restrict__ counts, int32_t *__restrict__ live,
-                                          int32_t *__restrict__ seg_off)
+                                          int32_t *__restrict__ seg_off, int32_t &my_live, int32_t &my_off)
 {
     __shared__ int32_t s_tot[1024];
     __shared__ int32_t s_warp[32];
@@ -108,7 +112,17 @@ __device__ __forceinline__ void scan_body(int32_t *__restrict__ blk, int nblk, i
     }
     __syncthreads();
     const int32_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
-    if (tid < E) seg_off[tid] = padded ? tid * capacity : incl - l;
+    my_live = l;
+    my_off = padded ? tid * capacity : incl - l;
+    if (tid < E) seg_off[tid] = my_off;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// E4M3 code of a float: round to nearest even, finite overflow saturates.
+__device__ __forceinline__ uint8_t to_e4m3(float v)
+{
+    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
 
 // Row of pair (t, j) from its in-block rank (left in dest by k_count_rank) and

@@ -134,10 +134,13 @@ __global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int32_t *sp
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSmemSegs = 2048; // segments whose tables the plan keeps in shared memory
 
+// have_reg: nseg <= kPlanThreads and thread s already holds segment s's
+// offset and live count in reg_off / reg_live (fused scan + plan).
 __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, int nseg,
                                                const int32_t *__restrict__ d_seg_off,
                                                const int32_t *__restrict__ d_live, int64_t src_rows, int P,
-                                               int64_t max_pages, int64_t N, int64_t SP)
+                                               int64_t max_pages, int64_t N, int64_t SP, bool have_reg = false,
+                                               int32_t reg_off = 0, int32_t reg_live = 0)
 {
     __shared__ int64_t s_warp[kPlanThreads / kWarp];
     __shared__ int64_t s_carry;
@@ -164,8 +167,8 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
         const int s = base + tid;
         int64_t n = 0;
         if (s < nseg) {
-            const int32_t o = d_seg_off[s];
-            int32_t l = d_live[s];
+            const int32_t o = have_reg ? reg_off : d_seg_off[s];
+            int32_t l = have_reg ? reg_live : d_live[s];
             if (l < 0 || o < 0 || (int64_t)o + (int64_t)l > src_rows) {
                 atomicOr(&s_flags, AP_FLAG_BAD_COUNT);
                 l = 0;
@@ -277,9 +280,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_scan_plan(int32_t *__restrict_
                                                              RecPtr rec, int64_t src_rows, int P, int64_t max_pages,
                                                              int64_t N, int64_t SP)
 {
-    scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off);
+    int32_t my_live, my_off;
+    scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off, my_live, my_off);
     __syncthreads();
-    push_plan_body(st, rec, E, seg_off, live, src_rows, P, max_pages, N, SP);
+    push_plan_body(st, rec, E, seg_off, live, src_rows, P, max_pages, N, SP, E <= kPlanThreads, my_off, my_live);
 }
 
 struct Planes {
@@ -457,6 +461,109 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
                         st_stream(dst + v, r[u]);
                         if (pdst) st_stream(pdst + v, r[u]);
                     }
+                }
+            }
+        }
+    }
+}
+
+// Fused dispatch + push for E4M3 payloads: the token row is held in registers
+// (NR 16-byte vectors per lane, H <= 256 * NR), quantised once with its row
+// scale (same arithmetic as the E4M3 dispatch), and each kept pair's codes and
+// scale go to its dispatch row and to its page (codes at row r, scale in the
+// page's second plane).  The pair holding row 0 of a page records the page.
+template <int NR>
+__global__ void __launch_bounds__(256, 3) k_dispatch_stash_e4m3(
+    const uint16_t *__restrict__ x, int64_t T, int H, const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
+    int k, int E, int capacity, const int32_t *__restrict__ blk, const int32_t *__restrict__ seg_off,
+    int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd, float *__restrict__ xd_scale, ap_pool_state *st,
+    RecPtr rec, const int32_t *__restrict__ ring, const int32_t *__restrict__ spill_ring, int64_t N, int64_t SP,
+    uint8_t *pool, uint8_t *spill, int64_t page_bytes, int P, int64_t plane1_off)
+{
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int nstep = H / 8;
+    const int64_t npages = rec.hdr->npages;
+    const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
+    const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+        int32_t my_d = -1;
+        uint8_t *my_row = nullptr;   // this lane's pair: codes row in its page
+        float *my_scale = nullptr;   // and its scale slot in the page's second plane
+        if (lane < k) {
+            my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
+            const int e = idx[t * k + lane];
+            if (my_d >= 0 && e >= 0 && e < E) {
+                const int64_t r = (int64_t)my_d - rec.seg_off[e];
+                if (r >= 0 && r < rec.live[e]) {
+                    const int64_t ord = rec.pg_base[e] + r / P;
+                    if (ord < npages) {
+                        int64_t id = -1;
+                        if (ord < ndev) id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
+                        else if (ord < ndev + nspill)
+                            id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
+                        const bool ok = (ord < ndev) ? (id >= 0 && id < N)
+                                                     : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
+                        if (!ok) {
+                            atomicOr(&st->flags, AP_FLAG_CORRUPT);
+                            id = -1;
+                        }
+                        if (r % P == 0) rec.page_table[ord] = (int32_t)id; // row 0 of the page records it
+                        if (id >= 0) {
+                            uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+                            my_row = page + (r % P) * H;
+                            my_scale = reinterpret_cast<float *>(page + plane1_off + (r % P) * 4);
+                        }
+                    }
+                }
+            }
+        }
+        const int4 *row = reinterpret_cast<const int4 *>(x + t * H);
+        int4 v[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const int s = lane + i * kWarp;
+            v[i] = (s < nstep) ? ld_stream(row + s) : make_int4(0, 0, 0, 0);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            uint16_t e8[8];
+            memcpy(e8, &v[i], 16);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(e8[q])));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+        const float inv = (amax == 0.f) ? 1.f : __fdiv_rn(448.f, amax);
+        if (my_d >= 0) {
+            xd_scale[my_d] = scale;
+            if (my_scale) *my_scale = scale;
+        }
+#pragma unroll
+        for (int i = 0; i < NR; ++i) { // codes replace the values in place
+            uint16_t e8[8];
+            memcpy(e8, &v[i], 16);
+            uint8_t q[8];
+#pragma unroll
+            for (int z = 0; z < 8; ++z) q[z] = to_e4m3(__fmul_rn(bf16_bits_to_f32(e8[z]), inv));
+            memcpy(&v[i], q, 8);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+            const unsigned long long pg =
+                __shfl_sync(0xffffffffu, (unsigned long long)reinterpret_cast<uintptr_t>(my_row), j);
+            if (d < 0) continue;
+            uint8_t *drow = xd + (int64_t)d * H;
+            uint8_t *prow = reinterpret_cast<uint8_t *>(static_cast<uintptr_t>(pg));
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                const int s = lane + i * kWarp;
+                if (s < nstep) {
+                    const int2 c = make_int2(v[i].x, v[i].y);
+                    st_stream(reinterpret_cast<int2 *>(drow + (int64_t)s * 8), c);
+                    if (prow) st_stream(reinterpret_cast<int2 *>(prow + (int64_t)s * 8), c);
                 }
             }
         }
@@ -738,9 +845,10 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
 
 extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, int64_t T, int32_t H,
                                        const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
-                                       void *xd, int64_t xd_rows, int32_t *counts, int32_t *live, int32_t *seg_off,
-                                       int32_t *dest, int32_t *src_tok, void *scratch, int64_t scratch_bytes,
-                                       uint32_t *d_status, uint64_t *record_id, void *stream)
+                                       int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows,
+                                       int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest,
+                                       int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
+                                       uint64_t *record_id, void *stream)
 {
     using namespace ap;
     if (!p) return fail(AP_EINVAL, "dispatch_stash: NULL pool");
@@ -751,16 +859,24 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
     if (s != AP_OK) return s;
     if (E > p->cfg.max_segments)
         return fail(AP_EINVAL, "dispatch_stash: E=%d segments > max_segments %d", E, p->cfg.max_segments);
-    int64_t rb[2] = {(int64_t)H * 2, 0};
+    if (out_dtype != AP_DTYPE_BF16 && out_dtype != AP_DTYPE_E4M3)
+        return fail(AP_EINVAL, "dispatch_stash: unknown out_dtype %d", out_dtype);
+    const bool fp8 = out_dtype == AP_DTYPE_E4M3;
+    const int nplanes = fp8 ? 2 : 1;
+    int64_t rb[2] = {fp8 ? (int64_t)H : (int64_t)H * 2, fp8 ? 4 : 0};
     int64_t page_off[2];
-    if (!plane_fit(p, 1, rb, page_off)) return fail(AP_EINVAL, "dispatch_stash: a BF16 row of H=%d does not fit", H);
+    if (!plane_fit(p, nplanes, rb, page_off))
+        return fail(AP_EINVAL, "dispatch_stash: the rows of H=%d do not fit a page", H);
+    if (fp8 && T > 0 && !xd_scale) return fail(AP_EINVAL, "dispatch_stash: E4M3 needs xd_scale");
     if (p->q_count[slot] >= p->cfg.max_records_per_slot)
         return fail(AP_EQFULL, "dispatch_stash: slot %d queue full", slot);
     const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xd) |
                          reinterpret_cast<uintptr_t>(p->dev_pool) | reinterpret_cast<uintptr_t>(p->spill_dev) |
                          (uintptr_t)rb[0] | (uintptr_t)p->cfg.page_bytes;
-    if (T > 0 && (al & 15) != 0 && (al & 7) != 0)
+    if (!fp8 && T > 0 && (al & 15) != 0 && (al & 7) != 0)
         return fail(AP_ENOTSUP, "dispatch_stash: rows must be 8-byte aligned (H %% 4 == 0)");
+    if (fp8 && T > 0 && (H % 8 != 0 || H > 256 * 16 || (reinterpret_cast<uintptr_t>(x) & 15) != 0 || (al & 7) != 0))
+        return fail(AP_ENOTSUP, "dispatch_stash: E4M3 needs H %% 8 == 0, H <= 4096 and aligned buffers");
     cudaStream_t st = p->stream;
     s = dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
     if (s != AP_OK) return s;
@@ -770,9 +886,9 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
     HostRec &h = p->q[index];
     h.id = p->next_id;
     h.index = index;
-    h.nplanes = 1;
+    h.nplanes = nplanes;
     h.rb[0] = rb[0];
-    h.rb[1] = 0;
+    h.rb[1] = rb[1];
     const int64_t P = p->cfg.page_tokens;
     int64_t rpt = 32768 / rb[0];
     if (rpt < 1) rpt = 1;
@@ -798,7 +914,19 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
         const uint8_t *xs = static_cast<const uint8_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         const int32_t *blk = static_cast<const int32_t *>(scratch);
-        if ((al & 15) == 0)
+        if (fp8) {
+            const uint16_t *xs16 = static_cast<const uint16_t *>(x);
+#define AP_LAUNCH_E4M3(NRV)                                                                                       \
+    ap::k_dispatch_stash_e4m3<NRV><<<grid, 256, 0, st>>>(                                                         \
+        xs16, T, H, idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, xd_scale, stt, rec, ring, sring,         \
+        p->cfg.num_pages, p->cfg.spill_pages, p->dev_pool, p->spill_dev, p->cfg.page_bytes, p->cfg.page_tokens,    \
+        page_off[1])
+            if (H <= 256 * 4) AP_LAUNCH_E4M3(4);
+            else if (H <= 256 * 8) AP_LAUNCH_E4M3(8);
+            else if (H <= 256 * 9) AP_LAUNCH_E4M3(9);
+            else AP_LAUNCH_E4M3(16);
+#undef AP_LAUNCH_E4M3
+        } else if ((al & 15) == 0)
             ap::k_dispatch_stash_copy<int4><<<grid, 256, 0, st>>>(
                 xs, T, rb[0], idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, stt, rec, ring, sring,
                 p->cfg.num_pages, p->cfg.spill_pages, p->dev_pool, p->spill_dev, p->cfg.page_bytes,

@@ -427,9 +427,9 @@ class ScheduleStep:
 
     Every source (a chunk, a microbatch x layer, an interleaved F/B source)
     is routed, dispatched and pushed into its slot; every pop reloads it and
-    the combine un-permutes the (synthetic) expert outputs.  BF16 sources use
-    the fused dispatch + push; the E4M3 stack dispatches, then pushes two
-    planes (codes and scales)."""
+    the combine un-permutes the (synthetic) expert outputs.  Every push is the
+    fused dispatch + push (BF16 rows, or E4M3 codes and row scales as two
+    planes)."""
 
     def __init__(self, wl, device):
         import torch
@@ -493,7 +493,7 @@ class ScheduleStep:
                       "combine": R * H * 2 + T * H * 2 + T * k * 8}
         self.tokens = T * sum(1 for op, _ in sched if op == "push")
         self.rows_kept = R
-        self.launches = sum((1 + (3 if not wl.fp8 else 5)) if op == "push" else 3 for op, _ in sched)
+        self.launches = sum(4 if op == "push" else 3 for op, _ in sched)
 
     def spilled_bytes(self):
         """Bytes one pass of the schedule sends over the host link: every
@@ -539,15 +539,9 @@ class ScheduleStep:
                 d = self.src[name]
                 if op == "push":
                     rec("route", lambda: ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=s))
-                    if wl.fp8:
-                        rec("dispatch", lambda: ap.dispatch_permute(d["x"], d["idx"], wl.E, wl.capacity, wl.padded,
-                                                                    fp8=True, out=d["disp"], stream=s))
-                        rec("push", lambda: self.pool.push(d["slot"], [d["disp"]["xd"], d["disp"]["xd_scale"]],
-                                                           d["disp"]["seg_off"], d["disp"]["live"]))
-                    else:
-                        rec("dispatch_stash", lambda: self.pool.dispatch_stash(d["slot"], d["x"], d["idx"], wl.E,
-                                                                               wl.capacity, wl.padded,
-                                                                               out=d["disp"]))
+                    rec("dispatch_stash", lambda: self.pool.dispatch_stash(d["slot"], d["x"], d["idx"], wl.E,
+                                                                           wl.capacity, wl.padded, fp8=wl.fp8,
+                                                                           out=d["disp"]))
                 else:
                     rec("pop", lambda: self.pool.pop(d["slot"], self.dst))
                     rec("combine", lambda: ap.combine_unpermute(self.y, d["disp"]["dest"], d["w"], out=self.out,

@@ -331,18 +331,21 @@ ap_status ap_stash_push(ap_pool *pool, int32_t slot, int32_t nplanes,
 
 /* Fused dispatch + push (the stash commit made by the producer of the rows:
  * torchtitan pull 5541, "AI-Generated Details", first paragraph).  Exactly
- * the results of ap_dispatch_permute(..., AP_DTYPE_BF16, ...) followed by
- * ap_stash_push(pool, slot, 1, {xd}, {2*H}, xd_rows, E, seg_off, live, ...):
- * the same xd rows, counts, live, seg_off, dest, src_tok, record, page table,
+ * the results of ap_dispatch_permute(..., out_dtype, ...) followed by
+ * ap_stash_push(pool, slot, planes, ..., xd_rows, E, seg_off, live, ...)
+ * with planes = {xd} (BF16 rows of 2H bytes) or {xd, xd_scale} (E4M3 rows of
+ * H bytes + 4-byte scales): the same dispatch outputs, record, page table,
  * pool bytes and flags; but each token row is read once and written to its
  * dispatch rows and its pages in the same pass, so the push does not read xd
- * back.  Runs on the paging stream.  BF16 payload only; rows must be 8-byte
- * aligned (H % 4 == 0 and 8-aligned buffers), else AP_ENOTSUP.  Arguments as
- * in the two calls; E must not exceed max_segments. */
+ * back.  Runs on the paging stream.  BF16 rows must be 8-byte aligned
+ * (H % 4 == 0, 8-aligned buffers); E4M3 needs H % 8 == 0, H <= 4096, x
+ * 16-aligned and xd 8-aligned; otherwise AP_ENOTSUP.  E must not exceed
+ * max_segments. */
 ap_status ap_dispatch_stash(ap_pool *pool, int32_t slot, const void *x,
                             int64_t T, int32_t H, const int32_t *idx,
                             int32_t k, int32_t E, int32_t capacity,
-                            int32_t padded, void *xd, int64_t xd_rows,
+                            int32_t padded, int32_t out_dtype, void *xd,
+                            float *xd_scale, int64_t xd_rows,
                             int32_t *counts, int32_t *live, int32_t *seg_off,
                             int32_t *dest, int32_t *src_tok, void *scratch,
                             int64_t scratch_bytes, uint32_t *d_status,

@@ -102,6 +102,51 @@ def test_fused_host_errors():
         with torch.cuda.stream(g.stream):
             g.dispatch_stash(0, x, idx, 4)
     assert e.value.status == -6
-    rc = g.lib.ap_dispatch_stash(g.handle, 0, None, 0, 8, None, 2, 4, 0, 0, None, 0, None, None, None, None, None,
-                                 None, 0, None, None, torch.cuda.Stream().cuda_stream)
+    rc = g.lib.ap_dispatch_stash(g.handle, 0, None, 0, 8, None, 2, 4, 0, 0, 0, None, None, 0, None, None, None, None,
+                                 None, None, 0, None, None, torch.cuda.Stream().cuda_stream)
     assert rc == -5  # not the paging stream
+
+
+@pytest.mark.parametrize("T,H,E,k,P,N,SP", [
+    (4096, 2048, 64, 6, 128, 120, 0),    # the FP8 layer-stack shape (register path, 8 vectors per lane)
+    (999, 2056, 64, 6, 128, 40, 64),     # odd hidden size, ragged tail, spill
+    (300, 1024, 16, 4, 32, 20, 4),       # 4 vectors per lane; lost pages
+])
+def test_fused_e4m3_matches_oracle(T, H, E, k, P, N, SP):
+    rb = (H, 4)
+    page_bytes = ap.page_bytes_for(P, rb)
+    g = ap.Pool(P, page_bytes, N, 1, 4, E, N + SP + E, SP, fill=FILL)
+    o = oracle.Pool(P, page_bytes, N, 1, 4, E, N + SP + E, SP, keep_bytes=True, fill=FILL)
+    logits = inputs.router_logits(H + T, T, E)
+    x = inputs.normal_bf16(H + T, inputs.X_STREAM, (T, H))
+    idx, _ = oracle.route_topk(logits, k)
+    plan = oracle.dispatch(x, idx, E, 0, False, fp8=True)
+    rid_o = o.push(0, [plan["xd"], plan["xd_scale"].view(np.uint8).reshape(-1, 4)], plan["rows"], plan["seg_off"],
+                   plan["live"])
+    xd = torch.full((plan["rows"], H), 0xA5, dtype=torch.uint8, device="cuda")
+    xs = torch.from_numpy(np.full(plan["rows"] * 4, 0xA5, np.uint8).view(np.float32)).cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(g.stream):
+        d = g.dispatch_stash(0, bf16_to_dev(x), to_dev(idx), E, fp8=True, out={"xd": xd, "xd_scale": xs})
+    torch.cuda.synchronize()
+    assert d["record_id"] == rid_o
+    for key in ("counts", "live", "seg_off", "dest"):
+        assert np.array_equal(host(d[key]), plan[key]), key
+    assert np.array_equal(host(d["xd"]), plan["xd"])
+    assert np.array_equal(host(d["xd_scale"]).view(np.uint32), plan["xd_scale"].view(np.uint32))
+    assert g.state() == o.state()
+    a, b = g.record(0, 0), o.record(0, 0)
+    for key in ("npages", "ndev", "nspill", "nlost"):
+        assert a[key] == b[key], key
+    assert np.array_equal(a["page_table"], b["page_table"])
+    assert np.array_equal(host(g.pool), o.pool_bytes())
+    if SP:
+        assert np.array_equal(g.spill.numpy(), o.spill_bytes())
+    dq = [np.full((plan["rows"], H), 0x3C, np.uint8), np.full((plan["rows"], 4), 0x3C, np.uint8)]
+    dg = [to_dev(dq[0]), to_dev(dq[1])]
+    torch.cuda.synchronize()
+    g.pop(0, dg)
+    o.pop(0, dq, plan["rows"])
+    torch.cuda.synchronize()
+    assert np.array_equal(host(dg[0]), dq[0]) and np.array_equal(host(dg[1]), dq[1])
+    assert g.state() == o.state()
