@@ -614,6 +614,7 @@ def kernel_hash() -> str:
     common = open(os.path.join(csrc, "ap_common.cuh")).read()
     dev = stash[stash.index("// ---- kernels"):stash.index("// ---- host runtime")]
     dev += common[common.index("// ---- device helpers"):]
+    dev += open(os.path.join(csrc, "dispatch_scan.cuh")).read()  # device helpers of the fused copies
     return hashlib.sha256(dev.encode()).hexdigest()[:16]
 
 
