@@ -73,7 +73,8 @@ def _load():
             "or_combine": (None, [P, i64, i32, P, P, i64, i32, P, P]),
             "or_combine_backward": (None, [P, P, i64, i32, P, P, i64, i32, P, P, P]),
             "or_dispatch_backward": (None, [P, i64, i32, P, i64, i32, P, P]),
-            "or_pool_new": (P, [i32, i64, i64, i32, i32, i32, i64, i64, i32, u8]),
+            "or_pool_new": (P, [i32, i64, i64, i32, i32, i32, i64, i64, i32, u8, i64]),
+            "or_pool_grow": (i32, [P, i64]),
             "or_pool_free": (None, [P]),
             "or_pool_reset": (None, [P]),
             "or_pool_push": (i32, [P, i32, i32, P, P, i64, i32, P, P, P]),
@@ -265,20 +266,30 @@ class Pool:
     """Byte-exact simulation of the page pool, free lists, records and flags.
 
     ``keep_bytes=False`` keeps metadata only (page tables, rings, flags), for
-    sizes whose byte image would not fit the host."""
+    sizes whose byte image would not fit the host.  ``max_num_pages``: the
+    most device pages ``grow`` may reach (0: ``num_pages``, a pool that never
+    grows); spill page ids start there.  ``num_pages`` may be 0 then (a
+    calibration pool with no device pages yet)."""
 
     def __init__(self, page_tokens: int, page_bytes: int, num_pages: int, num_slots: int,
                  max_records_per_slot: int, max_segments: int, max_pages_per_record: int,
-                 spill_pages: int = 0, keep_bytes: bool = True, fill: int = 0xA5):
+                 spill_pages: int = 0, keep_bytes: bool = True, fill: int = 0xA5, max_num_pages: int = 0):
         self.lib = _load()
         self.P, self.page_bytes, self.N = page_tokens, page_bytes, num_pages
+        self.NMAX = max_num_pages or num_pages
         self.SP, self.S, self.R = spill_pages, num_slots, max_records_per_slot
         self.max_pages = max_pages_per_record
         self.keep_bytes = keep_bytes
         self.h = self.lib.or_pool_new(page_tokens, page_bytes, num_pages, num_slots, max_records_per_slot,
-                                      max_segments, max_pages_per_record, spill_pages, int(keep_bytes), fill)
+                                      max_segments, max_pages_per_record, spill_pages, int(keep_bytes), fill,
+                                      max_num_pages)
         if not self.h:
             raise OracleError(EINVAL, "pool_new")
+
+    def grow(self, num_pages: int):
+        """Add device pages up to num_pages (see or_pool_grow)."""
+        _chk(self.lib.or_pool_grow(self.h, num_pages), "grow")
+        self.N = num_pages
 
     def close(self):
         if self.h:
@@ -341,10 +352,11 @@ class Pool:
     def state(self):
         ctr = np.zeros(4, np.uint64)
         flags = np.zeros(1, np.uint32)
-        hw = np.zeros(2, np.int64)
+        hw = np.zeros(5, np.int64)
         self.lib.or_pool_state(self.h, _ptr(ctr), _ptr(flags), _ptr(hw))
         return dict(head=int(ctr[0]), tail=int(ctr[1]), spill_head=int(ctr[2]), spill_tail=int(ctr[3]),
-                    flags=int(flags[0]), high_water=int(hw[0]), spill_high_water=int(hw[1]))
+                    flags=int(flags[0]), high_water=int(hw[0]), spill_high_water=int(hw[1]),
+                    held=int(hw[2]), held_high_water=int(hw[3]), num_pages=int(hw[4]))
 
     def rings(self):
         ring = np.empty(self.N, np.int32)

@@ -437,8 +437,14 @@ void or_dispatch_backward(const uint16_t *dxd, int64_t rows, int32_t H,
 /*     ceil(live/P) pages in order; each page takes the next free device      */
 /*     page, else the next free spill page (the excess spills), else it is    */
 /*     lost (not copied);                                                     */
-/*   - page-table entries: device page p -> p, spill page s -> N + s,         */
-/*     lost -> -1;                                                            */
+/*   - page-table entries: device page p -> p, spill page s -> NMAX + s,     */
+/*     lost -> -1 (NMAX, the most device pages the pool may grow to, is N     */
+/*     for a pool that never grows);                                          */
+/*   - calibration ([TT5541] "AI-Generated Details": calibration parks live   */
+/*     prefixes before the buffers exist): a pool may start with N = 0 device */
+/*     pages, so every page of a push goes to the spill pages (or is lost);   */
+/*     the pages held by queued records and their high-water mark measure the */
+/*     device pages the schedule needs, and or_pool_grow adds them;           */
 /*   - rows inside a page are dense: plane 0 at r*rb0, plane 1 at            */
 /*     roundup16(P*rb0) + r*rb1; bytes of a page past its live rows are left  */
 /*     untouched (page-tail mask); rows >= live are never copied (live-prefix */
@@ -468,12 +474,14 @@ typedef struct {
 typedef struct {
     int32_t P;
     int64_t page_bytes, N, SP;
+    int64_t NMAX; /* most device pages the pool may grow to; spill ids start here */
     int32_t S, R, max_segs;
     int64_t max_pages;
     int32_t *ring, *spill_ring;
     uint64_t head, tail, spill_head, spill_tail;
     uint32_t flags;
     int64_t high_water, spill_high_water;
+    int64_t held, held_high_water; /* pages (device + spill + lost) of queued records */
     uint8_t *pool;  /* N * page_bytes, or NULL (metadata only) */
     uint8_t *spill; /* SP * page_bytes, or NULL */
     or_record *q;   /* [S * R] */
@@ -493,30 +501,36 @@ static void or_record_free(or_record *r)
 
 static int64_t or_roundup16(int64_t v) { return (v + 15) / 16 * 16; }
 
+/* NMAX: the most device pages the pool may grow to (or_pool_grow); 0 means N.
+ * N may be 0 (no device pages yet) when NMAX >= 1. */
 or_pool *or_pool_new(int32_t P, int64_t page_bytes, int64_t N, int32_t S,
                      int32_t R, int32_t max_segs, int64_t max_pages,
-                     int64_t SP, int32_t keep_bytes, uint8_t fill)
+                     int64_t SP, int32_t keep_bytes, uint8_t fill, int64_t NMAX)
 {
-    if (P < 1 || page_bytes < 1 || N < 1 || S < 1 || R < 1 || max_segs < 1 ||
-        max_pages < 1 || SP < 0)
+    if (NMAX == 0)
+        NMAX = N;
+    if (P < 1 || page_bytes < 1 || N < 0 || NMAX < 1 || N > NMAX || S < 1 || R < 1 ||
+        max_segs < 1 || max_pages < 1 || SP < 0)
         return NULL;
     or_pool *p = (or_pool *)calloc(1, sizeof(or_pool));
     p->P = P;
     p->page_bytes = page_bytes;
     p->N = N;
+    p->NMAX = NMAX;
     p->SP = SP;
     p->S = S;
     p->R = R;
     p->max_segs = max_segs;
     p->max_pages = max_pages;
-    p->ring = (int32_t *)malloc((size_t)N * sizeof(int32_t));
+    p->ring = (int32_t *)malloc((size_t)NMAX * sizeof(int32_t));
     p->spill_ring = (int32_t *)malloc((size_t)(SP + 1) * sizeof(int32_t));
     p->q = (or_record *)calloc((size_t)S * R, sizeof(or_record));
     p->q_head = (int32_t *)calloc((size_t)S, sizeof(int32_t));
     p->q_count = (int32_t *)calloc((size_t)S, sizeof(int32_t));
     if (keep_bytes) {
-        p->pool = (uint8_t *)malloc((size_t)(N * page_bytes));
-        memset(p->pool, fill, (size_t)(N * page_bytes));
+        /* room for every page the pool may grow to; pages join with the fill */
+        p->pool = (uint8_t *)malloc((size_t)(NMAX * page_bytes));
+        memset(p->pool, fill, (size_t)(NMAX * page_bytes));
         if (SP > 0) {
             p->spill = (uint8_t *)malloc((size_t)(SP * page_bytes));
             memset(p->spill, fill, (size_t)(SP * page_bytes));
@@ -571,6 +585,33 @@ void or_pool_reset(or_pool *p)
     p->flags = 0;
     p->high_water = 0;
     p->spill_high_water = 0;
+    p->held = 0;
+    p->held_high_water = 0;
+}
+
+/* Lazy sizing ([MG7342] "Summary": the activation arena's capacity grows
+ * lazily).  Reading: the pool gains device pages N .. new_N-1 while records
+ * stay queued.  The free ring is rewritten from position 0 as the free pages
+ * in the order they would have been taken, followed by the new pages in id
+ * order (head = 0, tail = free + new); pages in use, page tables and spill
+ * ids (which start at NMAX) do not change. */
+int or_pool_grow(or_pool *p, int64_t new_N)
+{
+    if (new_N < p->N || new_N > p->NMAX)
+        return OR_EINVAL;
+    uint64_t avail = p->tail - p->head;
+    int32_t *tmp = (int32_t *)malloc((size_t)(avail + 1) * sizeof(int32_t));
+    for (uint64_t i = 0; i < avail; ++i)
+        tmp[i] = p->ring[(p->head + i) % (uint64_t)p->N];
+    for (uint64_t i = 0; i < avail; ++i)
+        p->ring[i] = tmp[i];
+    for (int64_t j = 0; j < new_N - p->N; ++j)
+        p->ring[avail + (uint64_t)j] = (int32_t)(p->N + j);
+    free(tmp);
+    p->head = 0;
+    p->tail = avail + (uint64_t)(new_N - p->N);
+    p->N = new_N;
+    return OR_OK;
 }
 
 static int or_layout_ok(const or_pool *p, int32_t nplanes, const int64_t *rb)
@@ -591,7 +632,7 @@ static uint8_t *or_page_addr(or_pool *p, int32_t id)
         return NULL;
     if (id < p->N)
         return p->pool ? p->pool + (int64_t)id * p->page_bytes : NULL;
-    return p->spill ? p->spill + (int64_t)(id - p->N) * p->page_bytes : NULL;
+    return p->spill ? p->spill + (int64_t)(id - p->NMAX) * p->page_bytes : NULL;
 }
 
 int or_pool_push(or_pool *p, int32_t slot, int32_t nplanes,
@@ -646,7 +687,7 @@ int or_pool_push(or_pool *p, int32_t slot, int32_t nplanes,
             } else {
                 p->flags |= OR_FLAG_POOL_OVERFLOW;
                 if (p->spill_tail - p->spill_head > 0) {
-                    id = (int32_t)(p->N + p->spill_ring[p->spill_head % (uint64_t)p->SP]);
+                    id = (int32_t)(p->NMAX + p->spill_ring[p->spill_head % (uint64_t)p->SP]);
                     p->spill_head += 1;
                     rec->nspill += 1;
                 } else {
@@ -676,6 +717,9 @@ int or_pool_push(or_pool *p, int32_t slot, int32_t nplanes,
         }
     }
     rec->npages = n;
+    p->held += n;
+    if (p->held > p->held_high_water)
+        p->held_high_water = p->held;
 
     int64_t in_use = p->N - (int64_t)(p->tail - p->head);
     if (in_use > p->high_water)
@@ -721,11 +765,12 @@ int or_pool_pop(or_pool *p, int32_t slot, int32_t nplanes, uint8_t *const *dst,
         if (id >= 0 && id < p->N) {
             p->ring[p->tail % (uint64_t)p->N] = id;
             p->tail += 1;
-        } else if (id >= p->N) {
-            p->spill_ring[p->spill_tail % (uint64_t)p->SP] = (int32_t)(id - p->N);
+        } else if (id >= p->NMAX) {
+            p->spill_ring[p->spill_tail % (uint64_t)p->SP] = (int32_t)(id - p->NMAX);
             p->spill_tail += 1;
         }
     }
+    p->held -= rec->npages;
     if (record_id)
         *record_id = rec->id;
     or_record_free(rec);
@@ -735,16 +780,21 @@ int or_pool_pop(or_pool *p, int32_t slot, int32_t nplanes, uint8_t *const *dst,
 }
 
 /* ---- state read-out for the tests ---- */
+/* hw5: device high water, spill high water, pages held by queued records,
+ * their high water, current device pages N. */
 void or_pool_state(const or_pool *p, uint64_t *ctr4, uint32_t *flags,
-                   int64_t *hw2)
+                   int64_t *hw5)
 {
     ctr4[0] = p->head;
     ctr4[1] = p->tail;
     ctr4[2] = p->spill_head;
     ctr4[3] = p->spill_tail;
     *flags = p->flags;
-    hw2[0] = p->high_water;
-    hw2[1] = p->spill_high_water;
+    hw5[0] = p->high_water;
+    hw5[1] = p->spill_high_water;
+    hw5[2] = p->held;
+    hw5[3] = p->held_high_water;
+    hw5[4] = p->N;
 }
 
 void or_pool_rings(const or_pool *p, int32_t *ring, int32_t *spill_ring)

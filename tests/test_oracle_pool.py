@@ -33,7 +33,7 @@ def live_pages(pool):
             r = pool.record(s, q)
             pt = r["page_table"]
             dev += [int(i) for i in pt if 0 <= i < pool.N]
-            sp += [int(i) - pool.N for i in pt if i >= pool.N]
+            sp += [int(i) - pool.NMAX for i in pt if i >= pool.NMAX]
     return dev, sp
 
 
