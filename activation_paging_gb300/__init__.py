@@ -8,7 +8,9 @@ raises.
 
     route_topk        softmax -> top-k -> renormalised weights
     dispatch_permute  expert-major, capacity-bounded permutation (BF16 / E4M3)
-    Pool              paged stash: push / pop / reset / overflow read-out
+    Pool              paged stash: push / pop / reset / overflow read-out,
+                      calibration and lazy growth (over an Arena)
+    Arena             device memory that grows in place
     combine_unpermute top-k weighted un-permute to dense BF16 [T, H]
 """
 from __future__ import annotations
@@ -29,7 +31,7 @@ FLAG_CORRUPT = 0x20
 DTYPE_BF16, DTYPE_E4M3 = 0, 1
 
 __all__ = ["route_topk", "dispatch_permute", "dispatch_scratch_bytes", "combine_unpermute", "combine_backward",
-           "dispatch_backward", "cast_e4m3", "Pool", "APError", "lib"]
+           "dispatch_backward", "cast_e4m3", "Pool", "Arena", "APError", "lib", "launch_count"]
 
 
 def lib():
@@ -65,6 +67,11 @@ def route_topk(logits: torch.Tensor, k: int, idx: torch.Tensor | None = None, w:
         w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
     check(lib().ap_route_topk(_p(logits), T, E, k, _p(idx), _p(w), _stream(stream)), "route_topk")
     return idx, w
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued in this process (a graph replay adds none)."""
+    return int(lib().ap_launch_count())
 
 
 def dispatch_scratch_bytes(T: int, k: int, E: int) -> int:
@@ -173,6 +180,56 @@ def page_bytes_for(page_tokens: int, row_bytes) -> int:
     return (need + 255) // 256 * 256
 
 
+class Arena:
+    """Device memory whose size grows in place (``ap_arena_*``: reserved
+    addresses, physical memory mapped on demand).  ``view(n)`` is a uint8
+    tensor over the first n bytes; views stay valid while the arena lives."""
+
+    def __init__(self, max_bytes: int, device="cuda"):
+        self.lib = lib()
+        self.device = torch.device(device)
+        self.handle = ctypes.c_void_p()
+        check(self.lib.ap_arena_create(ctypes.byref(self.handle), int(max_bytes), self.device.index or 0),
+              "arena_create")
+
+    def grow(self, nbytes: int):
+        check(self.lib.ap_arena_grow(self.handle, int(nbytes)), "arena_grow")
+
+    def info(self):
+        base, mapped, reserved = ctypes.c_void_p(), ctypes.c_int64(), ctypes.c_int64()
+        check(self.lib.ap_arena_info(self.handle, ctypes.byref(base), ctypes.byref(mapped), ctypes.byref(reserved)),
+              "arena_info")
+        return base.value or 0, mapped.value, reserved.value
+
+    def view(self, nbytes: int) -> torch.Tensor:
+        base, mapped, _ = self.info()
+        if nbytes > mapped:
+            raise ValueError(f"{nbytes} bytes requested, {mapped} mapped")
+        if nbytes == 0:  # nothing mapped yet: no address to view
+            return torch.empty(0, dtype=torch.uint8, device=self.device)
+        return torch.as_tensor(_DeviceSpan(base, nbytes, self), device=self.device)
+
+    def close(self):
+        if getattr(self, "handle", None) and self.handle.value:
+            check(self.lib.ap_arena_destroy(self.handle), "arena_destroy")
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class _DeviceSpan:
+    """A device byte range in the CUDA array interface (keeps its owner alive)."""
+
+    def __init__(self, ptr: int, nbytes: int, owner):
+        self.owner = owner
+        self.__cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
 class Pool:
     """Paged activation stash over PyTorch-owned memory.
 
@@ -180,22 +237,37 @@ class Pool:
     held by this object; the library keeps only their addresses.  Every push,
     pop and reset runs on ``self.stream`` (a high-priority stream by
     default).  Order work on other streams with ``stream.wait_stream`` /
-    ``self.stream.wait_stream``."""
+    ``self.stream.wait_stream``.
+
+    ``max_num_pages > num_pages`` makes a growable pool: its pages live in an
+    :class:`Arena` reserved for ``max_num_pages`` pages and mapped as the pool
+    grows (``grow``); ``num_pages`` may then be 0, a calibration pool whose
+    pushes park their live prefixes in the spill pages (or lose them) while
+    ``state()["held_high_water"]`` measures the device pages the schedule
+    needs (``calibrated_pages``)."""
 
     def __init__(self, page_tokens: int, page_bytes: int, num_pages: int, num_slots: int = 1,
                  max_records_per_slot: int = 8, max_segments: int = 1024, max_pages_per_record: int | None = None,
                  spill_pages: int = 0, max_ctas: int = 0, device="cuda", stream: torch.cuda.Stream | None = None,
-                 fill: int | None = None):
+                 fill: int | None = None, max_num_pages: int = 0):
         self.lib = lib()
+        nmax = max(max_num_pages, num_pages)
         if max_pages_per_record is None:
-            max_pages_per_record = num_pages + spill_pages
+            max_pages_per_record = nmax + spill_pages
         self.cfg = PoolConfig(page_tokens, num_slots, page_bytes, num_pages, spill_pages, max_records_per_slot,
-                              max_segments, max_pages_per_record, max_ctas, 0)
+                              max_segments, max_pages_per_record, max_ctas, 0, max_num_pages)
         a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
         check(self.lib.ap_pool_required_bytes(ctypes.byref(self.cfg), ctypes.byref(a), ctypes.byref(b),
                                               ctypes.byref(c)), "pool_required_bytes")
         self.device = torch.device(device)
-        self.pool = torch.empty(a.value, dtype=torch.uint8, device=self.device)
+        self.fill = fill
+        self.arena = None
+        if nmax > num_pages:
+            self.arena = Arena(nmax * page_bytes, self.device)
+            self.arena.grow(a.value)
+            self.pool = self.arena.view(a.value)
+        else:
+            self.pool = torch.empty(a.value, dtype=torch.uint8, device=self.device)
         self.meta = torch.empty(b.value, dtype=torch.uint8, device=self.device)
         self.spill = torch.empty(c.value, dtype=torch.uint8, pin_memory=True) if c.value else None
         if fill is not None:
@@ -205,17 +277,48 @@ class Pool:
             torch.cuda.synchronize(self.device)
         self.stream = stream if stream is not None else torch.cuda.Stream(device=self.device, priority=-1)
         self.handle = ctypes.c_void_p()
-        check(self.lib.ap_pool_init(ctypes.byref(self.handle), ctypes.byref(self.cfg), _p(self.pool),
-                                    _p(self.meta), _p(self.spill), self.stream.cuda_stream), "pool_init")
-        self.N, self.SP, self.P = num_pages, spill_pages, page_tokens
+        check(self.lib.ap_pool_init(ctypes.byref(self.handle), ctypes.byref(self.cfg),
+                                    _p(self.pool) if num_pages else None, _p(self.meta), _p(self.spill),
+                                    self.stream.cuda_stream), "pool_init")
+        self.N, self.SP, self.P, self.NMAX = num_pages, spill_pages, page_tokens, nmax
         self.page_bytes = page_bytes
         self.max_pages = max_pages_per_record
+
+    def grow(self, num_pages: int):
+        """Grow the device pool to ``num_pages`` in place, with records still
+        queued (``ap_pool_grow``).  New pages are filled with ``fill`` when the
+        pool was created with one.  Graphs captured before must be captured
+        again (they hold the old page count)."""
+        if num_pages == self.N:
+            return
+        if self.arena is None:
+            raise ValueError("this pool was created without room to grow (max_num_pages)")
+        nbytes = num_pages * self.page_bytes
+        self.arena.grow(nbytes)
+        pool = self.arena.view(nbytes)
+        if self.fill is not None:
+            with torch.cuda.stream(self.stream):
+                pool[self.N * self.page_bytes:].fill_(self.fill)
+        check(self.lib.ap_pool_grow(self.handle, num_pages, self.arena.info()[0], self.stream.cuda_stream),
+              "pool_grow")
+        self.pool, self.N = pool, num_pages
+
+    def calibrated_pages(self, margin: float = 1.0) -> int:
+        """Device pages for the schedule run so far: the most pages its queued
+        records ever held, times ``margin`` (synchronises the paging stream)."""
+        import math
+        return int(math.ceil(self.state()["held_high_water"] * margin))
 
     # -- lifecycle --------------------------------------------------------
     def close(self):
         if getattr(self, "handle", None) and self.handle.value:
             self.lib.ap_pool_destroy(self.handle)
             self.handle = ctypes.c_void_p()
+        if getattr(self, "arena", None) is not None:
+            # the paging stream's work on the pages ends before the mapping can
+            # go; the arena itself is released with its last tensor view
+            self.stream.synchronize()
+            self.arena = None
 
     def __del__(self):
         try:
@@ -339,7 +442,8 @@ class Pool:
         s = PoolState()
         check(self.lib.ap_pool_read_state(self.handle, ctypes.byref(s)), "pool_read_state")
         return dict(head=s.head, tail=s.tail, spill_head=s.spill_head, spill_tail=s.spill_tail, flags=s.flags,
-                    high_water=s.high_water, spill_high_water=s.spill_high_water)
+                    high_water=s.high_water, spill_high_water=s.spill_high_water, held=s.held,
+                    held_high_water=s.held_high_water, num_pages=s.num_pages)
 
     def rings(self):
         import numpy as np

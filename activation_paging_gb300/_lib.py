@@ -18,12 +18,13 @@ i32, i64, u32, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_u
 class PoolConfig(ctypes.Structure):
     _fields_ = [("page_tokens", i32), ("num_slots", i32), ("page_bytes", i64), ("num_pages", i64),
                 ("spill_pages", i64), ("max_records_per_slot", i32), ("max_segments", i32),
-                ("max_pages_per_record", i64), ("max_ctas", i32), ("reserved", i32)]
+                ("max_pages_per_record", i64), ("max_ctas", i32), ("reserved", i32), ("max_num_pages", i64)]
 
 
 class PoolState(ctypes.Structure):
     _fields_ = [("head", u64), ("tail", u64), ("spill_head", u64), ("spill_tail", u64), ("flags", u32),
-                ("pad0", u32), ("high_water", i64), ("spill_high_water", i64), ("pad1", i64)]
+                ("pad0", u32), ("high_water", i64), ("spill_high_water", i64), ("held", i64),
+                ("held_high_water", i64), ("num_pages", i64), ("pad", i64 * 6)]
 
 
 class RecordInfo(ctypes.Structure):
@@ -36,6 +37,7 @@ SIGNATURES = {
     "ap_status_str": (ctypes.c_char_p, [i32]),
     "ap_last_error": (ctypes.c_char_p, []),
     "ap_version": (ctypes.c_char_p, []),
+    "ap_launch_count": (ctypes.c_uint64, []),
     "ap_route_topk": (i32, [P, i64, i32, i32, P, P, P]),
     "ap_dispatch_scratch_bytes": (i32, [i64, i32, i32, P]),
     "ap_dispatch_permute": (i32, [P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P, i64, P, P]),
@@ -46,6 +48,7 @@ SIGNATURES = {
     "ap_pool_required_bytes": (i32, [P, P, P, P]),
     "ap_pool_init": (i32, [P, P, P, P, P, P]),
     "ap_pool_reset": (i32, [P, P]),
+    "ap_pool_grow": (i32, [P, i64, P, P]),
     "ap_pool_destroy": (i32, [P]),
     "ap_pool_max_ctas": (i32, [P, P]),
     "ap_pool_set_max_ctas": (i32, [P, i32]),
@@ -60,6 +63,10 @@ SIGNATURES = {
     "ap_pool_read_rings": (i32, [P, P, P]),
     "ap_pool_read_record": (i32, [P, i32, i32, P, P, P, P, i64]),
     "ap_cast_e4m3": (i32, [P, P, i64, P]),
+    "ap_arena_create": (i32, [P, i64, i32]),
+    "ap_arena_grow": (i32, [P, i64]),
+    "ap_arena_info": (i32, [P, P, P, P]),
+    "ap_arena_destroy": (i32, [P]),
 }
 
 _lib = None

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libap.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["common.cu", "route.cu", "dispatch.cu", "combine.cu", "stash.cu", "noalloc.cu"]
+SOURCES = ["common.cu", "route.cu", "dispatch.cu", "combine.cu", "stash.cu", "noalloc.cu", "arena.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

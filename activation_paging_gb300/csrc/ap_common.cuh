@@ -15,6 +15,8 @@ void set_error(const char *fmt, ...);
 ap_status fail(ap_status s, const char *fmt, ...);
 ap_status cuda_fail(cudaError_t e, const char *what);
 int sm_count();
+// Counts one enqueued kernel (ap_launch_count); every launch site calls it once.
+void note_launch();
 // Blocks of `kernel` (launched with `threads` threads and `smem` dynamic shared
 // bytes) that fit on the whole GPU at once: SMs x resident blocks per SM.
 // Grid-stride kernels launched with this grid run in exactly one wave.
@@ -41,6 +43,7 @@ int dispatch_blocks(int64_t T);
     do {                                                        \
         cudaError_t e_ = cudaGetLastError();                    \
         if (e_ != cudaSuccess) return ::ap::cuda_fail(e_, what); \
+        ::ap::note_launch();                                    \
     } while (0)
 
 // ---- device helpers ----------------------------------------------------------

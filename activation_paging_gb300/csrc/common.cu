@@ -2,6 +2,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "ap_common.cuh"
 
 namespace ap {
@@ -30,6 +32,10 @@ ap_status cuda_fail(cudaError_t e, const char *what)
     set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
     return AP_ECUDA;
 }
+
+static std::atomic<uint64_t> g_launches{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int sm_count()
 {
@@ -68,3 +74,5 @@ extern "C" const char *ap_status_str(ap_status s)
 extern "C" const char *ap_last_error(void) { return ap::g_err; }
 
 extern "C" const char *ap_version(void) { return "0.1.0"; }
+
+extern "C" uint64_t ap_launch_count(void) { return ap::g_launches.load(std::memory_order_relaxed); }

@@ -42,13 +42,48 @@ struct RecHdr {
     int64_t pad1[7];
 };
 static_assert(sizeof(RecHdr) == 128, "record header layout");
-static_assert(sizeof(ap_pool_state) == 64, "state layout");
+static_assert(sizeof(ap_pool_state) == 128, "state layout");
 
 struct PageDesc {
     int64_t row0; // first row in the source / destination planes
     int32_t nrows;
     int32_t pad;
 };
+
+// Where page ids point.  Device page p (0 <= p < N) lives at pool + p *
+// page_bytes; spill page s (0 <= s < SP) has id SB + s and lives at spill +
+// s * page_bytes (SB, the most device pages the pool may grow to, keeps spill
+// ids fixed while N grows); -1 is a lost page.
+struct PageSpace {
+    int32_t *ring, *spill_ring;
+    uint8_t *pool, *spill;
+    int64_t N, SB, SP, page_bytes;
+};
+
+__device__ __forceinline__ uint8_t *page_addr(const PageSpace &ps, int64_t id)
+{
+    return (id < ps.N) ? ps.pool + id * ps.page_bytes : ps.spill + (id - ps.SB) * ps.page_bytes;
+}
+
+// Id of page ordinal `ord` of a record being pushed: the device ring entry at
+// head0 + ord for the first ndev pages, then the spill ring entry at sh0 +
+// (ord - ndev) for the next nspill, else -1 (lost).  A ring entry out of its
+// range gives -1 and *corrupt = true.
+__device__ __forceinline__ int64_t pushed_page_id(const PageSpace &ps, int64_t ord, int64_t ndev, int64_t nspill,
+                                                  uint64_t head0, uint64_t sh0, bool *corrupt)
+{
+    *corrupt = false;
+    if (ord < ndev) {
+        const int64_t id = ps.ring[(head0 + (uint64_t)ord) % (uint64_t)ps.N];
+        if (id >= 0 && id < ps.N) return id;
+        *corrupt = true;
+    } else if (ord < ndev + nspill) {
+        const int64_t sp = ps.spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)ps.SP];
+        if (sp >= 0 && sp < ps.SP) return ps.SB + sp;
+        *corrupt = true;
+    }
+    return -1;
+}
 
 struct RecLayout {
     int64_t seg_off, live, pg_base, desc, page_table, stride;
@@ -75,16 +110,21 @@ RecLayout record_layout(const ap_pool_config &c)
 }
 
 struct MetaLayout {
-    int64_t ring, spill_ring, records, total;
+    int64_t ring, spill_ring, grow_tmp, records, total;
     RecLayout rec;
 };
+
+// Most device pages the pool may grow to (spill ids start here).
+inline int64_t max_pages_of(const ap_pool_config &c) { return c.max_num_pages > 0 ? c.max_num_pages : c.num_pages; }
 
 MetaLayout meta_layout(const ap_pool_config &c)
 {
     MetaLayout M;
+    const int64_t nmax = max_pages_of(c);
     M.ring = 256;
-    M.spill_ring = align_up(M.ring + 4 * c.num_pages, 256);
-    M.records = align_up(M.spill_ring + 4 * c.spill_pages, 256);
+    M.spill_ring = align_up(M.ring + 4 * nmax, 256);
+    M.grow_tmp = align_up(M.spill_ring + 4 * c.spill_pages, 256); // free-ring copy used by a grow
+    M.records = (nmax > c.num_pages) ? align_up(M.grow_tmp + 4 * nmax, 256) : M.grow_tmp;
     M.rec = record_layout(c);
     M.total = M.records + M.rec.stride * (int64_t)c.num_slots * c.max_records_per_slot;
     return M;
@@ -113,10 +153,12 @@ RecPtr rec_ptr(uint8_t *meta, const MetaLayout &M, int64_t index)
 }
 
 // ---- kernels -------------------------------------------------------------------
-__global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int32_t *spill_ring, int64_t SP)
+// NMAX: every slot of the device ring is written, also those a grow brings
+// into use later (slots at or past N are never read before then).
+__global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int64_t NMAX, int32_t *spill_ring, int64_t SP)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride) ring[i] = (int32_t)i;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < NMAX; i += stride) ring[i] = (int32_t)i;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < SP; i += stride) spill_ring[i] = (int32_t)i;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         st->head = 0;
@@ -127,12 +169,93 @@ __global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int32_t *sp
         st->pad0 = 0;
         st->high_water = 0;
         st->spill_high_water = 0;
-        st->pad1 = 0;
+        st->held = 0;
+        st->held_high_water = 0;
+        st->num_pages = N;
+        for (int i = 0; i < 6; ++i) st->pad[i] = 0;
+    }
+}
+
+// Grow the device pool from N0 to N1 pages (one CTA, on the paging stream):
+// the free pages, in the order they would be taken, move to ring positions
+// 0 .. free-1 (through tmp, since old and new positions overlap), the new
+// pages N0 .. N1-1 follow in id order, and the counters re-base to head = 0.
+__global__ void __launch_bounds__(1024) k_grow(ap_pool_state *st, int32_t *ring, int32_t *tmp, int64_t N0, int64_t N1)
+{
+    const uint64_t head = st->head, tail = st->tail;
+    const int64_t avail = (int64_t)(tail - head); // 0 when N0 == 0
+    for (int64_t i = threadIdx.x; i < avail; i += blockDim.x) tmp[i] = ring[(head + (uint64_t)i) % (uint64_t)N0];
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < avail; i += blockDim.x) ring[i] = tmp[i];
+    for (int64_t j = threadIdx.x; j < N1 - N0; j += blockDim.x) ring[avail + j] = (int32_t)(N0 + j);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        st->head = 0;
+        st->tail = (uint64_t)(avail + (N1 - N0));
+        st->num_pages = N1;
     }
 }
 
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSmemSegs = 2048; // segments whose tables the plan keeps in shared memory
+
+// Descriptor of page ordinal `ord`: its segment is the largest s with
+// pg_base[s] <= ord; the page holds rows [pg*P, min(live, (pg+1)*P)) of it.
+__device__ __forceinline__ void plan_descriptor(RecPtr rec, const int64_t *pg_base, const int32_t *seg_live,
+                                                const int32_t *seg_offs, int nseg, int64_t ord, int P)
+{
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pg_base[mid] <= ord) lo = mid;
+        else hi = mid - 1;
+    }
+    const int64_t r0 = (ord - pg_base[lo]) * P;
+    int64_t nr = (int64_t)seg_live[lo] - r0;
+    if (nr > P) nr = P;
+    PageDesc d;
+    d.row0 = (int64_t)seg_offs[lo] + r0;
+    d.nrows = (int32_t)nr;
+    d.pad = 0;
+    rec.desc[ord] = d;
+}
+
+// Allocation of a record of `total` pages (one thread): the first
+// min(total, max_pages) pages come from the device ring at the head snapshot,
+// then from the spill ring, the rest are lost; the head counters advance, the
+// high-water marks and the sticky flags are updated.
+__device__ __forceinline__ void plan_allocate(ap_pool_state *st, RecPtr rec, int nseg, int64_t total,
+                                              int64_t max_pages, uint32_t f, uint64_t head, uint64_t tail,
+                                              uint64_t sh, uint64_t stl, int64_t N, int64_t SP)
+{
+    const int64_t kept = total < max_pages ? total : max_pages;
+    if (total > max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
+    const int64_t avail = (int64_t)(tail - head);
+    const int64_t savail = (int64_t)(stl - sh);
+    const int64_t ndev = kept < avail ? kept : avail;
+    int64_t nspill = kept - ndev;
+    if (nspill > savail) nspill = savail;
+    const int64_t nlost = kept - ndev - nspill;
+    if (kept > avail) f |= AP_FLAG_POOL_OVERFLOW;
+    if (nlost > 0) f |= AP_FLAG_SPILL_OVERFLOW;
+    rec.hdr->nseg = nseg;
+    rec.hdr->npages = kept;
+    rec.hdr->ndev = ndev;
+    rec.hdr->nspill = nspill;
+    rec.hdr->nlost = nlost;
+    rec.hdr->head0 = head;
+    rec.hdr->spill_head0 = sh;
+    st->head = head + (uint64_t)ndev;
+    st->spill_head = sh + (uint64_t)nspill;
+    const int64_t in_use = N - (int64_t)(tail - (head + (uint64_t)ndev));
+    if (in_use > st->high_water) st->high_water = in_use;
+    const int64_t s_use = SP - (int64_t)(stl - (sh + (uint64_t)nspill));
+    if (s_use > st->spill_high_water) st->spill_high_water = s_use;
+    const int64_t held = st->held + kept; // pages of queued records, wherever they went
+    st->held = held;
+    if (held > st->held_high_water) st->held_high_water = held;
+    st->flags |= f;
+}
 
 // have_reg: nseg <= kPlanThreads and thread s already holds segment s's
 // offset and live count in reg_off / reg_live (fused scan + plan).
@@ -216,50 +339,9 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
     const int64_t *pg_base = in_smem ? s_base : rec.pg_base;
     const int32_t *seg_live = in_smem ? s_live : rec.live;
     const int32_t *seg_offs = in_smem ? s_off : rec.seg_off;
-    for (int64_t ord = tid; ord < kept; ord += kPlanThreads) {
-        int lo = 0, hi = nseg - 1; // largest s with pg_base[s] <= ord
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (pg_base[mid] <= ord) lo = mid;
-            else hi = mid - 1;
-        }
-        const int64_t pg = ord - pg_base[lo];
-        const int64_t r0 = pg * P;
-        int64_t nr = (int64_t)seg_live[lo] - r0;
-        if (nr > P) nr = P;
-        PageDesc d;
-        d.row0 = (int64_t)seg_offs[lo] + r0;
-        d.nrows = (int32_t)nr;
-        d.pad = 0;
-        rec.desc[ord] = d;
-    }
+    for (int64_t ord = tid; ord < kept; ord += kPlanThreads) plan_descriptor(rec, pg_base, seg_live, seg_offs, nseg, ord, P);
     // 3. allocation: device pages first, then spill pages, then lost
-    if (tid == 0) {
-        uint32_t f = s_flags;
-        if (total > max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
-        const int64_t avail = (int64_t)(tail - head);
-        const int64_t savail = (int64_t)(stl - sh);
-        const int64_t ndev = kept < avail ? kept : avail;
-        int64_t nspill = kept - ndev;
-        if (nspill > savail) nspill = savail;
-        const int64_t nlost = kept - ndev - nspill;
-        if (kept > avail) f |= AP_FLAG_POOL_OVERFLOW;
-        if (nlost > 0) f |= AP_FLAG_SPILL_OVERFLOW;
-        rec.hdr->nseg = nseg;
-        rec.hdr->npages = kept;
-        rec.hdr->ndev = ndev;
-        rec.hdr->nspill = nspill;
-        rec.hdr->nlost = nlost;
-        rec.hdr->head0 = head;
-        rec.hdr->spill_head0 = sh;
-        st->head = head + (uint64_t)ndev;
-        st->spill_head = sh + (uint64_t)nspill;
-        const int64_t in_use = N - (int64_t)(tail - (head + (uint64_t)ndev));
-        if (in_use > st->high_water) st->high_water = in_use;
-        const int64_t s_use = SP - (int64_t)(stl - (sh + (uint64_t)nspill));
-        if (s_use > st->spill_high_water) st->spill_high_water = s_use;
-        st->flags |= f;
-    }
+    if (tid == 0) plan_allocate(st, rec, nseg, total, max_pages, s_flags, head, tail, sh, stl, N, SP);
 }
 
 __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, RecPtr rec, int nseg,
@@ -295,12 +377,8 @@ struct Planes {
 
 constexpr int kCopyThreads = 256;
 
-__global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st, RecPtr rec,
-                                                             const int32_t *__restrict__ ring,
-                                                             const int32_t *__restrict__ spill_ring, int64_t N,
-                                                             int64_t SP, uint8_t *pool, uint8_t *spill,
-                                                             int64_t page_bytes, Planes src, int rows_per_tile,
-                                                             int tiles_per_page)
+__global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st, RecPtr rec, PageSpace ps,
+                                                             Planes src, int rows_per_tile, int tiles_per_page)
 {
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
@@ -314,17 +392,12 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st
         if (r0 >= d.nrows) continue;
         const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
         // resolve this tile's page once
-        int64_t id = -1;
-        if (ord < ndev) id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
-        else if (ord < ndev + nspill) id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
-        const bool ok = (ord < ndev) ? (id >= 0 && id < N) : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
-        if (!ok) {
-            if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-            id = -1;
-        }
+        bool corrupt;
+        const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
+        if (corrupt && threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
         if (sub == 0 && threadIdx.x == 0) rec.page_table[ord] = (int32_t)id; // first tile records the page
         if (id < 0) continue;
-        uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+        uint8_t *page = page_addr(ps, id);
 #pragma unroll
         for (int p = 0; p < 2; ++p)
             if (p < src.n)
@@ -340,14 +413,13 @@ __global__ void k_pop_plan(ap_pool_state *st, RecHdr *hdr)
         hdr->spill_tail0 = st->spill_tail;
         st->tail = st->tail + (uint64_t)hdr->ndev;
         st->spill_tail = st->spill_tail + (uint64_t)hdr->nspill;
+        st->held = st->held - hdr->npages;
     }
 }
 
-__global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st, RecPtr rec, int32_t *ring,
-                                                            int32_t *spill_ring, int64_t N, int64_t SP,
-                                                            const uint8_t *pool, const uint8_t *spill,
-                                                            int64_t page_bytes, Planes dst, int64_t dst_rows,
-                                                            int rows_per_tile, int tiles_per_page)
+__global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st, RecPtr rec, PageSpace ps,
+                                                            Planes dst, int64_t dst_rows, int rows_per_tile,
+                                                            int tiles_per_page)
 {
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
@@ -360,22 +432,24 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
         const int64_t r0 = (int64_t)sub * rows_per_tile;
         if (r0 >= d.nrows) continue;
         const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
-        int64_t id = rec.page_table[ord];
-        const bool ok = (ord < ndev) ? (id >= 0 && id < N) : (ord < ndev + nspill) ? (id >= N && id < N + SP) : (id == -1);
+        const int64_t id = rec.page_table[ord];
+        const bool ok = (ord < ndev) ? (id >= 0 && id < ps.N)
+                                     : (ord < ndev + nspill) ? (id >= ps.SB && id < ps.SB + ps.SP) : (id == -1);
         if (!ok) {
             if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
             continue;
         }
         if (sub == 0 && threadIdx.x == 0) { // first tile recycles the page
-            if (ord < ndev) ring[(tail0 + (uint64_t)ord) % (uint64_t)N] = (int32_t)id;
-            else if (id >= 0) spill_ring[(stail0 + (uint64_t)(ord - ndev)) % (uint64_t)SP] = (int32_t)(id - N);
+            if (ord < ndev) ps.ring[(tail0 + (uint64_t)ord) % (uint64_t)ps.N] = (int32_t)id;
+            else if (id >= 0)
+                ps.spill_ring[(stail0 + (uint64_t)(ord - ndev)) % (uint64_t)ps.SP] = (int32_t)(id - ps.SB);
         }
         if (id < 0) continue;
         if (d.row0 + d.nrows > dst_rows) {
             if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
             continue;
         }
-        const uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+        const uint8_t *page = page_addr(ps, id);
 #pragma unroll
         for (int p = 0; p < 2; ++p)
             if (p < dst.n)
@@ -397,10 +471,7 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
                                                              const int32_t *__restrict__ seg_off,
                                                              int32_t *__restrict__ src_tok,
                                                              uint8_t *__restrict__ xd, ap_pool_state *st, RecPtr rec,
-                                                             const int32_t *__restrict__ ring,
-                                                             const int32_t *__restrict__ spill_ring, int64_t N,
-                                                             int64_t SP, uint8_t *pool, uint8_t *spill,
-                                                             int64_t page_bytes, int P)
+                                                             PageSpace ps, int P)
 {
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
@@ -419,19 +490,12 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
                 if (r >= 0 && r < rec.live[e]) {
                     const int64_t ord = rec.pg_base[e] + r / P;
                     if (ord < npages) {
-                        int64_t id = -1;
-                        if (ord < ndev) id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
-                        else if (ord < ndev + nspill)
-                            id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
-                        const bool ok = (ord < ndev) ? (id >= 0 && id < N)
-                                                     : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
-                        if (!ok) {
-                            atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                            id = -1;
-                        }
+                        bool corrupt;
+                        const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
+                        if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
                         if (r % P == 0) rec.page_table[ord] = (int32_t)id; // row 0 of the page records it
                         if (id >= 0) {
-                            uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+                            uint8_t *page = page_addr(ps, id);
                             my_page = page + (r % P) * rb;
                         }
                     }
@@ -477,8 +541,7 @@ __global__ void __launch_bounds__(256, 3) k_dispatch_stash_e4m3(
     const uint16_t *__restrict__ x, int64_t T, int H, const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
     int k, int E, int capacity, const int32_t *__restrict__ blk, const int32_t *__restrict__ seg_off,
     int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd, float *__restrict__ xd_scale, ap_pool_state *st,
-    RecPtr rec, const int32_t *__restrict__ ring, const int32_t *__restrict__ spill_ring, int64_t N, int64_t SP,
-    uint8_t *pool, uint8_t *spill, int64_t page_bytes, int P, int64_t plane1_off)
+    RecPtr rec, PageSpace ps, int P, int64_t plane1_off)
 {
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
@@ -498,19 +561,12 @@ __global__ void __launch_bounds__(256, 3) k_dispatch_stash_e4m3(
                 if (r >= 0 && r < rec.live[e]) {
                     const int64_t ord = rec.pg_base[e] + r / P;
                     if (ord < npages) {
-                        int64_t id = -1;
-                        if (ord < ndev) id = ring[(head0 + (uint64_t)ord) % (uint64_t)N];
-                        else if (ord < ndev + nspill)
-                            id = N + spill_ring[(sh0 + (uint64_t)(ord - ndev)) % (uint64_t)SP];
-                        const bool ok = (ord < ndev) ? (id >= 0 && id < N)
-                                                     : (ord < ndev + nspill) ? (id >= N && id < N + SP) : true;
-                        if (!ok) {
-                            atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                            id = -1;
-                        }
+                        bool corrupt;
+                        const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
+                        if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
                         if (r % P == 0) rec.page_table[ord] = (int32_t)id; // row 0 of the page records it
                         if (id >= 0) {
-                            uint8_t *page = (id < N) ? pool + id * page_bytes : spill + (id - N) * page_bytes;
+                            uint8_t *page = page_addr(ps, id);
                             my_row = page + (r % P) * H;
                             my_scale = reinterpret_cast<float *>(page + plane1_off + (r % P) * 4);
                         }
@@ -612,8 +668,10 @@ ap_status check_config(const ap_pool_config *c)
     if (!c) return fail(AP_EINVAL, "pool config is NULL");
     if (c->page_tokens < 1) return fail(AP_EINVAL, "page_tokens must be >= 1");
     if (c->page_bytes < 16 || c->page_bytes % 16) return fail(AP_EINVAL, "page_bytes must be a positive multiple of 16");
-    if (c->num_pages < 1 || c->spill_pages < 0 || c->num_pages + c->spill_pages >= (int64_t(1) << 31))
-        return fail(AP_EINVAL, "num_pages + spill_pages must lie in [1, 2^31)");
+    const int64_t nmax = ap::max_pages_of(*c);
+    if (c->num_pages < 0 || c->max_num_pages < 0 || nmax < 1 || c->num_pages > nmax || c->spill_pages < 0 ||
+        nmax + c->spill_pages >= (int64_t(1) << 31))
+        return fail(AP_EINVAL, "need 0 <= num_pages <= max_num_pages (>= 1) and max_num_pages + spill_pages < 2^31");
     if (c->num_slots < 1 || c->max_records_per_slot < 1) return fail(AP_EINVAL, "num_slots and max_records_per_slot must be >= 1");
     if (c->max_segments < 1 || c->max_segments > (1 << 20)) return fail(AP_EINVAL, "max_segments must lie in [1, 2^20]");
     if (c->max_pages_per_record < 1 || c->max_pages_per_record >= (int64_t(1) << 31))
@@ -650,6 +708,20 @@ bool plane_fit(const ap_pool *p, int32_t nplanes, const int64_t *rb, int64_t *pa
     return need <= p->cfg.page_bytes;
 }
 
+ap::PageSpace page_space(const ap_pool *p)
+{
+    ap::PageSpace ps;
+    ps.ring = reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring);
+    ps.spill_ring = reinterpret_cast<int32_t *>(p->dev_meta + p->M.spill_ring);
+    ps.pool = p->dev_pool;
+    ps.spill = p->spill_dev;
+    ps.N = p->cfg.num_pages;
+    ps.SB = ap::max_pages_of(p->cfg);
+    ps.SP = p->cfg.spill_pages;
+    ps.page_bytes = p->cfg.page_bytes;
+    return ps;
+}
+
 ap_status sync_read(ap_pool *p, void *host, const void *dev, size_t bytes)
 {
     cudaError_t e = cudaMemcpyAsync(host, dev, bytes, cudaMemcpyDeviceToHost, p->stream);
@@ -679,7 +751,8 @@ extern "C" ap_status ap_pool_init(ap_pool **out, const ap_pool_config *cfg, void
     *out = nullptr;
     ap_status s = check_config(cfg);
     if (s != AP_OK) return s;
-    if (!dev_pool || !dev_meta) return fail(AP_EINVAL, "pool_init: NULL pool or metadata buffer");
+    if (!dev_meta || (!dev_pool && cfg->num_pages > 0))
+        return fail(AP_EINVAL, "pool_init: NULL pool or metadata buffer");
     if ((reinterpret_cast<uintptr_t>(dev_pool) | reinterpret_cast<uintptr_t>(dev_meta)) & 255)
         return fail(AP_EINVAL, "pool_init: pool and metadata buffers must be 256-byte aligned");
     if ((cfg->spill_pages > 0) != (host_spill != nullptr))
@@ -739,16 +812,40 @@ extern "C" ap_status ap_pool_reset(ap_pool *p, void *stream)
         p->q_count[s] = 0;
     }
     p->last_flags = 0;
-    const int64_t n = p->cfg.num_pages > p->cfg.spill_pages ? p->cfg.num_pages : p->cfg.spill_pages;
+    const int64_t nmax = ap::max_pages_of(p->cfg);
+    const int64_t n = nmax > p->cfg.spill_pages ? nmax : p->cfg.spill_pages;
     int64_t grid = (n + 255) / 256;
     if (grid > 1024) grid = 1024;
     if (grid < 1) grid = 1;
     ap::k_reset<<<(unsigned)grid, 256, 0, p->stream>>>(reinterpret_cast<ap_pool_state *>(p->dev_meta),
                                                       reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),
-                                                      p->cfg.num_pages,
+                                                      p->cfg.num_pages, nmax,
                                                       reinterpret_cast<int32_t *>(p->dev_meta + p->M.spill_ring),
                                                       p->cfg.spill_pages);
     AP_CHECK_LAUNCH("pool reset launch");
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_grow(ap_pool *p, int64_t num_pages, void *dev_pool, void *stream)
+{
+    if (!p) return fail(AP_EINVAL, "pool_grow: NULL pool");
+    if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "pool_grow: not the paging stream");
+    const int64_t n0 = p->cfg.num_pages, nmax = ap::max_pages_of(p->cfg);
+    if (num_pages < n0 || num_pages > nmax)
+        return fail(AP_EINVAL, "pool_grow: %lld pages outside [%lld, %lld]", (long long)num_pages, (long long)n0,
+                    (long long)nmax);
+    uint8_t *pool = static_cast<uint8_t *>(dev_pool);
+    if (num_pages > 0 && !pool) return fail(AP_EINVAL, "pool_grow: NULL pool memory");
+    if (reinterpret_cast<uintptr_t>(pool) & 255) return fail(AP_EINVAL, "pool_grow: pool memory not 256-byte aligned");
+    if (n0 > 0 && pool != p->dev_pool)
+        return fail(AP_EINVAL, "pool_grow: the pool memory must keep its address once it holds pages");
+    if (num_pages == n0) return AP_OK;
+    ap::k_grow<<<1, 1024, 0, p->stream>>>(reinterpret_cast<ap_pool_state *>(p->dev_meta),
+                                          reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),
+                                          reinterpret_cast<int32_t *>(p->dev_meta + p->M.grow_tmp), n0, num_pages);
+    AP_CHECK_LAUNCH("pool grow launch");
+    p->cfg.num_pages = num_pages;
+    p->dev_pool = pool;
     return AP_OK;
 }
 
@@ -832,10 +929,8 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
     int64_t grid = bound * h.tiles_per_page;
     if (grid > p->max_ctas) grid = p->max_ctas;
     if (grid < 1) grid = 1;
-    ap::k_push_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(
-        st, rec, reinterpret_cast<const int32_t *>(p->dev_meta + p->M.ring),
-        reinterpret_cast<const int32_t *>(p->dev_meta + p->M.spill_ring), p->cfg.num_pages, p->cfg.spill_pages,
-        p->dev_pool, p->spill_dev, p->cfg.page_bytes, pl, h.rows_per_tile, h.tiles_per_page);
+    ap::k_push_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(st, rec, page_space(p), pl, h.rows_per_tile,
+                                                                        h.tiles_per_page);
     AP_CHECK_LAUNCH("stash push copy launch");
     p->next_id += 1;
     p->q_count[slot] += 1;
@@ -909,8 +1004,7 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
         const int64_t want = (T + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 16;
         const int grid = (int)(want < cap ? want : cap);
-        const int32_t *ring = reinterpret_cast<const int32_t *>(p->dev_meta + p->M.ring);
-        const int32_t *sring = reinterpret_cast<const int32_t *>(p->dev_meta + p->M.spill_ring);
+        const ap::PageSpace ps = page_space(p);
         const uint8_t *xs = static_cast<const uint8_t *>(x);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         const int32_t *blk = static_cast<const int32_t *>(scratch);
@@ -918,24 +1012,21 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
             const uint16_t *xs16 = static_cast<const uint16_t *>(x);
 #define AP_LAUNCH_E4M3(NRV)                                                                                       \
     ap::k_dispatch_stash_e4m3<NRV><<<grid, 256, 0, st>>>(                                                         \
-        xs16, T, H, idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, xd_scale, stt, rec, ring, sring,         \
-        p->cfg.num_pages, p->cfg.spill_pages, p->dev_pool, p->spill_dev, p->cfg.page_bytes, p->cfg.page_tokens,    \
-        page_off[1])
+        xs16, T, H, idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, xd_scale, stt, rec, ps,                  \
+        p->cfg.page_tokens, page_off[1])
             if (H <= 256 * 4) AP_LAUNCH_E4M3(4);
             else if (H <= 256 * 8) AP_LAUNCH_E4M3(8);
             else if (H <= 256 * 9) AP_LAUNCH_E4M3(9);
             else AP_LAUNCH_E4M3(16);
 #undef AP_LAUNCH_E4M3
         } else if ((al & 15) == 0)
-            ap::k_dispatch_stash_copy<int4><<<grid, 256, 0, st>>>(
-                xs, T, rb[0], idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, stt, rec, ring, sring,
-                p->cfg.num_pages, p->cfg.spill_pages, p->dev_pool, p->spill_dev, p->cfg.page_bytes,
-                p->cfg.page_tokens);
+            ap::k_dispatch_stash_copy<int4><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, capacity, blk,
+                                                                  seg_off, src_tok, xo, stt, rec, ps,
+                                                                  p->cfg.page_tokens);
         else
-            ap::k_dispatch_stash_copy<int2><<<grid, 256, 0, st>>>(
-                xs, T, rb[0], idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, stt, rec, ring, sring,
-                p->cfg.num_pages, p->cfg.spill_pages, p->dev_pool, p->spill_dev, p->cfg.page_bytes,
-                p->cfg.page_tokens);
+            ap::k_dispatch_stash_copy<int2><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, capacity, blk,
+                                                                  seg_off, src_tok, xo, stt, rec, ps,
+                                                                  p->cfg.page_tokens);
         AP_CHECK_LAUNCH("dispatch_stash copy launch");
     }
     p->next_id += 1;
@@ -973,10 +1064,8 @@ extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, voi
     int64_t grid = h.bound_pages * h.tiles_per_page;
     if (grid > p->max_ctas) grid = p->max_ctas;
     if (grid < 1) grid = 1;
-    ap::k_pop_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(
-        st, rec, reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),
-        reinterpret_cast<int32_t *>(p->dev_meta + p->M.spill_ring), p->cfg.num_pages, p->cfg.spill_pages,
-        p->dev_pool, p->spill_dev, p->cfg.page_bytes, pl, dst_rows, h.rows_per_tile, h.tiles_per_page);
+    ap::k_pop_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(st, rec, page_space(p), pl, dst_rows,
+                                                                       h.rows_per_tile, h.tiles_per_page);
     AP_CHECK_LAUNCH("stash pop copy launch");
     if (record_id) *record_id = h.id;
     p->q_head[slot] = (p->q_head[slot] + 1) % p->cfg.max_records_per_slot;

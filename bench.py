@@ -201,11 +201,6 @@ class Step:
         torch.cuda.synchronize(device)
         self.R = wl.rows
         self.bytes = op_bytes(wl, self.R)
-        # kernels per chunk: route 1; dispatch 3 (count/rank, scan, copy); push 2
-        # (plan, copy); pop 2 (plan, copy); combine 1.  Fused dispatch + push 3
-        # (count/rank, scan + plan, copy).
-        self.launches_per_step = wl.chunks * (1 + 3 + 2 + 2 + 1)
-        self.launches_per_step_fused = wl.chunks * (1 + 3 + 2 + 1)
 
     def run(self, events=None, fused=False):
         """Enqueue one step.  events: dict op -> list of (start, end) event pairs.
@@ -493,7 +488,6 @@ class ScheduleStep:
                       "combine": R * H * 2 + T * H * 2 + T * k * 8}
         self.tokens = T * sum(1 for op, _ in sched if op == "push")
         self.rows_kept = R
-        self.launches = sum(4 if op == "push" else 3 for op, _ in sched)
 
     def spilled_bytes(self):
         """Bytes one pass of the schedule sends over the host link: every
@@ -562,8 +556,10 @@ def native_schedule(args):
         st.run()
     torch.cuda.synchronize(device)
     g = torch.cuda.CUDAGraph()
+    n0 = st.ap.launch_count()
     with torch.cuda.graph(g, stream=st.stream):
         st.run()
+    launches_per_pass = st.ap.launch_count() - n0  # library kernels one replay runs
     for _ in range(2):
         with torch.cuda.stream(st.stream):
             g.replay()
@@ -600,7 +596,7 @@ def native_schedule(args):
             "config": {"T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "capacity": wl.capacity, "padded": wl.padded,
                        "fp8": wl.fp8, "page_tokens": wl.page_tokens, "num_pages": wl.num_pages,
                        "spill_pages": wl.spill_pages, "schedule": [f"{op} {n}" for op, n in st.sched][:12]},
-            "ops": ops, "pool_flags": flags, "gpu_launches": st.launches * steps, "clocks": clocks,
+            "ops": ops, "pool_flags": flags, "gpu_launches": launches_per_pass * steps, "clocks": clocks,
             "note": "ops: mean CUDA-event time per call over eager passes; pops of spilled records read host memory"}
     print(json.dumps(line), flush=True)
 
@@ -638,22 +634,27 @@ def native(args):
     cuda_build.build()
     wl = inputs.WORKLOADS[WORKLOAD]
     step = Step(wl, device, seed_base=1000 * rank)
+    ap = step.ap
     tokens_per_step = wl.T * wl.chunks
 
     fused_main = not args.unfused
 
     def capture(fused):
+        """The step as a CUDA graph, and the library kernels one replay runs
+        (counted by the library while the graph is recorded)."""
         g = torch.cuda.CUDAGraph()
+        n0 = ap.launch_count()
         with torch.cuda.graph(g, stream=step.stream):
             if fused and wl.chunks == 2 and not args.serial:
                 step.run_concurrent()
             else:
                 step.run(fused=fused)
+        n = ap.launch_count() - n0
         for _ in range(3):
             with torch.cuda.stream(step.stream):
                 g.replay()
         torch.cuda.synchronize(device)
-        return g
+        return g, n
 
     for _ in range(max(args.warmup, 3)):
         step.run(fused=fused_main)
@@ -661,7 +662,7 @@ def native(args):
 
     # one step captured as a CUDA graph: live counts, offsets and pages stay on
     # the device, so every replay re-routes from the current inputs
-    graph = None if args.eager else capture(fused_main)
+    graph, launches_per_step = (None, 0) if args.eager else capture(fused_main)
 
     def one_step():
         if graph is not None:
@@ -677,10 +678,14 @@ def native(args):
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    n_launch0 = ap.launch_count()
     t0.record(step.stream)
     for _ in range(args.steps):
         one_step()
     t1.record(step.stream)
+    # kernels run in the timed region: eager calls count as they launch, a
+    # graph replay runs the kernels counted when it was captured
+    timed_launches = launches_per_step * args.steps if graph is not None else ap.launch_count() - n_launch0
     torch.cuda.synchronize(device)
     barrier(world)
     clocks = sampler.stop()
@@ -698,7 +703,7 @@ def native(args):
     # the other step variant (fused <-> separate dispatch and push), for comparison
     alt = None
     if not args.eager and not args.no_alt:
-        g2 = capture(not fused_main)
+        g2, _ = capture(not fused_main)
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(step.stream)
@@ -795,7 +800,7 @@ def native(args):
                            "step": ("route, fused dispatch + push, pop, combine per chunk" if fused_main
                                     else "route, dispatch, push, pop, combine per chunk")},
                 "roofline": roofline, "ops": ops, "alt": alt, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
-                "gpu_launches": (step.launches_per_step_fused if fused_main else step.launches_per_step) * args.steps,
+                "gpu_launches": timed_launches,
                 "clocks": clocks}
         print(json.dumps(line), flush=True)
     if world > 1:

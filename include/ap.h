@@ -66,6 +66,12 @@ const char *ap_last_error(void);
 /* Library version, e.g. "0.1.0". */
 const char *ap_version(void);
 
+/* Number of kernels this library has enqueued in this process (launched on a
+ * stream, or recorded into a CUDA graph under stream capture; a graph replay
+ * does not count again).  Every call that enqueues work adds its launches here
+ * after the launch succeeded.  Thread-safe; never fails. */
+uint64_t ap_launch_count(void);
+
 /* ============================================================================
  * route_topk
  *
@@ -249,7 +255,7 @@ typedef struct {
     int32_t page_tokens;          /* P: rows per page, >= 1                    */
     int32_t num_slots;            /* S: independent FIFO record queues         */
     int64_t page_bytes;           /* bytes per page, multiple of 16            */
-    int64_t num_pages;            /* N: device pages, 1 .. 2^31-1              */
+    int64_t num_pages;            /* N: device pages now, 0 .. max_num_pages   */
     int64_t spill_pages;          /* host spill pages, >= 0                    */
     int32_t max_records_per_slot; /* queue depth of each slot                  */
     int32_t max_segments;         /* largest nseg of a push                    */
@@ -257,10 +263,17 @@ typedef struct {
     int32_t max_ctas;             /* copy grid bound; 0: environment variable
                                      AP_STASH_MAX_CTAS if set, else 2048       */
     int32_t reserved;             /* must be 0                                 */
+    int64_t max_num_pages;        /* most device pages ap_pool_grow may reach;
+                                     0: num_pages (the pool never grows).  Spill
+                                     page ids start here.  num_pages may be 0
+                                     when this is >= 1 (calibration: no device
+                                     pages yet)                                */
 } ap_pool_config;
 
-/* Device state word block at the start of the metadata buffer (read-only for
- * users; counters grow monotonically, ring positions are counter mod size). */
+/* Device state block at the start of the metadata buffer (read-only for
+ * users; counters grow monotonically between grows, ring positions are
+ * counter mod the current number of pages; ap_pool_grow re-bases the device
+ * ring to head = 0). */
 typedef struct {
     uint64_t head, tail;             /* free device ring: free = tail - head   */
     uint64_t spill_head, spill_tail; /* free spill ring                        */
@@ -268,7 +281,13 @@ typedef struct {
     uint32_t pad0;
     int64_t high_water;              /* most device pages ever in use          */
     int64_t spill_high_water;        /* most spill pages ever in use           */
-    int64_t pad1;
+    int64_t held;                    /* pages (device + spill + lost) of the
+                                        queued records                         */
+    int64_t held_high_water;         /* most pages ever held by queued records:
+                                        the device pages at which no push of
+                                        the same schedule spills (calibration) */
+    int64_t num_pages;               /* device pages now                       */
+    int64_t pad[6];
 } ap_pool_state;
 
 /* Per-record summary returned by ap_pool_read_record. */
@@ -278,7 +297,8 @@ typedef struct {
     int64_t npages, ndev, nspill, nlost;
 } ap_record_info;
 
-/* Sizes the caller must provide: device pool bytes (N * page_bytes),
+/* Sizes the caller must provide: device pool bytes (N * page_bytes; a pool
+ * that will grow needs max_num_pages * page_bytes of address range by then),
  * device metadata bytes, and host spill bytes (spill_pages * page_bytes). */
 ap_status ap_pool_required_bytes(const ap_pool_config *cfg,
                                  int64_t *dev_pool_bytes,
@@ -286,7 +306,8 @@ ap_status ap_pool_required_bytes(const ap_pool_config *cfg,
                                  int64_t *host_spill_bytes);
 
 /* Create a pool over caller-owned memory.  dev_pool: device, 256-byte aligned,
- * dev_pool_bytes.  dev_meta: device, 256-byte aligned, dev_meta_bytes.
+ * dev_pool_bytes (may be NULL when num_pages == 0: its first grow gives it).
+ * dev_meta: device, 256-byte aligned, dev_meta_bytes.
  * host_spill: pinned host memory (cudaHostAlloc / torch pin_memory) of
  * host_spill_bytes, mapped into the device address space; NULL iff
  * spill_pages == 0.  paging_stream: the one stream every later push, pop and
@@ -299,6 +320,23 @@ ap_status ap_pool_init(ap_pool **out, const ap_pool_config *cfg,
 /* Asynchronously return every page, clear flags and statistics, and empty
  * the record queues.  Pool bytes are not touched. */
 ap_status ap_pool_reset(ap_pool *pool, void *stream);
+/* Lazy sizing (Megatron-LM pull 7342, "Summary": the activation arena's
+ * capacity grows lazily; torchtitan pull 5541, "AI-Generated Details":
+ * calibration before the paged buffers exist).  Grow the device pool to
+ * num_pages (num_pages .. max_num_pages) on the paging stream, with records
+ * still queued: pages N .. num_pages-1 join the free ring after the pages
+ * already free (the ring is rewritten from position 0 in the order the free
+ * pages would have been taken: head = 0, tail = free + new).  Pages in use,
+ * page tables, spill pages and flags do not change.  dev_pool: the pool
+ * memory, now at least num_pages * page_bytes bytes; it must be the address
+ * given before (grow the mapping in place, e.g. with ap_arena_grow) unless
+ * the pool had no device pages, in which case it is the first pool address.
+ * Kernels take the page count by value: a CUDA graph captured before a grow
+ * must be captured again.  A typical use: run one step on a pool created
+ * with num_pages = 0 and spill pages for its records (the live prefixes are
+ * parked in pinned host memory and reload restores them), read
+ * held_high_water, grow to it, reset, and run. */
+ap_status ap_pool_grow(ap_pool *pool, int64_t num_pages, void *dev_pool, void *stream);
 /* Free the host object (not the caller's buffers). */
 ap_status ap_pool_destroy(ap_pool *pool);
 /* Resolved copy-grid bound of the pool (max_ctas after the environment). */
@@ -374,17 +412,41 @@ ap_status ap_pool_flags_device_ptr(const ap_pool *pool, uint32_t **d_flags);
 ap_status ap_overflow_query(ap_pool *pool, uint32_t *flags, int32_t wait);
 /* Whole state block (synchronises). */
 ap_status ap_pool_read_state(ap_pool *pool, ap_pool_state *state);
-/* Free rings: ring [num_pages] int32 and spill_ring [spill_pages] int32
+/* Free rings: ring [num_pages now] int32 and spill_ring [spill_pages] int32
  * (host, written; spill_ring may be NULL).  Synchronises. */
 ap_status ap_pool_read_rings(ap_pool *pool, int32_t *ring,
                              int32_t *spill_ring);
 /* Record at queue position qpos (0 = oldest) of a slot: its summary and up
- * to cap page-table entries (device page p -> p, spill page s -> N + s,
- * lost -> -1), first rows and row counts (host arrays, each may be NULL).
- * Synchronises. */
+ * to cap page-table entries (device page p -> p, spill page s ->
+ * max_num_pages + s, lost -> -1), first rows and row counts (host arrays,
+ * each may be NULL).  Synchronises. */
 ap_status ap_pool_read_record(ap_pool *pool, int32_t slot, int32_t qpos,
                               ap_record_info *info, int32_t *page_table,
                               int64_t *row0, int32_t *nrows, int64_t cap);
+
+/* ============================================================================
+ * Growable device arena: a reserved range of device virtual addresses whose
+ * prefix is backed by physical memory on demand (CUDA virtual memory
+ * management), so a pool can grow in place without moving the pages it
+ * already holds.  The arena is the caller's allocator: the pool calls never
+ * create or grow one.  Memory is mapped read-write for the device it was
+ * created on, in steps of the allocation granularity.
+ * ========================================================================== */
+typedef struct ap_arena ap_arena; /* opaque host object */
+
+/* Reserve max_bytes (> 0, rounded up to the granularity) of address range on
+ * `device`; nothing is mapped yet.  AP_ENOTSUP when the device or driver
+ * lacks virtual memory management. */
+ap_status ap_arena_create(ap_arena **out, int64_t max_bytes, int32_t device);
+/* Back the first `bytes` of the arena with memory (rounded up to the
+ * granularity; never shrinks; AP_EINVAL beyond the reservation).  Mapped
+ * bytes keep their contents and address. */
+ap_status ap_arena_grow(ap_arena *arena, int64_t bytes);
+/* Base address and bytes mapped so far (host, written). */
+ap_status ap_arena_info(const ap_arena *arena, void **base, int64_t *mapped_bytes, int64_t *reserved_bytes);
+/* Unmap and release everything.  The caller makes sure no queued work still
+ * uses the arena (e.g. synchronises the streams that used it). */
+ap_status ap_arena_destroy(ap_arena *arena);
 
 /* ============================================================================
  * E4M3 conversion used by the FP8 dispatch, exposed for testing the format:

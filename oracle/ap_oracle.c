@@ -536,7 +536,8 @@ or_pool *or_pool_new(int32_t P, int64_t page_bytes, int64_t N, int32_t S,
             memset(p->spill, fill, (size_t)(SP * page_bytes));
         }
     }
-    for (int64_t i = 0; i < N; ++i)
+    /* every slot of the ring, also those a grow brings into use later */
+    for (int64_t i = 0; i < NMAX; ++i)
         p->ring[i] = (int32_t)i;
     for (int64_t i = 0; i < SP; ++i)
         p->spill_ring[i] = (int32_t)i;
@@ -574,7 +575,7 @@ void or_pool_reset(or_pool *p)
         p->q_head[s] = 0;
         p->q_count[s] = 0;
     }
-    for (int64_t i = 0; i < p->N; ++i)
+    for (int64_t i = 0; i < p->NMAX; ++i)
         p->ring[i] = (int32_t)i;
     for (int64_t i = 0; i < p->SP; ++i)
         p->spill_ring[i] = (int32_t)i;

@@ -59,9 +59,28 @@ def test_required_bytes_host_only(lib):
         PoolConfig(4, 1, 4096, 2 ** 31, 0, 8, 8, 16, 0, 0),  # page ids beyond int32
         PoolConfig(4, 1, 4096, 16, 0, 8, 8, 16, -1, 0),     # negative grid bound
         PoolConfig(4, 1, 4096, 16, 0, 8, 8, 16, 0, 7),      # reserved != 0
+        PoolConfig(4, 1, 4096, 17, 0, 8, 8, 16, 0, 0, 16),  # more pages than the growth limit
+        PoolConfig(4, 1, 4096, 0, 0, 8, 8, 16, 0, 0, -1),   # negative growth limit
+        PoolConfig(4, 1, 4096, 8, 2 ** 31 - 16, 8, 8, 16, 0, 0, 16),  # spill ids beyond int32
     ]
     for cfg in bad:
         assert lib.ap_pool_required_bytes(ctypes.byref(cfg), None, None, None) == -1
+    # a calibration pool: no device pages yet, room for 100; the metadata
+    # holds the ring for 100 pages and the grow work space
+    cal = PoolConfig(4, 1, 4096, 0, 50, 8, 8, 16, 0, 0, 100)
+    assert lib.ap_pool_required_bytes(ctypes.byref(cal), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)) == 0
+    assert a.value == 0 and c.value == 50 * 4096
+    assert b.value >= 256 + 4 * 100 + 4 * 50 + 4 * 100
+
+
+def test_arena_without_a_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    a = ctypes.c_void_p(1)
+    assert lib.ap_arena_create(ctypes.byref(a), 1 << 20, 0) in (-4, -6)  # AP_ECUDA or AP_ENOTSUP
+    assert not a.value
+    assert lib.ap_arena_destroy(None) == 0
 
 
 def test_route_rejects_bad_sizes(lib):
@@ -72,8 +91,10 @@ def test_route_rejects_bad_sizes(lib):
     assert lib.ap_route_topk(p, 10, 64, 33, p, p, None) == -1     # k > 32
     assert lib.ap_route_topk(None, 10, 8, 2, p, p, None) == -1    # NULL logits
     assert lib.ap_route_topk(None, 0, 8, 2, None, None, None) == 0  # empty: nothing to do
+    n0 = lib.ap_launch_count()
     assert lib.ap_route_topk(p, 10, 8, 9, p, p, None) == -1
     assert b"bad sizes" in lib.ap_last_error()
+    assert lib.ap_launch_count() == n0  # a rejected call enqueues nothing
 
 
 def test_dispatch_rejects_bad_arguments(lib):

@@ -23,6 +23,8 @@ FILL = 0xA5
     (1000, 264, 16, 4, 0, False, 32, 150, 0),     # compact, 8-byte rows path, page tails
     (777, 2056, 32, 6, 0, False, 64, 40, 64),     # odd hidden size; pool overflows into spill
     (300, 64, 8, 2, 0, False, 8, 10, 5),          # spill exhausted: lost pages
+    (600, 64, 1024, 16, 0, False, 8, 3000, 0),    # the most experts
+    (131100, 64, 64, 8, 0, False, 64, 16000, 2000),  # a record of 1.05 M pairs; spills
 ])
 def test_fused_matches_oracle_dispatch_then_push(T, H, E, k, C, padded, P, N, SP):
     rb = H * 2
@@ -111,6 +113,7 @@ def test_fused_host_errors():
     (4096, 2048, 64, 6, 128, 120, 0),    # the FP8 layer-stack shape (register path, 8 vectors per lane)
     (999, 2056, 64, 6, 128, 40, 64),     # odd hidden size, ragged tail, spill
     (300, 1024, 16, 4, 32, 20, 4),       # 4 vectors per lane; lost pages
+    (175000, 64, 64, 6, 128, 8300, 100),  # a record of 1.05 M pairs; spills
 ])
 def test_fused_e4m3_matches_oracle(T, H, E, k, P, N, SP):
     rb = (H, 4)
@@ -150,3 +153,36 @@ def test_fused_e4m3_matches_oracle(T, H, E, k, P, N, SP):
     torch.cuda.synchronize()
     assert np.array_equal(host(dg[0]), dq[0]) and np.array_equal(host(dg[1]), dq[1])
     assert g.state() == o.state()
+
+
+def test_launch_counter_counts_enqueued_kernels():
+    """The library counts the kernels it enqueues: eager calls as they launch,
+    graph capture once, replays not at all."""
+    T, H, E, k = 256, 64, 8, 2
+    logits = torch.from_numpy(inputs.router_logits(3, T, E)).cuda()
+    x = bf16_to_dev(inputs.normal_bf16(3, inputs.X_STREAM, (T, H)))
+    g = ap.Pool(16, ap.page_bytes_for(16, (2 * H,)), 64, 1, 2, E)
+    n0 = ap.launch_count()
+    idx, w = ap.route_topk(logits, k)
+    assert ap.launch_count() - n0 == 1
+    n1 = ap.launch_count()
+    with torch.cuda.stream(g.stream):
+        g.stream.wait_stream(torch.cuda.default_stream())
+        d = g.dispatch_stash(0, x, idx, E)
+        y = torch.empty_like(d["xd"])
+        g.pop(0, [y])
+    torch.cuda.synchronize()
+    assert ap.launch_count() - n1 == 5  # count/rank, scan + plan, fused copy, pop plan, pop copy
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ap.route_topk(logits, k, idx, w, stream=s)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    n2 = ap.launch_count()
+    with torch.cuda.graph(graph, stream=s):
+        ap.route_topk(logits, k, idx, w, stream=s)
+    assert ap.launch_count() - n2 == 1
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert ap.launch_count() - n2 == 1

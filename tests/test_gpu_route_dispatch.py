@@ -82,6 +82,9 @@ def check_plan(plan, out):
     (7, 40, 4, 3, 2, True),            # fewer tokens than a warp
     (300, 12, 8, 2, 0, False),         # rows of 24 bytes: 8-byte vectors
     (100, 7, 8, 2, 0, False),          # rows of 14 bytes: 2-byte vectors
+    (3000, 32, 1024, 32, 0, False),    # the most experts and choices
+    (131073, 64, 64, 8, 0, False),     # a record of 2^20 + 8 pairs (2049 rank blocks)
+    (140000, 32, 128, 8, 9000, True),  # large padded record with drops
 ])
 def test_dispatch_bf16_matches_oracle(T, H, E, k, C, padded):
     plan, out, st = dispatch_both(T, H, E, k, C, padded, seed=T)
@@ -91,7 +94,7 @@ def test_dispatch_bf16_matches_oracle(T, H, E, k, C, padded):
 
 
 @pytest.mark.parametrize("T,H,E,k", [(4096, 2048, 64, 6), (4096, 2056, 64, 6), (333, 100, 8, 3), (65, 30, 4, 2),
-                                     (50, 9, 4, 2)])
+                                     (50, 9, 4, 2), (175000, 64, 64, 6)])  # the last: a record of 1.05 M pairs
 def test_dispatch_e4m3_matches_oracle(T, H, E, k):
     plan, out, st = dispatch_both(T, H, E, k, 0, False, fp8=True, seed=H)
     assert st == 0

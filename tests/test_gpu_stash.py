@@ -21,13 +21,20 @@ FILL = 0xA5
 class Twin:
     """One GPU pool and one oracle pool driven with the same operations."""
 
-    def __init__(self, P, rb, N, S=2, R=8, segs=64, maxp=None, SP=0, max_ctas=0, keep_bytes=True):
+    def __init__(self, P, rb, N, S=2, R=8, segs=64, maxp=None, SP=0, max_ctas=0, keep_bytes=True, NMAX=0):
         self.page_bytes = ap.page_bytes_for(P, rb)
-        maxp = maxp or (N + SP)
-        self.g = ap.Pool(P, self.page_bytes, N, S, R, segs, maxp, SP, max_ctas=max_ctas, fill=FILL)
-        self.o = oracle.Pool(P, self.page_bytes, N, S, R, segs, maxp, SP, keep_bytes=keep_bytes, fill=FILL)
+        maxp = maxp or (max(N, NMAX) + SP)
+        self.g = ap.Pool(P, self.page_bytes, N, S, R, segs, maxp, SP, max_ctas=max_ctas, fill=FILL,
+                         max_num_pages=NMAX)
+        self.o = oracle.Pool(P, self.page_bytes, N, S, R, segs, maxp, SP, keep_bytes=keep_bytes, fill=FILL,
+                             max_num_pages=NMAX)
         self.S = S
         self.rb = rb
+
+    def grow(self, n):
+        self.g.grow(n)
+        self.o.grow(n)
+        torch.cuda.synchronize()
 
     def push(self, slot, planes_np, seg_off, live):
         dev = [to_dev(p) for p in planes_np]
@@ -68,7 +75,7 @@ class Twin:
                 for key in ("page_table", "row0", "nrows"):
                     assert np.array_equal(a[key], b[key]), key
         if images:
-            assert np.array_equal(host(self.g.pool), self.o.pool_bytes())
+            assert np.array_equal(host(self.g.pool), self.o.pool_bytes()[:self.g.N * self.page_bytes])
             if self.g.spill is not None:
                 assert np.array_equal(self.g.spill.numpy(), self.o.spill_bytes())
 
