@@ -422,6 +422,17 @@ class Pool:
                                     self.stream.cuda_stream), "stash_pop")
         return rid.value
 
+    def time_copies(self, before: torch.cuda.Event | None, after: torch.cuda.Event | None):
+        """Record ``before`` / ``after`` (timing events) around the copy kernel
+        of every following push, fused dispatch + push and pop; None, None
+        stops it.  The events must stay alive while set."""
+        for e in (before, after):
+            if e is not None and e.cuda_event == 0:
+                e.record(self.stream)  # torch creates the event on its first record
+        self._timing = (before, after)  # keep them alive while the library holds them
+        check(self.lib.ap_pool_time_copies(self.handle, before.cuda_event if before is not None else None,
+                                           after.cuda_event if after is not None else None), "pool_time_copies")
+
     def queue_len(self, slot: int) -> int:
         v = ctypes.c_int32()
         check(self.lib.ap_pool_queue_len(self.handle, slot, ctypes.byref(v)), "pool_queue_len")

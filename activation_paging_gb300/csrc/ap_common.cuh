@@ -1,6 +1,8 @@
 // Shared device and host helpers of the CUDA library (not part of the ABI).
 #pragma once
 
+#include <utility>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -45,6 +47,38 @@ int dispatch_blocks(int64_t T);
         if (e_ != cudaSuccess) return ::ap::cuda_fail(e_, what); \
         ::ap::note_launch();                                    \
     } while (0)
+
+// ---- programmatic dependent launch -------------------------------------------
+// Every kernel of the library begins with pdl_begin() and is launched with
+// launch(), i.e. with programmatic stream serialization: the next kernel on
+// the stream may start launching once every block of this one has started,
+// and its blocks then wait in their own pdl_begin() until this grid has
+// finished and its memory is visible.  The chains of small dependent kernels
+// (route, count/rank, scan + plan, copy, pop plan, pop copy, combine) thereby
+// overlap each launch with the end of the kernel before it; no kernel touches
+// memory before its wait, so results do not change.  After a kernel launched
+// without the attribute, or an event, the wait returns at once.
+template <typename... KArgs, typename... Args>
+inline void launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...); // errors surface in AP_CHECK_LAUNCH
+}
+
+__device__ __forceinline__ void pdl_begin()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // ---- device helpers ----------------------------------------------------------
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(256, 4) k_combine(const uint16_t *__restrict__
                                                  const int32_t *__restrict__ dest, const float *__restrict__ w,
                                                  int64_t T, int k, uint16_t *__restrict__ out, uint32_t *d_status)
 {
+    pdl_begin();
     using V = typename Vec<VE>::T;
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
@@ -136,7 +137,7 @@ void launch_combine(const uint16_t *y, int64_t y_rows, int H, const int32_t *des
     const int64_t items = T * ((nstep + U * kWarp - 1) / (U * kWarp));
     const int64_t want = (items + 7) / 8;
     const int grid = (int)(want < resident ? want : resident);
-    k_combine<VE, U, KB><<<grid, 256, 0, st>>>(y, y_rows, H, dest, w, T, k, out, d_status);
+    launch(k_combine<VE, U, KB>, grid, 256, 0, st, y, y_rows, H, dest, w, T, k, out, d_status);
 }
 
 // Backward of combine, one warp per token (a deterministic dot product):
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t *__restrict_
                                                      int64_t T, int k, uint16_t *__restrict__ dy,
                                                      float *__restrict__ dw, uint32_t *d_status)
 {
+    pdl_begin();
     using V = typename Vec<VE>::T;
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
@@ -201,7 +203,7 @@ void launch_combine_bwd(const uint16_t *dout, const uint16_t *y, int64_t y_rows,
 {
     static const int resident = resident_grid((const void *)k_combine_bwd<VE>, 256);
     const int64_t want = (T + 7) / 8;
-    k_combine_bwd<VE><<<(int)(want < resident ? want : resident), 256, 0, st>>>(dout, y, y_rows, H, dest, w, T, k,
+    launch(k_combine_bwd<VE>, (int)(want < resident ? want : resident), 256, 0, st, dout, y, y_rows, H, dest, w, T, k,
                                                                               dy, dw, d_status);
 }
 

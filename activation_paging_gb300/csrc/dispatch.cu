@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(1024) k_scan(int32_t *__restrict__ blk, int nb
                                                 int padded, int32_t *__restrict__ counts,
                                                 int32_t *__restrict__ live, int32_t *__restrict__ seg_off)
 {
+    pdl_begin();
     int32_t my_live, my_off;
     scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off, my_live, my_off);
 }
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__re
                                                              int32_t *__restrict__ blk, int32_t *__restrict__ dest,
                                                              uint32_t *d_status)
 {
+    pdl_begin();
     extern __shared__ int32_t cnt[]; // [kRankWarps][E]
     const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
     for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(256) k_copy_rows(const uint8_t *__restrict__ x
                                                    const int32_t *__restrict__ seg_off,
                                                    int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd)
 {
+    pdl_begin();
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int64_t nvec = rb / (int64_t)sizeof(V);
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(256) k_copy_rows_e4m3(const uint16_t *__restri
                                                         int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd,
                                                         float *__restrict__ xd_scale)
 {
+    pdl_begin();
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int nstep = H / VE;
@@ -235,6 +239,7 @@ __global__ void __launch_bounds__(256) k_copy_rows_e4m3_reg(const uint16_t *__re
                                                             int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd,
                                                             float *__restrict__ xd_scale)
 {
+    pdl_begin();
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int nstep = H / 8;
@@ -286,6 +291,7 @@ __global__ void __launch_bounds__(256) k_copy_rows_e4m3_reg(const uint16_t *__re
 
 __global__ void k_cast_e4m3(const float *__restrict__ in, uint8_t *__restrict__ out, int64_t n)
 {
+    pdl_begin();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         out[i] = to_e4m3(in[i]);
 }
@@ -307,7 +313,7 @@ void launch_copy(const uint8_t *x, int64_t T, int64_t rb, const Ranks &r, uint8_
     // one warp per token; blocks beyond the resident ones start as others retire
     const int64_t want = (T + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * 16;
-    k_copy_rows<V><<<(int)(want < cap ? want : cap), 256, 0, st>>>(x, T, rb, r.idx, r.dest, r.k, r.E, r.capacity,
+    launch(k_copy_rows<V>, (int)(want < cap ? want : cap), 256, 0, st, x, T, rb, r.idx, r.dest, r.k, r.E, r.capacity,
                                                                    r.blk, r.seg_off, r.src_tok, xd);
 }
 
@@ -317,7 +323,7 @@ void launch_e4m3_reg(const uint16_t *x, int64_t T, int H, const Ranks &r, uint8_
 {
     const int64_t want = (T + 7) / 8; // one warp per token
     const int64_t cap = (int64_t)sm_count() * 16;
-    k_copy_rows_e4m3_reg<NR><<<(int)(want < cap ? want : cap), 256, 0, st>>>(
+    launch(k_copy_rows_e4m3_reg<NR>, (int)(want < cap ? want : cap), 256, 0, st, 
         x, T, H, r.idx, r.dest, r.k, r.E, r.capacity, r.blk, r.seg_off, r.src_tok, xd, xd_scale);
 }
 
@@ -326,7 +332,7 @@ void launch_e4m3(const uint16_t *x, int64_t T, int H, const Ranks &r, uint8_t *x
 {
     static const int resident = resident_grid((const void *)k_copy_rows_e4m3<VE>, 256);
     const int64_t want = (T + 7) / 8; // one warp per token
-    k_copy_rows_e4m3<VE><<<(int)(want < resident ? want : resident), 256, 0, st>>>(
+    launch(k_copy_rows_e4m3<VE>, (int)(want < resident ? want : resident), 256, 0, st, 
         x, T, H, r.idx, r.dest, r.k, r.E, r.capacity, r.blk, r.seg_off, r.src_tok, xd, xd_scale);
 }
 
@@ -371,7 +377,7 @@ ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t 
     const int64_t nb = nblocks(T);
     if (nb == 0) return AP_OK;
     const size_t smem = (size_t)kRankWarps * E * sizeof(int32_t);
-    k_count_rank<<<(unsigned)nb, kRankThreads, smem, st>>>(idx, T, k, E, static_cast<int32_t *>(scratch), dest,
+    launch(k_count_rank, (unsigned)nb, kRankThreads, smem, st, idx, T, k, E, static_cast<int32_t *>(scratch), dest,
                                                            d_status);
     AP_CHECK_LAUNCH("dispatch count/rank launch");
     return AP_OK;
@@ -385,7 +391,7 @@ ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E,
 {
     ap_status s = dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
     if (s != AP_OK) return s;
-    k_scan<<<1, 1024, 0, st>>>(static_cast<int32_t *>(scratch), (int)nblocks(T), E, capacity, padded, counts, live,
+    launch(k_scan, 1, 1024, 0, st, static_cast<int32_t *>(scratch), (int)nblocks(T), E, capacity, padded, counts, live,
                                seg_off);
     AP_CHECK_LAUNCH("dispatch scan launch");
     return AP_OK;
@@ -455,7 +461,7 @@ extern "C" ap_status ap_cast_e4m3(const float *in, uint8_t *out, int64_t n, void
     if (!in || !out) return fail(AP_EINVAL, "cast_e4m3: NULL pointer");
     const int64_t want = (n + 255) / 256;
     const int grid = (int)(want < (int64_t)sm_count() * 8 ? want : (int64_t)sm_count() * 8);
-    k_cast_e4m3<<<grid, 256, 0, (cudaStream_t)stream>>>(in, out, n);
+    launch(k_cast_e4m3, grid, 256, 0, (cudaStream_t)stream, in, out, n);
     AP_CHECK_LAUNCH("cast_e4m3 launch");
     return AP_OK;
 }

@@ -41,6 +41,7 @@ template <int NV>
 __global__ void __launch_bounds__(256) k_route_topk(const float *__restrict__ logits, int64_t T, int E, int k,
                                                      int32_t *__restrict__ idx, float *__restrict__ w)
 {
+    pdl_begin();
     constexpr int kNone = 0x7fffffff;
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
@@ -116,17 +117,17 @@ extern "C" ap_status ap_route_topk(const float *logits, int64_t T, int32_t E, in
     const int64_t want = (T + 7) / 8;
     const int grid = (int)(want < (int64_t)sm_count() * 16 ? want : (int64_t)sm_count() * 16);
     if (E <= 32)
-        k_route_topk<1><<<grid, threads, 0, st>>>(logits, T, E, k, idx, w);
+        launch(k_route_topk<1>, grid, threads, 0, st, logits, T, E, k, idx, w);
     else if (E <= 64)
-        k_route_topk<2><<<grid, threads, 0, st>>>(logits, T, E, k, idx, w);
+        launch(k_route_topk<2>, grid, threads, 0, st, logits, T, E, k, idx, w);
     else if (E <= 128)
-        k_route_topk<4><<<grid, threads, 0, st>>>(logits, T, E, k, idx, w);
+        launch(k_route_topk<4>, grid, threads, 0, st, logits, T, E, k, idx, w);
     else if (E <= 256)
-        k_route_topk<8><<<grid, threads, 0, st>>>(logits, T, E, k, idx, w);
+        launch(k_route_topk<8>, grid, threads, 0, st, logits, T, E, k, idx, w);
     else if (E <= 512)
-        k_route_topk<16><<<grid, threads, 0, st>>>(logits, T, E, k, idx, w);
+        launch(k_route_topk<16>, grid, threads, 0, st, logits, T, E, k, idx, w);
     else
-        k_route_topk<32><<<grid, threads, 0, st>>>(logits, T, E, k, idx, w);
+        launch(k_route_topk<32>, grid, threads, 0, st, logits, T, E, k, idx, w);
     AP_CHECK_LAUNCH("route_topk launch");
     return AP_OK;
 }

@@ -157,6 +157,7 @@ RecPtr rec_ptr(uint8_t *meta, const MetaLayout &M, int64_t index)
 // into use later (slots at or past N are never read before then).
 __global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int64_t NMAX, int32_t *spill_ring, int64_t SP)
 {
+    pdl_begin();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < NMAX; i += stride) ring[i] = (int32_t)i;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < SP; i += stride) spill_ring[i] = (int32_t)i;
@@ -182,6 +183,7 @@ __global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int64_t NMA
 // pages N0 .. N1-1 follow in id order, and the counters re-base to head = 0.
 __global__ void __launch_bounds__(1024) k_grow(ap_pool_state *st, int32_t *ring, int32_t *tmp, int64_t N0, int64_t N1)
 {
+    pdl_begin();
     const uint64_t head = st->head, tail = st->tail;
     const int64_t avail = (int64_t)(tail - head); // 0 when N0 == 0
     for (int64_t i = threadIdx.x; i < avail; i += blockDim.x) tmp[i] = ring[(head + (uint64_t)i) % (uint64_t)N0];
@@ -224,10 +226,35 @@ __device__ __forceinline__ void plan_descriptor(RecPtr rec, const int64_t *pg_ba
 // min(total, max_pages) pages come from the device ring at the head snapshot,
 // then from the spill ring, the rest are lost; the head counters advance, the
 // high-water marks and the sticky flags are updated.
-__device__ __forceinline__ void plan_allocate(ap_pool_state *st, RecPtr rec, int nseg, int64_t total,
-                                              int64_t max_pages, uint32_t f, uint64_t head, uint64_t tail,
-                                              uint64_t sh, uint64_t stl, int64_t N, int64_t SP)
+// The state fields a push plan reads, loaded together by the one thread that
+// later writes them back (a single round trip instead of one per field; only
+// the plan kernel running on the paging stream changes them meanwhile).
+struct StateSnap {
+    uint64_t head, tail, sh, stl;
+    int64_t hw, shw, held, hhw;
+    uint32_t flags;
+};
+
+__device__ __forceinline__ StateSnap load_state(const ap_pool_state *__restrict__ st)
 {
+    StateSnap s;
+    s.head = st->head;
+    s.tail = st->tail;
+    s.sh = st->spill_head;
+    s.stl = st->spill_tail;
+    s.hw = st->high_water;
+    s.shw = st->spill_high_water;
+    s.held = st->held;
+    s.hhw = st->held_high_water;
+    s.flags = st->flags;
+    return s;
+}
+
+__device__ __forceinline__ void plan_allocate(ap_pool_state *__restrict__ st, RecPtr rec, int nseg, int64_t total,
+                                              int64_t max_pages, uint32_t f, const StateSnap &snap, int64_t N,
+                                              int64_t SP)
+{
+    const uint64_t head = snap.head, tail = snap.tail, sh = snap.sh, stl = snap.stl;
     const int64_t kept = total < max_pages ? total : max_pages;
     if (total > max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
     const int64_t avail = (int64_t)(tail - head);
@@ -248,13 +275,13 @@ __device__ __forceinline__ void plan_allocate(ap_pool_state *st, RecPtr rec, int
     st->head = head + (uint64_t)ndev;
     st->spill_head = sh + (uint64_t)nspill;
     const int64_t in_use = N - (int64_t)(tail - (head + (uint64_t)ndev));
-    if (in_use > st->high_water) st->high_water = in_use;
+    if (in_use > snap.hw) st->high_water = in_use;
     const int64_t s_use = SP - (int64_t)(stl - (sh + (uint64_t)nspill));
-    if (s_use > st->spill_high_water) st->spill_high_water = s_use;
-    const int64_t held = st->held + kept; // pages of queued records, wherever they went
+    if (s_use > snap.shw) st->spill_high_water = s_use;
+    const int64_t held = snap.held + kept; // pages of queued records, wherever they went
     st->held = held;
-    if (held > st->held_high_water) st->held_high_water = held;
-    st->flags |= f;
+    if (held > snap.hhw) st->held_high_water = held;
+    st->flags = snap.flags | f;
 }
 
 // have_reg: nseg <= kPlanThreads and thread s already holds segment s's
@@ -262,8 +289,8 @@ __device__ __forceinline__ void plan_allocate(ap_pool_state *st, RecPtr rec, int
 __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, int nseg,
                                                const int32_t *__restrict__ d_seg_off,
                                                const int32_t *__restrict__ d_live, int64_t src_rows, int P,
-                                               int64_t max_pages, int64_t N, int64_t SP, bool have_reg = false,
-                                               int32_t reg_off = 0, int32_t reg_live = 0)
+                                               int64_t max_pages, int64_t N, int64_t SP, const StateSnap &snap,
+                                               bool have_reg = false, int32_t reg_off = 0, int32_t reg_live = 0)
 {
     __shared__ int64_t s_warp[kPlanThreads / kWarp];
     __shared__ int64_t s_carry;
@@ -274,13 +301,7 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
     __shared__ int32_t s_off[kPlanSmemSegs], s_live[kPlanSmemSegs];
     const bool in_smem = nseg <= kPlanSmemSegs;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    // the free-ring counters, read early (only this kernel changes them now)
-    uint64_t head = 0, tail = 0, sh = 0, stl = 0;
     if (tid == 0) {
-        head = st->head;
-        tail = st->tail;
-        sh = st->spill_head;
-        stl = st->spill_tail;
         s_carry = 0;
         s_flags = 0;
     }
@@ -341,7 +362,7 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
     const int32_t *seg_offs = in_smem ? s_off : rec.seg_off;
     for (int64_t ord = tid; ord < kept; ord += kPlanThreads) plan_descriptor(rec, pg_base, seg_live, seg_offs, nseg, ord, P);
     // 3. allocation: device pages first, then spill pages, then lost
-    if (tid == 0) plan_allocate(st, rec, nseg, total, max_pages, s_flags, head, tail, sh, stl, N, SP);
+    if (tid == 0) plan_allocate(st, rec, nseg, total, max_pages, s_flags, snap, N, SP);
 }
 
 __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, RecPtr rec, int nseg,
@@ -349,7 +370,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, R
                                                              const int32_t *__restrict__ d_live, int64_t src_rows,
                                                              int P, int64_t max_pages, int64_t N, int64_t SP)
 {
-    push_plan_body(st, rec, nseg, d_seg_off, d_live, src_rows, P, max_pages, N, SP);
+    pdl_begin();
+    StateSnap snap;
+    if (threadIdx.x == 0) snap = load_state(st);
+    push_plan_body(st, rec, nseg, d_seg_off, d_live, src_rows, P, max_pages, N, SP, snap);
 }
 
 // Fused dispatch + stash: the dispatch's expert scan and the record's page
@@ -362,10 +386,14 @@ __global__ void __launch_bounds__(kPlanThreads) k_scan_plan(int32_t *__restrict_
                                                              RecPtr rec, int64_t src_rows, int P, int64_t max_pages,
                                                              int64_t N, int64_t SP)
 {
+    pdl_begin();
+    StateSnap snap; // loaded before the scan, so its latency hides under it
+    if (threadIdx.x == 0) snap = load_state(st);
     int32_t my_live, my_off;
     scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off, my_live, my_off);
     __syncthreads();
-    push_plan_body(st, rec, E, seg_off, live, src_rows, P, max_pages, N, SP, E <= kPlanThreads, my_off, my_live);
+    push_plan_body(st, rec, E, seg_off, live, src_rows, P, max_pages, N, SP, snap, E <= kPlanThreads, my_off,
+                   my_live);
 }
 
 struct Planes {
@@ -380,6 +408,7 @@ constexpr int kCopyThreads = 256;
 __global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st, RecPtr rec, PageSpace ps,
                                                              Planes src, int rows_per_tile, int tiles_per_page)
 {
+    pdl_begin();
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
     const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
@@ -406,14 +435,18 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st
     }
 }
 
-__global__ void k_pop_plan(ap_pool_state *st, RecHdr *hdr)
+__global__ void k_pop_plan(ap_pool_state *__restrict__ st, RecHdr *__restrict__ hdr)
 {
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        hdr->tail0 = st->tail;
-        hdr->spill_tail0 = st->spill_tail;
-        st->tail = st->tail + (uint64_t)hdr->ndev;
-        st->spill_tail = st->spill_tail + (uint64_t)hdr->nspill;
-        st->held = st->held - hdr->npages;
+    pdl_begin();
+    if (blockIdx.x == 0 && threadIdx.x == 0) { // every load first: one round trip
+        const uint64_t tail = st->tail, stail = st->spill_tail;
+        const int64_t held = st->held;
+        const int64_t ndev = hdr->ndev, nspill = hdr->nspill, npages = hdr->npages;
+        hdr->tail0 = tail;
+        hdr->spill_tail0 = stail;
+        st->tail = tail + (uint64_t)ndev;
+        st->spill_tail = stail + (uint64_t)nspill;
+        st->held = held - npages;
     }
 }
 
@@ -421,6 +454,7 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
                                                             Planes dst, int64_t dst_rows, int rows_per_tile,
                                                             int tiles_per_page)
 {
+    pdl_begin();
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
     const uint64_t tail0 = rec.hdr->tail0, stail0 = rec.hdr->spill_tail0;
@@ -473,6 +507,7 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
                                                              uint8_t *__restrict__ xd, ap_pool_state *st, RecPtr rec,
                                                              PageSpace ps, int P)
 {
+    pdl_begin();
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int64_t nvec = rb / (int64_t)sizeof(V);
@@ -543,6 +578,7 @@ __global__ void __launch_bounds__(256, 3) k_dispatch_stash_e4m3(
     int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd, float *__restrict__ xd_scale, ap_pool_state *st,
     RecPtr rec, PageSpace ps, int P, int64_t plane1_off)
 {
+    pdl_begin();
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int nstep = H / 8;
@@ -657,6 +693,7 @@ struct ap_pool {
     uint64_t next_id = 1;
     void *pinned = nullptr; // small pinned host buffer for read-outs
     uint32_t last_flags = 0;
+    cudaEvent_t copy_before = nullptr, copy_after = nullptr; // ap_pool_time_copies
 };
 
 namespace {
@@ -706,6 +743,12 @@ bool plane_fit(const ap_pool *p, int32_t nplanes, const int64_t *rb, int64_t *pa
         need = page_off[1] + P * rb[1];
     }
     return need <= p->cfg.page_bytes;
+}
+
+// Records the caller's timing event (if set) on the paging stream.
+void mark(const ap_pool *p, cudaEvent_t ev)
+{
+    if (ev) (void)cudaEventRecord(ev, p->stream);
 }
 
 ap::PageSpace page_space(const ap_pool *p)
@@ -817,7 +860,7 @@ extern "C" ap_status ap_pool_reset(ap_pool *p, void *stream)
     int64_t grid = (n + 255) / 256;
     if (grid > 1024) grid = 1024;
     if (grid < 1) grid = 1;
-    ap::k_reset<<<(unsigned)grid, 256, 0, p->stream>>>(reinterpret_cast<ap_pool_state *>(p->dev_meta),
+    ap::launch(ap::k_reset, (unsigned)grid, 256, 0, p->stream, reinterpret_cast<ap_pool_state *>(p->dev_meta),
                                                       reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),
                                                       p->cfg.num_pages, nmax,
                                                       reinterpret_cast<int32_t *>(p->dev_meta + p->M.spill_ring),
@@ -840,12 +883,21 @@ extern "C" ap_status ap_pool_grow(ap_pool *p, int64_t num_pages, void *dev_pool,
     if (n0 > 0 && pool != p->dev_pool)
         return fail(AP_EINVAL, "pool_grow: the pool memory must keep its address once it holds pages");
     if (num_pages == n0) return AP_OK;
-    ap::k_grow<<<1, 1024, 0, p->stream>>>(reinterpret_cast<ap_pool_state *>(p->dev_meta),
+    ap::launch(ap::k_grow, 1, 1024, 0, p->stream, reinterpret_cast<ap_pool_state *>(p->dev_meta),
                                           reinterpret_cast<int32_t *>(p->dev_meta + p->M.ring),
                                           reinterpret_cast<int32_t *>(p->dev_meta + p->M.grow_tmp), n0, num_pages);
     AP_CHECK_LAUNCH("pool grow launch");
     p->cfg.num_pages = num_pages;
     p->dev_pool = pool;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_time_copies(ap_pool *p, void *before, void *after)
+{
+    if (!p) return fail(AP_EINVAL, "pool_time_copies: NULL pool");
+    if ((before == nullptr) != (after == nullptr)) return fail(AP_EINVAL, "pool_time_copies: give both events or neither");
+    p->copy_before = static_cast<cudaEvent_t>(before);
+    p->copy_after = static_cast<cudaEvent_t>(after);
     return AP_OK;
 }
 
@@ -915,7 +967,7 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
 
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *st = reinterpret_cast<ap_pool_state *>(p->dev_meta);
-    ap::k_push_plan<<<1, ap::kPlanThreads, 0, p->stream>>>(st, rec, nseg, d_seg_off, d_live, src_rows,
+    ap::launch(ap::k_push_plan, 1, ap::kPlanThreads, 0, p->stream, st, rec, nseg, d_seg_off, d_live, src_rows,
                                                            p->cfg.page_tokens, p->cfg.max_pages_per_record,
                                                            p->cfg.num_pages, p->cfg.spill_pages);
     AP_CHECK_LAUNCH("stash push plan launch");
@@ -929,9 +981,11 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
     int64_t grid = bound * h.tiles_per_page;
     if (grid > p->max_ctas) grid = p->max_ctas;
     if (grid < 1) grid = 1;
-    ap::k_push_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(st, rec, page_space(p), pl, h.rows_per_tile,
+    mark(p, p->copy_before);
+    ap::launch(ap::k_push_copy, (unsigned)grid, ap::kCopyThreads, 0, p->stream, st, rec, page_space(p), pl, h.rows_per_tile,
                                                                         h.tiles_per_page);
     AP_CHECK_LAUNCH("stash push copy launch");
+    mark(p, p->copy_after);
     p->next_id += 1;
     p->q_count[slot] += 1;
     if (record_id) *record_id = h.id;
@@ -995,7 +1049,7 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
     h.bound_pages = bound;
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
-    ap::k_scan_plan<<<1, ap::kPlanThreads, 0, st>>>(static_cast<int32_t *>(scratch), dispatch_blocks(T), E, capacity,
+    ap::launch(ap::k_scan_plan, 1, ap::kPlanThreads, 0, st, static_cast<int32_t *>(scratch), dispatch_blocks(T), E, capacity,
                                                     padded, counts, live, seg_off, stt, rec, xd_rows,
                                                     p->cfg.page_tokens, p->cfg.max_pages_per_record,
                                                     p->cfg.num_pages, p->cfg.spill_pages);
@@ -1006,12 +1060,13 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
         const int grid = (int)(want < cap ? want : cap);
         const ap::PageSpace ps = page_space(p);
         const uint8_t *xs = static_cast<const uint8_t *>(x);
+        mark(p, p->copy_before);
         uint8_t *xo = static_cast<uint8_t *>(xd);
         const int32_t *blk = static_cast<const int32_t *>(scratch);
         if (fp8) {
             const uint16_t *xs16 = static_cast<const uint16_t *>(x);
 #define AP_LAUNCH_E4M3(NRV)                                                                                       \
-    ap::k_dispatch_stash_e4m3<NRV><<<grid, 256, 0, st>>>(                                                         \
+    ap::launch(ap::k_dispatch_stash_e4m3<NRV>, grid, 256, 0, st,                                                          \
         xs16, T, H, idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, xd_scale, stt, rec, ps,                  \
         p->cfg.page_tokens, page_off[1])
             if (H <= 256 * 4) AP_LAUNCH_E4M3(4);
@@ -1020,14 +1075,15 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
             else AP_LAUNCH_E4M3(16);
 #undef AP_LAUNCH_E4M3
         } else if ((al & 15) == 0)
-            ap::k_dispatch_stash_copy<int4><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, capacity, blk,
+            ap::launch(ap::k_dispatch_stash_copy<int4>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,
                                                                   seg_off, src_tok, xo, stt, rec, ps,
                                                                   p->cfg.page_tokens);
         else
-            ap::k_dispatch_stash_copy<int2><<<grid, 256, 0, st>>>(xs, T, rb[0], idx, dest, k, E, capacity, blk,
+            ap::launch(ap::k_dispatch_stash_copy<int2>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,
                                                                   seg_off, src_tok, xo, stt, rec, ps,
                                                                   p->cfg.page_tokens);
         AP_CHECK_LAUNCH("dispatch_stash copy launch");
+        mark(p, p->copy_after);
     }
     p->next_id += 1;
     p->q_count[slot] += 1;
@@ -1052,7 +1108,7 @@ extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, voi
     plane_fit(p, h.nplanes, h.rb, page_off);
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *st = reinterpret_cast<ap_pool_state *>(p->dev_meta);
-    ap::k_pop_plan<<<1, 32, 0, p->stream>>>(st, rec.hdr);
+    ap::launch(ap::k_pop_plan, 1, 32, 0, p->stream, st, rec.hdr);
     AP_CHECK_LAUNCH("stash pop plan launch");
     ap::Planes pl;
     for (int i = 0; i < 2; ++i) {
@@ -1064,9 +1120,11 @@ extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, voi
     int64_t grid = h.bound_pages * h.tiles_per_page;
     if (grid > p->max_ctas) grid = p->max_ctas;
     if (grid < 1) grid = 1;
-    ap::k_pop_copy<<<(unsigned)grid, ap::kCopyThreads, 0, p->stream>>>(st, rec, page_space(p), pl, dst_rows,
+    mark(p, p->copy_before);
+    ap::launch(ap::k_pop_copy, (unsigned)grid, ap::kCopyThreads, 0, p->stream, st, rec, page_space(p), pl, dst_rows,
                                                                        h.rows_per_tile, h.tiles_per_page);
     AP_CHECK_LAUNCH("stash pop copy launch");
+    mark(p, p->copy_after);
     if (record_id) *record_id = h.id;
     p->q_head[slot] = (p->q_head[slot] + 1) % p->cfg.max_records_per_slot;
     p->q_count[slot] -= 1;

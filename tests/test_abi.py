@@ -83,6 +83,12 @@ def test_arena_without_a_gpu_fails_cleanly(lib):
     assert lib.ap_arena_destroy(None) == 0
 
 
+def test_pool_calls_reject_a_null_pool(lib):
+    assert lib.ap_pool_time_copies(None, None, None) == -1
+    assert lib.ap_pool_grow(None, 8, None, None) == -1
+    assert lib.ap_pool_reset(None, None) == -1
+
+
 def test_route_rejects_bad_sizes(lib):
     p = ctypes.c_void_p(16)
     assert lib.ap_route_topk(p, 10, 0, 1, p, p, None) == -1       # E = 0

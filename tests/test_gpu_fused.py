@@ -186,3 +186,33 @@ def test_launch_counter_counts_enqueued_kernels():
         graph.replay()
     torch.cuda.synchronize()
     assert ap.launch_count() - n2 == 1
+
+
+def test_copy_kernel_timing_events():
+    """ap_pool_time_copies: the library records the caller's events around
+    the copy kernel; that span lies inside the whole call's span."""
+    T, H, E, k = 4096, 512, 16, 4
+    logits = torch.from_numpy(inputs.router_logits(9, T, E)).cuda()
+    x = bf16_to_dev(inputs.normal_bf16(9, inputs.X_STREAM, (T, H)))
+    g = ap.Pool(16, ap.page_bytes_for(16, (2 * H,)), T * k // 16 + E, 1, 2, E)
+    idx, _ = ap.route_topk(logits, k)
+    torch.cuda.synchronize()
+    spans = []
+    for call in ("dispatch_stash", "pop"):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g.time_copies(ca, cb)
+        with torch.cuda.stream(g.stream):
+            a.record(g.stream)
+            if call == "dispatch_stash":
+                d = g.dispatch_stash(0, x, idx, E)
+            else:
+                y = torch.empty_like(d["xd"])
+                g.pop(0, [y])
+            b.record(g.stream)
+        g.time_copies(None, None)
+        torch.cuda.synchronize()
+        spans.append((a.elapsed_time(b), ca.elapsed_time(cb), a.elapsed_time(ca), cb.elapsed_time(b)))
+    for whole, copy, lead, trail in spans:
+        assert 0 < copy <= whole and lead >= 0 and trail >= 0
+    assert torch.equal(y, d["xd"])
