@@ -11,6 +11,10 @@
 // allocation and recycling, device counts that change under CUDA-graph replay,
 // BF16/FP8 payloads, host spill and overflow.
 //
+// A fused dispatch + push (k_scan_plan, then k_dispatch_stash_copy or its
+// E4M3 form) plans the same way but leaves the page descriptors to the copy
+// kernel: the pair that holds row 0 of a page writes its descriptor with its
+// page-table entry.
 // A push is two launches on the paging stream:
 //   k_push_plan (1 CTA): snapshot live/seg_off, page ordinals by a prefix sum of
 //     ceil(live/P), one (first row, rows) descriptor per page, and the
@@ -290,7 +294,8 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
                                                const int32_t *__restrict__ d_seg_off,
                                                const int32_t *__restrict__ d_live, int64_t src_rows, int P,
                                                int64_t max_pages, int64_t N, int64_t SP, const StateSnap &snap,
-                                               bool have_reg = false, int32_t reg_off = 0, int32_t reg_live = 0)
+                                               bool write_desc, bool have_reg = false, int32_t reg_off = 0,
+                                               int32_t reg_live = 0)
 {
     __shared__ int64_t s_warp[kPlanThreads / kWarp];
     __shared__ int64_t s_carry;
@@ -360,7 +365,9 @@ __device__ __forceinline__ void push_plan_body(ap_pool_state *st, RecPtr rec, in
     const int64_t *pg_base = in_smem ? s_base : rec.pg_base;
     const int32_t *seg_live = in_smem ? s_live : rec.live;
     const int32_t *seg_offs = in_smem ? s_off : rec.seg_off;
-    for (int64_t ord = tid; ord < kept; ord += kPlanThreads) plan_descriptor(rec, pg_base, seg_live, seg_offs, nseg, ord, P);
+    if (write_desc) // (the fused copy writes them itself, beside the page-table entry)
+        for (int64_t ord = tid; ord < kept; ord += kPlanThreads)
+            plan_descriptor(rec, pg_base, seg_live, seg_offs, nseg, ord, P);
     // 3. allocation: device pages first, then spill pages, then lost
     if (tid == 0) plan_allocate(st, rec, nseg, total, max_pages, s_flags, snap, N, SP);
 }
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_push_plan(ap_pool_state *st, R
     pdl_begin();
     StateSnap snap;
     if (threadIdx.x == 0) snap = load_state(st);
-    push_plan_body(st, rec, nseg, d_seg_off, d_live, src_rows, P, max_pages, N, SP, snap);
+    push_plan_body(st, rec, nseg, d_seg_off, d_live, src_rows, P, max_pages, N, SP, snap, true);
 }
 
 // Fused dispatch + stash: the dispatch's expert scan and the record's page
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_scan_plan(int32_t *__restrict_
     int32_t my_live, my_off;
     scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off, my_live, my_off);
     __syncthreads();
-    push_plan_body(st, rec, E, seg_off, live, src_rows, P, max_pages, N, SP, snap, E <= kPlanThreads, my_off,
+    push_plan_body(st, rec, E, seg_off, live, src_rows, P, max_pages, N, SP, snap, false, E <= kPlanThreads, my_off,
                    my_live);
 }
 
@@ -521,14 +528,22 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
             my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
             const int e = idx[t * k + lane];
             if (my_d >= 0 && e >= 0 && e < E) {
-                const int64_t r = (int64_t)my_d - rec.seg_off[e]; // row within the expert segment
-                if (r >= 0 && r < rec.live[e]) {
+                const int64_t so = rec.seg_off[e], lv = rec.live[e];
+                const int64_t r = (int64_t)my_d - so; // row within the expert segment
+                if (r >= 0 && r < lv) {
                     const int64_t ord = rec.pg_base[e] + r / P;
                     if (ord < npages) {
                         bool corrupt;
                         const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
                         if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                        if (r % P == 0) rec.page_table[ord] = (int32_t)id; // row 0 of the page records it
+                        if (r % P == 0) { // row 0 of the page records it and its descriptor
+                            rec.page_table[ord] = (int32_t)id;
+                            PageDesc pd;
+                            pd.row0 = so + r;
+                            pd.nrows = (int32_t)(lv - r < P ? lv - r : P);
+                            pd.pad = 0;
+                            rec.desc[ord] = pd;
+                        }
                         if (id >= 0) {
                             uint8_t *page = page_addr(ps, id);
                             my_page = page + (r % P) * rb;
@@ -593,14 +608,22 @@ __global__ void __launch_bounds__(256, 3) k_dispatch_stash_e4m3(
             my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
             const int e = idx[t * k + lane];
             if (my_d >= 0 && e >= 0 && e < E) {
-                const int64_t r = (int64_t)my_d - rec.seg_off[e];
-                if (r >= 0 && r < rec.live[e]) {
+                const int64_t so = rec.seg_off[e], lv = rec.live[e];
+                const int64_t r = (int64_t)my_d - so;
+                if (r >= 0 && r < lv) {
                     const int64_t ord = rec.pg_base[e] + r / P;
                     if (ord < npages) {
                         bool corrupt;
                         const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
                         if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                        if (r % P == 0) rec.page_table[ord] = (int32_t)id; // row 0 of the page records it
+                        if (r % P == 0) { // row 0 of the page records it and its descriptor
+                            rec.page_table[ord] = (int32_t)id;
+                            PageDesc pd;
+                            pd.row0 = so + r;
+                            pd.nrows = (int32_t)(lv - r < P ? lv - r : P);
+                            pd.pad = 0;
+                            rec.desc[ord] = pd;
+                        }
                         if (id >= 0) {
                             uint8_t *page = page_addr(ps, id);
                             my_row = page + (r % P) * H;

@@ -63,6 +63,9 @@ def parse_args(argv=None):
                     help="qwen3_moe (default) is the benchmark; the others time that workload's stash schedule")
     ap.add_argument("--overlap", action="store_true",
                     help="also measure reload (pop) overlapped with a bf16 GEMM on another stream")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="also size the pool by calibration (no device pages, live prefixes parked in pinned "
+                         "spill pages), grow it to the measured demand and time the step on it")
     return ap.parse_args(argv)
 
 
@@ -347,6 +350,63 @@ class Step:
         h2d = sum(h["logits"].nbytes + h["x"].nbytes + h["y"].nbytes for h, _ in self.chunks)
         d2h = sum(h["out"].nbytes for h, _ in self.chunks)
         return h2d, d2h
+
+
+def calibration_report(step, device, steps=100):
+    """Lazy pool sizing on the benchmark step.  One step runs on a pool with
+    no device pages: every record parks its live prefixes in pinned spill
+    pages and the pool counts the pages its queued records hold.  The pool
+    then grows in place to the most pages held, is reset, and the step (as a
+    CUDA graph) is timed on it.  The other pool of the step is put back after."""
+    import torch
+    ap, wl = step.ap, step.wl
+    per_record = wl.T * wl.k // wl.page_tokens + wl.E  # pages a record can need at most
+    spill = wl.chunks * per_record
+    cal = ap.Pool(wl.page_tokens, wl.page_bytes, 0, wl.num_slots, 4, wl.E, per_record, spill,
+                  device=device, stream=step.stream, max_num_pages=2 * wl.num_pages)
+    main_pool, step.pool = step.pool, cal
+    try:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record(step.stream)
+        step.run(fused=True)  # the calibration step: every page crosses the host link twice
+        b.record(step.stream)
+        torch.cuda.synchronize(device)
+        cal_ms = a.elapsed_time(b)
+        st = cal.state()
+        demand = cal.calibrated_pages()
+        cal.grow(demand)
+        cal.reset()
+        step.run(fused=True)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=step.stream):
+            step.run_concurrent()
+        for _ in range(3):
+            with torch.cuda.stream(step.stream):
+                g.replay()
+        torch.cuda.synchronize(device)
+        a.record(step.stream)
+        for _ in range(steps):
+            with torch.cuda.stream(step.stream):
+                g.replay()
+        b.record(step.stream)
+        torch.cuda.synchronize(device)
+        el = a.elapsed_time(b) / 1e3
+        after = cal.state()
+        del g
+        return {"demand_pages": demand, "configured_pages": wl.num_pages,
+                "pool_bytes": demand * wl.page_bytes, "configured_pool_bytes": wl.num_pages * wl.page_bytes,
+                "calibration_step_ms": round(cal_ms, 3), "calibration_spill_pages": st["spill_high_water"],
+                "calibration_device_pages": st["high_water"],
+                "value": round(wl.T * wl.chunks * steps / el, 1), "unit": "tokens/s",
+                "ms_per_step": round(el * 1e3 / steps, 5), "steps": steps,
+                "flags_after": after["flags"], "device_high_water_after": after["high_water"],
+                "note": "calibration step on a pool with no device pages (live prefixes parked in pinned spill "
+                        "pages), then the pool grown in place to the most pages held and the step timed on it"}
+    finally:
+        step.pool = main_pool
+        cal.close()
 
 
 def overlap_report(step, device, grid_bounds=(64, 152, 304, 608, 1216, 2048), reps=15):
@@ -811,6 +871,7 @@ def native(args):
                        "pipelined per chunk on separate copy streams"}
 
     overlap = overlap_report(step, device) if args.overlap else None
+    calibration = calibration_report(step, device) if args.calibrate and world == 1 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -834,6 +895,7 @@ def native(args):
                            "step": ("route, fused dispatch + push, pop, combine per chunk" if fused_main
                                     else "route, dispatch, push, pop, combine per chunk")},
                 "roofline": roofline, "ops": ops, "alt": alt, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
+                "calibration": calibration,
                 "gpu_launches": timed_launches,
                 "clocks": clocks}
         print(json.dumps(line), flush=True)
