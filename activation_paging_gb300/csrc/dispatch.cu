@@ -253,28 +253,23 @@ __global__ void __launch_bounds__(256) k_copy_rows_e4m3_reg(const uint16_t *__re
             const int s = lane + i * kWarp;
             v[i] = (s < nstep) ? ld_stream(row + s) : make_int4(0, 0, 0, 0);
         }
-        float amax = 0.f;
+        uint32_t m = 0;
 #pragma unroll
         for (int i = 0; i < NR; ++i) {
-            uint16_t e[8];
-            memcpy(e, &v[i], 16);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(e[q])));
+            m = absmax_bf16x2(m, (uint32_t)v[i].x);
+            m = absmax_bf16x2(m, (uint32_t)v[i].y);
+            m = absmax_bf16x2(m, (uint32_t)v[i].z);
+            m = absmax_bf16x2(m, (uint32_t)v[i].w);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
-        const float inv = (amax == 0.f) ? 1.f : __fdiv_rn(448.f, amax);
+        float scale, inv;
+        e4m3_scales(__reduce_max_sync(0xffffffffu, absmax_bits(m)), scale, inv);
         if (lane < k && my_d >= 0) xd_scale[my_d] = scale;
         // codes replace the values in place (8 code bytes in the vector's first half)
 #pragma unroll
         for (int i = 0; i < NR; ++i) {
-            uint16_t e[8];
-            memcpy(e, &v[i], 16);
-            uint8_t q[8];
-#pragma unroll
-            for (int z = 0; z < 8; ++z) q[z] = to_e4m3(__fmul_rn(bf16_bits_to_f32(e[z]), inv));
-            memcpy(&v[i], q, 8);
+            const int2 c = quantize8_e4m3(v[i], inv);
+            v[i].x = c.x;
+            v[i].y = c.y;
         }
         for (int j = 0; j < k; ++j) {
             const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
@@ -289,11 +284,21 @@ __global__ void __launch_bounds__(256) k_copy_rows_e4m3_reg(const uint16_t *__re
     }
 }
 
+// Pairs of values per conversion instruction, as the dispatch kernels convert.
 __global__ void k_cast_e4m3(const float *__restrict__ in, uint8_t *__restrict__ out, int64_t n)
 {
     pdl_begin();
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        out[i] = to_e4m3(in[i]);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; 2 * i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        if (2 * i + 1 < n) {
+            const uint16_t q = __nv_cvt_float2_to_fp8x2(make_float2(in[2 * i], in[2 * i + 1]), __NV_SATFINITE,
+                                                        __NV_E4M3);
+            out[2 * i] = (uint8_t)(q & 0xffu);
+            out[2 * i + 1] = (uint8_t)(q >> 8);
+        } else {
+            out[2 * i] = to_e4m3(in[2 * i]);
+        }
+    }
 }
 
 int64_t nblocks(int64_t T) { return (T + kTokPerBlk - 1) / kTokPerBlk; }

@@ -125,6 +125,49 @@ __device__ __forceinline__ uint8_t to_e4m3(float v)
     return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
 
+// Row amax of the E4M3 quantisation on packed BF16 (two values per 32-bit
+// word).  |x| clears the sign bits; NaN halves (above 0x7F80) become 0, so a
+// NaN never wins, as in a float max; the halves are then maxed as unsigned
+// 16-bit integers, whose order is the order of non-negative values.  Exactly
+// max |x| over the non-NaN values, two values per instruction.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m, uint32_t w)
+{
+    const uint32_t a = w & 0x7fff7fffu;
+    return __vmaxu2(m, a & ~__vcmpgtu2(a, 0x7f807f80u));
+}
+
+// The larger half of a packed absmax as the bits of a non-negative float
+// (unsigned order = value order, so a warp reduces it with one redux.sync).
+__device__ __forceinline__ uint32_t absmax_bits(uint32_t m)
+{
+    const uint32_t lo = m & 0xffffu, hi = m >> 16;
+    return (lo > hi ? lo : hi) << 16;
+}
+
+// E4M3 codes of the eight BF16 values of v times inv, in element order: each
+// product is rounded to float, then converted with round-to-nearest-even and
+// finite saturation, two values per conversion instruction.
+__device__ __forceinline__ int2 quantize8_e4m3(const int4 &v, float inv)
+{
+    const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __fmul_rn(__uint_as_float(w[i] << 16), inv);
+        const float hi = __fmul_rn(__uint_as_float(w[i] & 0xffff0000u), inv);
+        q[i] = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+    }
+    return make_int2((int)(q[0] | (q[1] << 16)), (int)(q[2] | (q[3] << 16)));
+}
+
+// Scale and inverse scale of a row from its amax bits (amax 0: both 1).
+__device__ __forceinline__ void e4m3_scales(uint32_t amax_bits, float &scale, float &inv)
+{
+    const float amax = __uint_as_float(amax_bits);
+    scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+    inv = (amax == 0.f) ? 1.f : __fdiv_rn(448.f, amax);
+}
+
 // Row of pair (t, j) from its in-block rank (left in dest by k_count_rank) and
 // the block bases (left in blk by the scan): rank = base[b][e] + in-block
 // rank; kept iff capacity <= 0 or rank < capacity.  Writes the final dest and,

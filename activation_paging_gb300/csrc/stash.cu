@@ -640,30 +640,25 @@ __global__ void __launch_bounds__(256, 3) k_dispatch_stash_e4m3(
             const int s = lane + i * kWarp;
             v[i] = (s < nstep) ? ld_stream(row + s) : make_int4(0, 0, 0, 0);
         }
-        float amax = 0.f;
+        uint32_t m = 0;
 #pragma unroll
         for (int i = 0; i < NR; ++i) {
-            uint16_t e8[8];
-            memcpy(e8, &v[i], 16);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(e8[q])));
+            m = absmax_bf16x2(m, (uint32_t)v[i].x);
+            m = absmax_bf16x2(m, (uint32_t)v[i].y);
+            m = absmax_bf16x2(m, (uint32_t)v[i].z);
+            m = absmax_bf16x2(m, (uint32_t)v[i].w);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
-        const float inv = (amax == 0.f) ? 1.f : __fdiv_rn(448.f, amax);
+        float scale, inv;
+        e4m3_scales(__reduce_max_sync(0xffffffffu, absmax_bits(m)), scale, inv);
         if (my_d >= 0) {
             xd_scale[my_d] = scale;
             if (my_scale) *my_scale = scale;
         }
 #pragma unroll
-        for (int i = 0; i < NR; ++i) { // codes replace the values in place
-            uint16_t e8[8];
-            memcpy(e8, &v[i], 16);
-            uint8_t q[8];
-#pragma unroll
-            for (int z = 0; z < 8; ++z) q[z] = to_e4m3(__fmul_rn(bf16_bits_to_f32(e8[z]), inv));
-            memcpy(&v[i], q, 8);
+        for (int i = 0; i < NR; ++i) { // codes replace the values in place (first 8 bytes)
+            const int2 c = quantize8_e4m3(v[i], inv);
+            v[i].x = c.x;
+            v[i].y = c.y;
         }
         for (int j = 0; j < k; ++j) {
             const int32_t d = __shfl_sync(0xffffffffu, my_d, j);

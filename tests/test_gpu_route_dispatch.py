@@ -103,6 +103,33 @@ def test_dispatch_e4m3_matches_oracle(T, H, E, k):
     assert np.array_equal(host(out["xd_scale"]).view(np.uint32), plan["xd_scale"].view(np.uint32))
 
 
+@pytest.mark.parametrize("H", [2048, 64, 20])  # register path (8 vectors per lane, a partial vector); generic path
+def test_dispatch_e4m3_special_values(H):
+    """Rows with NaN (either sign), infinities, -0, BF16 denormals, all
+    zeros and all NaN: the row amax ignores NaN, as the oracle's float max
+    does, and every code and scale matches the oracle bit for bit."""
+    T, E, k = 12, 4, 2
+    x = inputs.normal_bf16(H, inputs.X_STREAM, (T, H))
+    x[0, 5] = 0x7FC0                       # NaN
+    x[1, 3] = 0xFFC1                       # negative NaN, other payload
+    x[2, 7] = 0x7F80                       # +inf: amax inf, scale inf, codes of finite values 0
+    x[3, 1] = 0xFF80                       # -inf
+    x[4, :] = 0x8000                       # all -0: amax 0, scale 1
+    x[5, :] = 0x0001                       # all smallest denormals
+    x[6, :] = 0x7FC0                       # all NaN: amax 0
+    x[7, ::3] = 0x0003                     # denormals among normal values
+    x[8, :] = 0x0000
+    x[9, H - 1] = 0x4F80                   # a large value (2^32) at the end of the row
+    logits = inputs.router_logits(H, T, E)
+    idx, _ = oracle.route_topk(logits, k)
+    plan = oracle.dispatch(x, idx, E, 0, False, fp8=True, fill=0xA5)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = ap.dispatch_permute(bf16_to_dev(x), to_dev(idx), E, 0, False, fp8=True, status=status)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(out["xd"]), plan["xd"])
+    assert np.array_equal(host(out["xd_scale"]).view(np.uint32), plan["xd_scale"].view(np.uint32))
+
+
 def test_dispatch_full_size_skewed():
     wl = inputs.WORKLOADS["skewed"]
     plan, out, st = dispatch_both(wl.T, wl.H, wl.E, wl.k, wl.capacity, True, seed=0, zipf_s=wl.zipf_s,
