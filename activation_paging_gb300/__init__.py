@@ -380,10 +380,30 @@ class Pool:
         """Fused dispatch + push into ``slot`` (BF16 rows, or E4M3 codes and
         row scales as two planes): returns the dispatch dict (as
         ``dispatch_permute``) with the record id under ``record_id``."""
-        _need(x, torch.bfloat16, "x")
         _need(idx, torch.int32, "idx")
+        return self._dispatch_stash(slot, x, idx, idx.shape[1], E, capacity, padded, fp8, out, status)
+
+    def route_dispatch_stash(self, slot: int, logits: torch.Tensor, x: torch.Tensor, k: int, E: int | None = None,
+                             capacity: int = 0, padded: bool = False, fp8: bool = False, out: dict | None = None,
+                             status: torch.Tensor | None = None):
+        """Route (as ``route_topk``) and fused dispatch + push in one call:
+        the routing runs inside the count/rank launch.  Returns the dispatch
+        dict with ``idx``, ``w`` and ``record_id`` added (``out`` may supply
+        ``idx`` and ``w`` too)."""
+        _need(logits, torch.float32, "logits")
+        T, E_l = logits.shape
+        E = E_l if E is None else E
+        o = dict(out) if out is not None else {}
+        if "idx" not in o:
+            o["idx"] = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+        if "w" not in o:
+            o["w"] = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+        return self._dispatch_stash(slot, x, o["idx"], k, E, capacity, padded, fp8, o, status, logits=logits,
+                                    w=o["w"])
+
+    def _dispatch_stash(self, slot, x, idx, k, E, capacity, padded, fp8, out, status, logits=None, w=None):
+        _need(x, torch.bfloat16, "x")
         T, H = x.shape
-        k = idx.shape[1]
         dev = x.device
         rows = E * capacity if padded else T * k
         o = dict(out) if out is not None else {}
@@ -399,14 +419,18 @@ class Pool:
         sb = dispatch_scratch_bytes(T, k, E)
         if "scratch" not in o or o["scratch"].numel() < sb:
             o["scratch"] = torch.empty(sb, dtype=torch.uint8, device=dev)
-        self._order_after_caller([x, idx, status] + [v for v in o.values() if isinstance(v, torch.Tensor)])
+        self._order_after_caller([x, idx, status, logits] + [v for v in o.values() if isinstance(v, torch.Tensor)])
         rid = ctypes.c_uint64()
         xd = o["xd"]
-        check(self.lib.ap_dispatch_stash(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity, int(padded),
-                                         DTYPE_E4M3 if fp8 else DTYPE_BF16, _p(xd), _p(o.get("xd_scale") if fp8 else None),
-                                         xd.shape[0], _p(o["counts"]), _p(o["live"]), _p(o["seg_off"]),
-                                         _p(o["dest"]), _p(o["src_tok"]), _p(o["scratch"]), o["scratch"].numel(),
-                                         _p(status), ctypes.byref(rid), self.stream.cuda_stream), "dispatch_stash")
+        tail = (DTYPE_E4M3 if fp8 else DTYPE_BF16, _p(xd), _p(o.get("xd_scale") if fp8 else None), xd.shape[0],
+                _p(o["counts"]), _p(o["live"]), _p(o["seg_off"]), _p(o["dest"]), _p(o["src_tok"]), _p(o["scratch"]),
+                o["scratch"].numel(), _p(status), ctypes.byref(rid), self.stream.cuda_stream)
+        if logits is None:
+            check(self.lib.ap_dispatch_stash(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity, int(padded),
+                                             *tail), "dispatch_stash")
+        else:
+            check(self.lib.ap_route_dispatch_stash(self.handle, slot, _p(logits), _p(w), _p(x), T, H, _p(idx), k, E,
+                                                   capacity, int(padded), *tail), "route_dispatch_stash")
         o["record_id"] = rid.value
         return o
 

@@ -40,6 +40,11 @@ ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E,
 ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
                               uint32_t *d_status, cudaStream_t st);
 int dispatch_blocks(int64_t T);
+// Route (as ap_route_topk, into idx and w) and count/rank in one launch: the
+// same outputs as ap_route_topk followed by dispatch_count_rank.  Arguments
+// are checked by the caller.
+ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
+                                    void *scratch, int32_t *dest, cudaStream_t st);
 
 #define AP_CHECK_LAUNCH(what)                                   \
     do {                                                        \

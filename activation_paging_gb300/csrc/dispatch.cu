@@ -19,6 +19,7 @@
 #include <cuda_fp8.h>
 
 #include "dispatch_scan.cuh"
+#include "route_topk.cuh"
 
 namespace ap {
 namespace {
@@ -36,33 +37,31 @@ __global__ void __launch_bounds__(1024) k_scan(int32_t *__restrict__ blk, int nb
     scan_body(blk, nblk, E, capacity, padded, counts, live, seg_off, my_live, my_off);
 }
 
-// Block histograms and stable in-block ranks, in one pass over idx.  The
-// block's pairs are split into kRankWarps contiguous ranges; each warp counts
-// its range, a per-expert scan over warps gives each warp's base inside the
-// block (the block's totals go to blk[b][e]), then each warp walks its range
-// 32 pairs at a time in order (match_any + popc).  dest[p] temporarily holds
-// the pair's rank inside its block (-1 for an invalid id); the copy kernels
-// add the block's base from the scan and write the final row.
-__global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
-                                                             int32_t *__restrict__ blk, int32_t *__restrict__ dest,
-                                                             uint32_t *d_status)
+// Block histogram and stable in-block ranks of the pairs [p0, p1) of one
+// count/rank block (pair p = t*k + j), read from pidx[p - p0] (global or
+// shared memory) by W warps.  The pairs are split into W contiguous ranges;
+// each warp counts its range into cnt[w][e] (shared), a per-expert scan over
+// warps gives each warp's base inside the block (the block totals go to
+// blk_row[e]), then each warp walks its range 32 pairs at a time in order
+// (match_any + popc).  dest[p] temporarily holds the pair's rank inside its
+// block (-1 for an invalid id); the copy kernels add the block's base from the
+// scan and write the final row.  The ranks do not depend on W.  Returns true
+// if an id was out of range.
+template <int W>
+__device__ __forceinline__ bool block_count_rank(const int32_t *pidx, int64_t p0, int64_t p1, int E, int32_t *cnt,
+                                                 int32_t *__restrict__ blk_row, int32_t *__restrict__ dest)
 {
-    pdl_begin();
-    extern __shared__ int32_t cnt[]; // [kRankWarps][E]
     const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
-    for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
+    for (int i = threadIdx.x; i < W * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
-    const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
-    int64_t p1 = p0 + (int64_t)kTokPerBlk * k;
-    if (p1 > T * k) p1 = T * k;
-    const int64_t per_warp = ((p1 - p0) + kRankWarps - 1) / kRankWarps;
+    const int64_t per_warp = ((p1 - p0) + W - 1) / W;
     const int64_t w0 = p0 + wid * per_warp;
     const int64_t w1 = (w0 + per_warp < p1) ? w0 + per_warp : p1;
     int32_t *my = cnt + wid * E;
     bool bad = false;
     // phase 1: count per warp
     for (int64_t p = w0 + lane; p < w1; p += kWarp) {
-        const int e = idx[p];
+        const int e = pidx[p - p0];
         if (e >= 0 && e < E) atomicAdd(&my[e], 1);
         else bad = true;
     }
@@ -71,19 +70,19 @@ __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__re
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int32_t run = 0;
 #pragma unroll
-        for (int w2 = 0; w2 < kRankWarps; ++w2) {
+        for (int w2 = 0; w2 < W; ++w2) {
             const int32_t c = cnt[w2 * E + e];
             cnt[w2 * E + e] = run;
             run += c;
         }
-        blk[(int64_t)blockIdx.x * E + e] = run;
+        blk_row[e] = run;
     }
     __syncthreads();
     // phase 3: ordered walk, 32 pairs per step
     for (int64_t pb = w0; pb < w1; pb += kWarp) {
         const int64_t p = pb + lane;
         const bool in = p < w1;
-        int e = in ? idx[p] : -1;
+        int e = in ? pidx[p - p0] : -1;
         const bool valid = in && e >= 0 && e < E;
         if (!valid) e = -1 - (int)(in ? 0 : 1); // -1: bad id, -2: past the end
         const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -93,7 +92,55 @@ __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__re
         if (valid && (peers & lanemask_lt()) == 0) my[e] += __popc(peers);
         __syncwarp();
     }
+    return bad;
+}
+
+// Count/rank blocks of kTokPerBlk tokens reading idx from global memory.
+__global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
+                                                             int32_t *__restrict__ blk, int32_t *__restrict__ dest,
+                                                             uint32_t *d_status)
+{
+    pdl_begin();
+    extern __shared__ int32_t cnt[]; // [kRankWarps][E]
+    const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
+    const int64_t p1 = (p0 + (int64_t)kTokPerBlk * k < T * k) ? p0 + (int64_t)kTokPerBlk * k : T * k;
+    const bool bad = block_count_rank<kRankWarps>(idx + p0, p0, p1, E, cnt, blk + (int64_t)blockIdx.x * E, dest);
     if (bad && d_status) atomicOr(d_status, AP_FLAG_BAD_INDEX);
+}
+
+// Route + count/rank: one block of 32 warps routes its kTokPerBlk tokens
+// (route_topk.cuh; warp w takes tokens w and w + 32), writes idx and w, keeps
+// the block's ids in shared memory and ranks them there (block_count_rank), so
+// the ids are never read back from global memory.  Same idx, w, block counts
+// and ranks as k_route_topk followed by k_count_rank.
+constexpr int kRouteRankWarps = 32;
+
+template <int NV>
+__global__ void __launch_bounds__(kRouteRankWarps * kWarp) k_route_count_rank(
+    const float *__restrict__ logits, int64_t T, int E, int k, int32_t *__restrict__ idx, float *__restrict__ w,
+    int32_t *__restrict__ blk, int32_t *__restrict__ dest)
+{
+    pdl_begin();
+    extern __shared__ int32_t smem[]; // cnt [32][E], then the block's ids [kTokPerBlk * k]
+    int32_t *cnt = smem;
+    int32_t *sidx = smem + kRouteRankWarps * E;
+    const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
+    const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
+    const int ntok = (int)((T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
+    for (int tt = wid; tt < ntok; tt += kRouteRankWarps) {
+        int e;
+        float wt;
+        route_token<NV>(logits + (t0 + tt) * E, E, k, lane, &e, &wt);
+        if (lane < k) {
+            const int64_t p = (t0 + tt) * k + lane;
+            idx[p] = e;
+            w[p] = wt;
+            sidx[tt * k + lane] = e;
+        }
+    }
+    // block_count_rank starts with a barrier after clearing cnt: sidx is complete by then
+    (void)block_count_rank<kRouteRankWarps>(sidx, t0 * k, (t0 + ntok) * k, E, cnt, blk + (int64_t)blockIdx.x * E,
+                                            dest); // routed ids are always in range
 }
 
 // ---- BF16 row copy: one warp per token, row read once, written k times ------
@@ -389,6 +436,38 @@ ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t 
 }
 
 int dispatch_blocks(int64_t T) { return (int)nblocks(T); }
+
+template <int NV>
+ap_status launch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
+                                  int32_t *blk, int32_t *dest, cudaStream_t st)
+{
+    const size_t smem = ((size_t)kRouteRankWarps * E + (size_t)kTokPerBlk * k) * sizeof(int32_t);
+    static const cudaError_t attr = cudaFuncSetAttribute((const void *)k_route_count_rank<NV>,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         (int)((kRouteRankWarps * 1024 + kTokPerBlk * 32) *
+                                                               sizeof(int32_t)));
+    if (attr != cudaSuccess) return cuda_fail(attr, "route + count/rank: shared memory limit");
+    launch(k_route_count_rank<NV>, (unsigned)nblocks(T), kRouteRankWarps * kWarp, smem, st, logits, T, E, k, idx, w,
+           blk, dest);
+    AP_CHECK_LAUNCH("route + count/rank launch");
+    return AP_OK;
+}
+
+ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
+                                    void *scratch, int32_t *dest, cudaStream_t st)
+{
+    if (nblocks(T) == 0) return AP_OK;
+    int32_t *blk = static_cast<int32_t *>(scratch);
+    if (E <= 32) return launch_route_count_rank<1>(logits, T, E, k, idx, w, blk, dest, st);
+    if (E <= 64) return launch_route_count_rank<2>(logits, T, E, k, idx, w, blk, dest, st);
+    if (E <= 128) return launch_route_count_rank<4>(logits, T, E, k, idx, w, blk, dest, st);
+    if (E <= 256) return launch_route_count_rank<8>(logits, T, E, k, idx, w, blk, dest, st);
+    // more than 8 candidates per lane do not fit a 1024-thread block's
+    // registers: route and count/rank as two launches
+    ap_status s = ap_route_topk(logits, T, E, k, idx, w, st);
+    if (s != AP_OK) return s;
+    return dispatch_count_rank(T, idx, k, E, scratch, dest, nullptr, st);
+}
 
 ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
                             int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, void *scratch,

@@ -1010,12 +1010,15 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
     return AP_OK;
 }
 
-extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, int64_t T, int32_t H,
-                                       const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
-                                       int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows,
-                                       int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest,
-                                       int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
-                                       uint64_t *record_id, void *stream)
+namespace {
+
+// Fused dispatch + push; with logits != NULL the routing (into idx and w) is
+// done by the count/rank launch itself.
+ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, float *w, const void *x, int64_t T,
+                              int32_t H, int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
+                              int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows, int32_t *counts,
+                              int32_t *live, int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
+                              int64_t scratch_bytes, uint32_t *d_status, uint64_t *record_id, void *stream)
 {
     using namespace ap;
     if (!p) return fail(AP_EINVAL, "dispatch_stash: NULL pool");
@@ -1044,8 +1047,11 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
         return fail(AP_ENOTSUP, "dispatch_stash: rows must be 8-byte aligned (H %% 4 == 0)");
     if (fp8 && T > 0 && (H % 8 != 0 || H > 256 * 16 || (reinterpret_cast<uintptr_t>(x) & 15) != 0 || (al & 7) != 0))
         return fail(AP_ENOTSUP, "dispatch_stash: E4M3 needs H %% 8 == 0, H <= 4096 and aligned buffers");
+    if (logits && k > E) return fail(AP_EINVAL, "route_dispatch_stash: k=%d > E=%d", k, E);
+    if (logits && T > 0 && !w) return fail(AP_EINVAL, "route_dispatch_stash: NULL weights");
     cudaStream_t st = p->stream;
-    s = dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
+    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st)
+               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
     if (s != AP_OK) return s;
 
     const int32_t pos = (p->q_head[slot] + p->q_count[slot]) % p->cfg.max_records_per_slot;
@@ -1107,6 +1113,35 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
     p->q_count[slot] += 1;
     if (record_id) *record_id = h.id;
     return AP_OK;
+}
+
+} // namespace
+
+extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, int64_t T, int32_t H,
+                                       const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
+                                       int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows,
+                                       int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest,
+                                       int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
+                                       uint64_t *record_id, void *stream)
+{
+    return dispatch_stash_impl(p, slot, nullptr, nullptr, x, T, H, const_cast<int32_t *>(idx), k, E, capacity,
+                               padded, out_dtype, xd, xd_scale, xd_rows, counts, live, seg_off, dest, src_tok,
+                               scratch, scratch_bytes, d_status, record_id, stream);
+}
+
+extern "C" ap_status ap_route_dispatch_stash(ap_pool *p, int32_t slot, const float *logits, float *w, const void *x,
+                                             int64_t T, int32_t H, int32_t *idx, int32_t k, int32_t E,
+                                             int32_t capacity, int32_t padded, int32_t out_dtype, void *xd,
+                                             float *xd_scale, int64_t xd_rows, int32_t *counts, int32_t *live,
+                                             int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
+                                             int64_t scratch_bytes, uint32_t *d_status, uint64_t *record_id,
+                                             void *stream)
+{
+    if (T > 0 && !logits) return ap::fail(AP_EINVAL, "route_dispatch_stash: NULL logits");
+    static const float kNoLogits = 0.f; // T == 0: nothing to route, still the routing variant
+    return dispatch_stash_impl(p, slot, logits ? logits : &kNoLogits, w, x, T, H, idx, k, E, capacity, padded,
+                               out_dtype, xd, xd_scale, xd_rows, counts, live, seg_off, dest, src_tok, scratch,
+                               scratch_bytes, d_status, record_id, stream);
 }
 
 extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, void *const *dst_planes,

@@ -165,6 +165,8 @@ def op_bytes(wl, R):
         "combine": R * H * 2 + T * H * 2 + T * k * 8,
         # fused dispatch + push: x read once, dispatch rows and page rows written
         "dispatch_stash": T * H * 2 + 2 * R * rb + T * k * 8 + R * 4,
+        # route + fused dispatch + push in one call
+        "route_dispatch_stash": T * E * 4 + T * k * 8 + T * H * 2 + 2 * R * rb + T * k * 8 + R * 4,
     }
 
 
@@ -216,7 +218,7 @@ class Step:
                 return
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
-            pool_call = name in ("dispatch_stash", "push", "pop")
+            pool_call = name in COPY_KERNEL
             if pool_call:  # also time the call's copy kernel alone
                 ca = torch.cuda.Event(enable_timing=True)
                 cb = torch.cuda.Event(enable_timing=True)
@@ -230,7 +232,11 @@ class Step:
                 events.setdefault(name + ":copy", []).append((ca, cb))
 
         with torch.cuda.stream(s):
-            for h, d in self.chunks:
+            for c, (h, d) in enumerate(self.chunks):
+                if fused and c == 0:  # as in the captured step: chunk 0 routes inside its dispatch + push
+                    rec("route_dispatch_stash", lambda: self.pool.route_dispatch_stash(
+                        0, d["logits"], d["x"], wl.k, wl.E, out=dict(d["disp"], idx=d["idx"], w=d["w"])))
+                    continue
                 rec("route", lambda: ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=s))
                 if fused:
                     rec("dispatch_stash", lambda: self.pool.dispatch_stash(0, d["x"], d["idx"], wl.E, out=d["disp"]))
@@ -245,9 +251,10 @@ class Step:
 
     def run_concurrent(self):
         """The fused step with its independent work forked to a second stream:
-        chunk 1's routing runs beside chunk 0's dispatch + push, and chunk 0's
-        combine beside chunk 1's pop.  Every pool call stays on the paging
-        stream.  Used for the captured graph (fork and join become graph edges)."""
+        chunk 1's routing runs beside chunk 0's route + dispatch + push (one
+        call), and chunk 0's combine beside chunk 1's pop.  Every pool call
+        stays on the paging stream.  Used for the captured graph (fork and
+        join become graph edges)."""
         torch, ap, wl, s = self.torch, self.ap, self.wl, self.stream
         side = self.side
         (h0, d0), (h1, d1) = self.chunks[0], self.chunks[1]
@@ -259,8 +266,10 @@ class Step:
                 ap.route_topk(d1["logits"], wl.k, d1["idx"], d1["w"], stream=side)
                 r1 = torch.cuda.Event()
                 r1.record(side)
-            ap.route_topk(d0["logits"], wl.k, d0["idx"], d0["w"], stream=s)
-            self.pool.dispatch_stash(0, d0["x"], d0["idx"], wl.E, out=d0["disp"])
+            # chunk 0: routing inside its dispatch + push (one launch fewer on
+            # the paging stream); chunk 1 was routed on the side stream
+            self.pool.route_dispatch_stash(0, d0["logits"], d0["x"], wl.k, wl.E,
+                                           out=dict(d0["disp"], idx=d0["idx"], w=d0["w"]))
             s.wait_event(r1)
             self.pool.dispatch_stash(0, d1["x"], d1["idx"], wl.E, out=d1["disp"])
             self.pool.pop(0, [d0["dst"]])
@@ -552,6 +561,7 @@ class ScheduleStep:
                       "dispatch": T * H * 2 + plane_bytes + T * k * 8 + R * 4,
                       "push": 2 * plane_bytes,
                       "dispatch_stash": T * H * 2 + 2 * plane_bytes + T * k * 8 + R * 4,
+                      "route_dispatch_stash": T * E * 4 + T * k * 8 + T * H * 2 + 2 * plane_bytes + T * k * 8 + R * 4,
                       "pop": 2 * plane_bytes,
                       "combine": R * H * 2 + T * H * 2 + T * k * 8}
         self.tokens = T * sum(1 for op, _ in sched if op == "push")
@@ -591,7 +601,7 @@ class ScheduleStep:
                 return
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
-            pool_call = name in ("dispatch_stash", "push", "pop")
+            pool_call = name in COPY_KERNEL
             if pool_call:  # also time the call's copy kernel alone
                 ca = torch.cuda.Event(enable_timing=True)
                 cb = torch.cuda.Event(enable_timing=True)
@@ -608,6 +618,9 @@ class ScheduleStep:
             for op, name in self.sched:
                 d = self.src[name]
                 if op == "push":
+                    # route, then the fused dispatch + push: for these records the one-call
+                    # route + dispatch + push measured slower (its 64-token blocks of 32
+                    # routing warps cover fewer SMs than the router's own grid)
                     rec("route", lambda: ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=s))
                     rec("dispatch_stash", lambda: self.pool.dispatch_stash(d["slot"], d["x"], d["idx"], wl.E,
                                                                            wl.capacity, wl.padded, fp8=wl.fp8,
@@ -686,10 +699,17 @@ def kernel_hash() -> str:
     return hashlib.sha256(dev.encode()).hexdigest()[:16]
 
 
+# the pool calls whose copy kernel the library times, and the kernel each runs
+COPY_KERNEL = {"dispatch_stash": "k_dispatch_stash_copy", "route_dispatch_stash": "k_dispatch_stash_copy",
+               "push": "k_push_copy", "pop": "k_pop_copy"}
+
+
 def ops_table(events, op_bytes_of, peak):
     """Per-call rates from event pairs: for each call its mean event time and
     algorithmic GB/s; for pool calls also their copy kernel alone (events the
-    library recorded around it), under copy_ms / copy_gbs / copy_frac."""
+    library recorded around it), under copy_ms / copy_gbs / copy_frac, over
+    the bytes that kernel moves (a routing call's copy moves the dispatch +
+    push bytes, not the router's)."""
     ops = {}
     for name, pairs in events.items():
         if name.endswith(":copy"):
@@ -701,7 +721,8 @@ def ops_table(events, op_bytes_of, peak):
         if name + ":copy" in events:
             cp = events[name + ":copy"]
             cms = sum(a.elapsed_time(b) for a, b in cp) / len(cp)
-            cgbs = op_bytes_of[name] / (cms / 1e3) / 1e9
+            kbytes = op_bytes_of["dispatch_stash" if name == "route_dispatch_stash" else name]
+            cgbs = kbytes / (cms / 1e3) / 1e9
             ops[name].update(copy_ms=round(cms, 5), copy_gbs=round(cgbs, 1), copy_frac=round(cgbs / peak, 4))
     return ops
 
@@ -812,7 +833,7 @@ def native(args):
 
     step_ops = (("route", "dispatch_stash", "pop", "combine") if fused_main
                 else ("route", "dispatch", "push", "pop", "combine"))
-    total_bytes = sum(step.bytes[o] for o in step_ops) * wl.chunks
+    total_bytes = sum(step.bytes[o] for o in step_ops) * wl.chunks  # however the calls split the step
     ms_per_step = max_elapsed * 1e3 / args.steps
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
@@ -822,19 +843,19 @@ def native(args):
     # small plan kernels are timed with the call, not with the kernel)
     dom = max(ops, key=lambda n: ops[n]["ms"])
     timed = "copy_ms" in ops[dom]
-    kernel = {"dispatch_stash": "k_dispatch_stash_copy", "push": "k_push_copy", "pop": "k_pop_copy",
-              "dispatch": "k_copy_rows", "combine": "k_combine", "route": "k_route_topk"}[dom]
+    kernel = dict(COPY_KERNEL, dispatch="k_copy_rows", combine="k_combine", route="k_route_topk")[dom]
+    kcall = "dispatch_stash" if dom == "route_dispatch_stash" else dom  # the kernel's own bytes and traffic
     traffic = None
     try:
         tr = json.load(open(PROFILE_TRAFFIC))
-        if tr.get("kernel_hash") == kernel_hash() and dom in tr.get("per_launch_bytes", {}):
-            traffic = tr["per_launch_bytes"][dom]
+        if tr.get("kernel_hash") == kernel_hash() and kcall in tr.get("per_launch_bytes", {}):
+            traffic = tr["per_launch_bytes"][kcall]
     except Exception:
         pass
     roofline = {"bound": "hbm", "kernel": kernel, "call": dom,
                 "achieved": ops[dom]["copy_gbs" if timed else "gbs"], "peak": peak, "unit": "GB/s",
                 "frac": ops[dom]["copy_frac" if timed else "frac"], "traffic": traffic, "peak_source": peak_src,
-                "bytes_per_launch": ops[dom]["bytes"],
+                "bytes_per_launch": step.bytes[kcall],
                 "note": (f"achieved = the call's algorithmic bytes / mean CUDA-event time of its copy kernel, events "
                          f"recorded by the library on the paging stream around the kernel, over {op_steps} eager "
                          f"steps; the whole call (with its plan kernels) is under ops")}

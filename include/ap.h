@@ -389,6 +389,23 @@ ap_status ap_dispatch_stash(ap_pool *pool, int32_t slot, const void *x,
                             int64_t scratch_bytes, uint32_t *d_status,
                             uint64_t *record_id, void *stream);
 
+/* Route + fused dispatch + push: ap_route_topk(logits, T, E, k, idx, w)
+ * followed by ap_dispatch_stash(pool, slot, x, T, H, idx, k, E, ...), with the
+ * same results (idx, w, every dispatch output, the record, pool bytes and
+ * flags), but the routing runs inside the count/rank launch: each block of
+ * 64 tokens routes them (one warp per token) and ranks their pairs from
+ * shared memory, so the ids are not read back and one launch is saved (for
+ * E <= 256; wider routers take the two launches).  logits: device f32 [T, E];
+ * idx (int32) and w (f32): device outputs [T, k].  Other arguments, streams
+ * and errors as ap_dispatch_stash, plus AP_EINVAL for k > E or NULL
+ * logits / w with T > 0. */
+ap_status ap_route_dispatch_stash(ap_pool *pool, int32_t slot, const float *logits, float *w, const void *x,
+                                  int64_t T, int32_t H, int32_t *idx, int32_t k, int32_t E, int32_t capacity,
+                                  int32_t padded, int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows,
+                                  int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest,
+                                  int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
+                                  uint64_t *record_id, void *stream);
+
 /* Pop the oldest record of `slot` into dst_planes (host array of nplanes
  * device pointers, each [dst_rows, row_bytes of the push]).  A page whose
  * rows fall outside dst_rows is not copied (AP_FLAG_BAD_COUNT) but still
