@@ -17,7 +17,10 @@ pytestmark = pytest.mark.gpu
 ap = pytest.importorskip("activation_paging_gb300")
 
 
-def test_graph_replay_with_changing_routing():
+@pytest.mark.parametrize("mode", ["separate", "fused", "route_fused"])
+def test_graph_replay_with_changing_routing(mode):
+    """mode: route, dispatch and push as three calls; route then the fused
+    dispatch + push; or route, dispatch and push as one call."""
     T, H, E, k, P, chunks = 1024, 256, 32, 4, 16, 2
     rb = H * 2
     rows = T * k
@@ -55,9 +58,16 @@ def test_graph_replay_with_changing_routing():
 
     def step():
         for b in bufs:
+            if mode == "route_fused":
+                b["disp"] = pool.route_dispatch_stash(0, b["logits"], b["x"], k, E,
+                                                      out=dict(b["disp"], idx=b["idx"], w=b["w"]))
+                continue
             ap.route_topk(b["logits"], k, b["idx"], b["w"], stream=s)
-            b["disp"] = ap.dispatch_permute(b["x"], b["idx"], E, out=b["disp"], stream=s)
-            pool.push(0, [b["disp"]["xd"]], b["disp"]["seg_off"], b["disp"]["live"])
+            if mode == "fused":
+                b["disp"] = pool.dispatch_stash(0, b["x"], b["idx"], E, out=b["disp"])
+            else:
+                b["disp"] = ap.dispatch_permute(b["x"], b["idx"], E, out=b["disp"], stream=s)
+                pool.push(0, [b["disp"]["xd"]], b["disp"]["seg_off"], b["disp"]["live"])
         for b in bufs:
             pool.pop(0, [b["dst"]])
             ap.combine_unpermute(b["y"], b["disp"]["dest"], b["w"], out=b["out"], stream=s)
