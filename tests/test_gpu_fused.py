@@ -216,3 +216,48 @@ def test_copy_kernel_timing_events():
     for whole, copy, lead, trail in spans:
         assert 0 < copy <= whole and lead >= 0 and trail >= 0
     assert torch.equal(y, d["xd"])
+
+
+@pytest.mark.parametrize("padded", [False, True])
+def test_fused_empty_record_matches_oracle(padded):
+    """No tokens: the record is still planned (no pages), like a push of
+    empty segments; then a normal record and both pops."""
+    E, H, P, C = 16, 64, 8, 4
+    rb = 2 * H
+    page_bytes = ap.page_bytes_for(P, (rb,))
+    g = ap.Pool(P, page_bytes, 40, 1, 4, E, 64, 0, fill=FILL)
+    o = oracle.Pool(P, page_bytes, 40, 1, 4, E, 64, 0, keep_bytes=True, fill=FILL)
+    x0 = torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    i0 = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(g.stream):
+        g.stream.wait_stream(torch.cuda.default_stream())
+        d = g.dispatch_stash(0, x0, i0, E, C if padded else 0, padded)
+    torch.cuda.synchronize()
+    plan = oracle.dispatch(np.zeros((0, H), np.uint16), np.zeros((0, 2), np.int32), E, C if padded else 0, padded)
+    rows = plan["rows"]
+    o.push(0, [np.zeros((rows, rb), np.uint8)], rows, plan["seg_off"], plan["live"])
+    for key in ("counts", "live", "seg_off"):
+        assert np.array_equal(host(d[key]), plan[key]), key
+    assert g.state() == o.state()
+    assert g.record(0)["npages"] == o.record(0)["npages"] == 0
+    T = 40
+    x = inputs.normal_bf16(5, inputs.X_STREAM, (T, H))
+    idx, _ = oracle.route_topk(inputs.router_logits(5, T, E), 2)
+    plan = oracle.dispatch(x, idx, E, 0, False)
+    o.push(0, [plan["xd"].view(np.uint8).reshape(plan["rows"], rb)], plan["rows"], plan["seg_off"], plan["live"])
+    with torch.cuda.stream(g.stream):
+        g.dispatch_stash(0, bf16_to_dev(x), to_dev(idx), E)
+    torch.cuda.synchronize()
+    assert g.state() == o.state()
+    for _ in range(2):
+        r = o.record(0)
+        n = int(max(r["row0"] + r["nrows"])) if r["npages"] else 0
+        dst_np = [np.full((max(n, 1), rb), 0x3C, np.uint8)]
+        dst = to_dev(dst_np[0])
+        torch.cuda.synchronize()
+        g.pop(0, [dst])
+        o.pop(0, dst_np, dst_np[0].shape[0])
+        torch.cuda.synchronize()
+        assert np.array_equal(host(dst), dst_np[0])
+    assert g.state() == o.state()
+    assert np.array_equal(host(g.pool), o.pool_bytes())
