@@ -430,7 +430,16 @@ def overlap_report(step, device, grid_bounds=(64, 152, 304, 608, 1216, 2048), re
     a = torch.randn((8192, 2304), device=device, dtype=torch.bfloat16, generator=g)
     b = torch.randn((2304, 8192), device=device, dtype=torch.bfloat16, generator=g)
     c = torch.empty((8192, 8192), device=device, dtype=torch.bfloat16)
+    scrub_buf = torch.ones(256 << 20, device=device, dtype=torch.float16)  # 512 MB, four times L2
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def scrub():
+        """Read a buffer larger than L2 (dirty lines are written back) and
+        wait, so every timed part starts from the same cache state and idle
+        streams."""
+        with torch.cuda.stream(compute):
+            scrub_buf.sum()
+        torch.cuda.synchronize(device)
 
     def gemm():
         with torch.cuda.stream(compute):
@@ -452,25 +461,29 @@ def overlap_report(step, device, grid_bounds=(64, 152, 304, 608, 1216, 2048), re
     out = {"gemm": "bf16 8192x2304 @ 2304x8192 on a normal-priority stream",
            "reload": f"{len(step.chunks)} pops of the step on the high-priority paging stream",
            "method": f"median of {reps} rounds; each round measures every grid bound in turn: the GEMM alone, "
-                     "the reloads alone, then both with the reloads launched first and waited on last",
+                     "the reloads alone, then both with the reloads launched first and waited on last; "
+                     "every timed part starts after an L2 scrub and with no other work in flight",
            "by_grid_bound": {}}
     samples = {gb: ([], [], []) for gb in grid_bounds}
     for _ in range(reps):
         for gb in grid_bounds:
             step.pool.max_ctas = gb
             t_gemm, t_pop, t_both = samples[gb]
+            scrub()
             s0, s1 = ev(), ev()
             s0.record(compute)
             gemm()
             s1.record(compute)
-            push_all()
             torch.cuda.synchronize(device)
+            push_all()
+            scrub()
             p0, p1 = ev(), ev()
             p0.record(paging)
             pop_all()
             p1.record(paging)
-            push_all()
             torch.cuda.synchronize(device)
+            push_all()
+            scrub()
             b0, done, b1 = ev(), ev(), ev()
             b0.record(compute)
             paging.wait_event(b0)
