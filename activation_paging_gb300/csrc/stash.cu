@@ -957,7 +957,7 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
         return fail(AP_EINVAL, "stash_push: nseg %d outside [0, %d]", nseg, p->cfg.max_segments);
     if (src_rows < 0) return fail(AP_EINVAL, "stash_push: src_rows < 0");
     int64_t rb[2] = {row_bytes[0], nplanes == 2 ? row_bytes[1] : 0};
-    int64_t page_off[2];
+    int64_t page_off[2] = {0, 0};
     if (!plane_fit(p, nplanes, rb, page_off))
         return fail(AP_EINVAL, "stash_push: %d plane(s) of the given row bytes do not fit a page", nplanes);
     for (int i = 0; i < nplanes; ++i)
@@ -1034,7 +1034,7 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     const bool fp8 = out_dtype == AP_DTYPE_E4M3;
     const int nplanes = fp8 ? 2 : 1;
     int64_t rb[2] = {fp8 ? (int64_t)H : (int64_t)H * 2, fp8 ? 4 : 0};
-    int64_t page_off[2];
+    int64_t page_off[2] = {0, 0};
     if (!plane_fit(p, nplanes, rb, page_off))
         return fail(AP_EINVAL, "dispatch_stash: the rows of H=%d do not fit a page", H);
     if (fp8 && T > 0 && !xd_scale) return fail(AP_EINVAL, "dispatch_stash: E4M3 needs xd_scale");
@@ -1157,7 +1157,7 @@ extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, voi
     if (!dst_planes || dst_rows < 0) return fail(AP_EINVAL, "stash_pop: bad destination");
     for (int i = 0; i < nplanes; ++i)
         if (!dst_planes[i]) return fail(AP_EINVAL, "stash_pop: NULL destination plane");
-    int64_t page_off[2];
+    int64_t page_off[2] = {0, 0};
     plane_fit(p, h.nplanes, h.rb, page_off);
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *st = reinterpret_cast<ap_pool_state *>(p->dev_meta);
