@@ -986,7 +986,7 @@ def cpu_baseline(wl, budget_s: float):
     return {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{reps} oracle passes of {T_sample} tokens per chunk x {wl.chunks} chunks "
                       f"(route, dispatch, byte-exact stash push/pop, combine), single-threaded C",
-            "seconds": round(secs, 2)}
+            "seconds": round(secs, 2), "host_cores": os.cpu_count()}
 
 
 def reference(args):
@@ -1018,7 +1018,7 @@ def reference(args):
             "config": {"workload": f"{WORKLOAD}: T=16384 (2 chunks x 8192), H=2048, E=128, top-8, dropless, "
                                    f"page=64 tokens", "sample_tokens_per_step": T_sample * wl.chunks},
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "kind": "oracle", "cores": 1,
-                             "sample": sample},
+                             "sample": sample, "host_cores": os.cpu_count()},
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
