@@ -63,6 +63,8 @@ def parse_args(argv=None):
                     help="qwen3_moe (default) is the benchmark; the others time that workload's stash schedule")
     ap.add_argument("--overlap", action="store_true",
                     help="also measure reload (pop) overlapped with a bf16 GEMM on another stream")
+    ap.add_argument("--backward", action="store_true",
+                    help="also time the backward pair (combine backward, dispatch backward) on the step's shapes")
     ap.add_argument("--calibrate", action="store_true",
                     help="also size the pool by calibration (no device pages, live prefixes parked in pinned "
                          "spill pages), grow it to the measured demand and time the step on it")
@@ -359,6 +361,49 @@ class Step:
         h2d = sum(h["logits"].nbytes + h["x"].nbytes + h["y"].nbytes for h, _ in self.chunks)
         d2h = sum(h["out"].nbytes for h, _ in self.chunks)
         return h2d, d2h
+
+
+def backward_report(step, device, reps=50):
+    """The backward pair on one chunk of the step: combine backward (dy rows
+    and dw from dout, y, dest, w) and dispatch backward (dx from the k row
+    gradients of each token), each timed with CUDA events on the paging
+    stream over `reps` calls, against their algorithmic bytes."""
+    import torch
+    ap, wl, s = step.ap, step.wl, step.stream
+    h, d = step.chunks[0]
+    T, H, k, R = wl.T, wl.H, wl.k, step.R
+    dout = d["out"]
+    dy = torch.zeros_like(d["y"])
+    dw = torch.empty((T, k), dtype=torch.float32, device=device)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    calls = {
+        # dout read once per token, y rows read for dw, dy rows written; dest, w in and dw out
+        "combine_backward": (lambda: ap.combine_backward(dout, d["y"], d["disp"]["dest"], d["w"], dy=dy, dw=dw,
+                                                         stream=s), T * H * 2 + 2 * R * H * 2 + T * k * 12),
+        # the k rows of every token read, dx written, dest in
+        "dispatch_backward": (lambda: ap.dispatch_backward(d["dst"], d["disp"]["dest"], dx=dx, stream=s),
+                              R * H * 2 + T * H * 2 + T * k * 4),
+    }
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
+    out = {}
+    with torch.cuda.stream(s):
+        for name, (fn, nbytes) in calls.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(device)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(reps):
+                fn()
+            b.record(s)
+            torch.cuda.synchronize(device)
+            ms = a.elapsed_time(b) / reps
+            gbs = nbytes / (ms / 1e3) / 1e9
+            out[name] = {"ms": round(ms, 5), "bytes": nbytes, "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    out["note"] = (f"one chunk of the step (T={T}, H={H}, k={k}, {R} rows), mean over {reps} back-to-back calls "
+                   f"on the paging stream")
+    return out
 
 
 def calibration_report(step, device, steps=100):
@@ -906,6 +951,7 @@ def native(args):
 
     overlap = overlap_report(step, device) if args.overlap else None
     calibration = calibration_report(step, device) if args.calibrate and world == 1 else None
+    backward = backward_report(step, device) if args.backward else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -929,7 +975,7 @@ def native(args):
                            "step": ("route, fused dispatch + push, pop, combine per chunk" if fused_main
                                     else "route, dispatch, push, pop, combine per chunk")},
                 "roofline": roofline, "ops": ops, "alt": alt, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
-                "calibration": calibration,
+                "calibration": calibration, "backward": backward,
                 "gpu_launches": timed_launches,
                 "clocks": clocks}
         print(json.dumps(line), flush=True)

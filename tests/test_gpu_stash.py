@@ -247,3 +247,32 @@ def test_many_segments_plan_in_global_memory():
     t.check(images=True)
     t.pop(0, [(rows, 16)])
     t.check(images=True)
+
+
+@pytest.mark.parametrize("P,rb,N,SP", [(1, (24,), 30, 6), (512, (8,), 4, 2), (3, (20, 4), 25, 5)])
+def test_page_size_extremes(P, rb, N, SP):
+    """One-row pages (the page table is the ring order, row by row), pages far
+    larger than any segment (every segment's tail page is mostly empty), and
+    an odd page size with two planes, through wrap-around and spill."""
+    rng = np.random.default_rng(P)
+    t = Twin(P, rb, N=N, S=2, R=4, segs=4, SP=SP)
+    held = {s: [] for s in range(2)}
+    for step in range(40):
+        s = int(rng.integers(0, 2))
+        if held[s] and (rng.random() < 0.5 or len(held[s]) == 4):
+            shapes = held[s].pop(0)
+            t.pop(s, shapes)
+        else:
+            nseg = int(rng.integers(1, 5))
+            cap = int(rng.integers(1, 9))
+            live = rng.integers(0, cap + 1, size=nseg).astype(np.int32)
+            seg_off = (np.arange(nseg) * cap).astype(np.int32)
+            rows = nseg * cap
+            planes = [rows_np(100 * step + i, rows, b) for i, b in enumerate(rb)]
+            t.push(s, planes, seg_off, live)
+            held[s].append([p.shape for p in planes])
+            if P == 1:
+                rec = t.o.record(s, len(held[s]) - 1)
+                assert int(rec["npages"]) == int(live.sum())  # one page per live row
+        t.check()
+    t.check(images=True)
