@@ -196,6 +196,128 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t *__restrict_
     }
 }
 
+// Combine backward for BF16 rows in 16-byte vectors, split by columns: each
+// block takes two tokens at a time and gives each token four warps; warp q of
+// a token owns column pieces q, q + 4, ... of U * 32 vectors (512 bytes of a
+// row for U = 1).  For every pair j (KB rows per batch, all loads of a batch
+// in flight before the first use) a warp writes its pieces of dy and sums its
+// part of the dot product (columns ascending within a lane, then a butterfly);
+// the four parts of dw[t, j] are added in warp order through shared memory,
+// so dw is deterministic.  More warps in flight per token than one warp per
+// token, with few registers per lane.  A sweep on GB300 over (U, KB) in
+// {1, 2, 4} x {2, 4, 8} chose U = 1, KB = 4 (0.93 of the copy rate at the
+// Qwen3-like chunk; one warp per token reached 0.44).
+constexpr int kBwdWarpsPerTok = 4;
+
+template <int U, int KB>
+__global__ void __launch_bounds__(256, 4) k_combine_bwd_pieces(const uint16_t *__restrict__ dout,
+                                                              const uint16_t *__restrict__ y, int64_t y_rows, int H,
+                                                              const int32_t *__restrict__ dest,
+                                                              const float *__restrict__ w, int64_t T, int k,
+                                                              uint16_t *__restrict__ dy, float *__restrict__ dw,
+                                                              uint32_t *d_status)
+{
+    pdl_begin();
+    using V = int4;
+    constexpr int kTokPerIter = 8 / kBwdWarpsPerTok; // tokens a 256-thread block takes at a time
+    __shared__ float s_part[kTokPerIter][kWarp][kBwdWarpsPerTok];
+    const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
+    const int tb = wid / kBwdWarpsPerTok, q = wid % kBwdWarpsPerTok;
+    const int nstep = H / 8;
+    const int pieces = (nstep + U * kWarp - 1) / (U * kWarp);
+    for (int64_t t0 = (int64_t)blockIdx.x * kTokPerIter; t0 < T; t0 += (int64_t)gridDim.x * kTokPerIter) {
+        const int64_t t = t0 + tb;
+        const bool tv = t < T; // warp-uniform
+        int32_t my_d = -1;
+        float my_w = 0.f;
+        if (tv && lane < k) {
+            my_d = dest[t * k + lane];
+            my_w = w[t * k + lane];
+            if (my_d >= y_rows) {
+                if (d_status && q == 0) atomicOr(d_status, AP_FLAG_BAD_INDEX);
+                my_d = -1;
+            }
+        }
+        const V *grow = reinterpret_cast<const V *>(dout + (tv ? t : 0) * H);
+        for (int j0 = 0; j0 < k; j0 += KB) {
+            int32_t d[KB];
+            float wj[KB];
+            float dot[KB];
+#pragma unroll
+            for (int jj = 0; jj < KB; ++jj) {
+                d[jj] = __shfl_sync(0xffffffffu, my_d, (j0 + jj) & (kWarp - 1));
+                wj[jj] = __shfl_sync(0xffffffffu, my_w, (j0 + jj) & (kWarp - 1));
+                if (j0 + jj >= k || !tv) d[jj] = -1;
+                dot[jj] = 0.f;
+            }
+            for (int pc = q; pc < pieces; pc += kBwdWarpsPerTok) {
+                const int s0 = pc * U * kWarp;
+                V yv[KB][U];
+#pragma unroll
+                for (int jj = 0; jj < KB; ++jj) {
+                    if (d[jj] < 0) continue;
+                    const V *yrow = reinterpret_cast<const V *>(y + (int64_t)d[jj] * H);
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int s = s0 + u * kWarp + lane;
+                        if (s < nstep) yv[jj][u] = ld_stream(yrow + s);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int s = s0 + u * kWarp + lane;
+                    if (s >= nstep) continue;
+                    float g[8];
+                    unpack<8>(grow[s], g);
+#pragma unroll
+                    for (int jj = 0; jj < KB; ++jj) {
+                        if (d[jj] < 0) continue;
+                        float yf[8], o[8];
+                        unpack<8>(yv[jj][u], yf);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o[i] = __fmul_rn(wj[jj], g[i]);
+                            dot[jj] = fmaf(g[i], yf[i], dot[jj]);
+                        }
+                        st_stream(reinterpret_cast<V *>(dy + (int64_t)d[jj] * H) + s, pack<8>(o));
+                    }
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < KB; ++jj) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) dot[jj] += __shfl_xor_sync(0xffffffffu, dot[jj], off);
+                if (lane == 0 && j0 + jj < k) s_part[tb][j0 + jj][q] = dot[jj];
+            }
+        }
+        __syncthreads();
+        // dw[t, j]: the four warps' parts in warp order (a dropped pair gives 0)
+        if (threadIdx.x < kTokPerIter * kWarp) {
+            const int tt = threadIdx.x / kWarp, j = threadIdx.x % kWarp;
+            const int64_t t2 = t0 + tt;
+            if (t2 < T && j < k) {
+                float sum = 0.f;
+#pragma unroll
+                for (int qq = 0; qq < kBwdWarpsPerTok; ++qq) sum += s_part[tt][j][qq];
+                const int32_t dd = dest[t2 * k + j];
+                dw[t2 * k + j] = (dd >= 0 && dd < y_rows) ? sum : 0.f;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int U, int KB>
+void launch_combine_bwd_pieces(const uint16_t *dout, const uint16_t *y, int64_t y_rows, int H, const int32_t *dest,
+                               const float *w, int64_t T, int k, uint16_t *dy, float *dw, uint32_t *d_status,
+                               cudaStream_t st)
+{
+    static const int resident = resident_grid((const void *)k_combine_bwd_pieces<U, KB>, 256);
+    const int64_t want = (T + 1) / 2;
+    launch(k_combine_bwd_pieces<U, KB>, (int)(want < resident ? want : resident), 256, 0, st, dout, y, y_rows, H,
+           dest, w, T, k, dy, dw, d_status);
+}
+
 template <int VE>
 void launch_combine_bwd(const uint16_t *dout, const uint16_t *y, int64_t y_rows, int H, const int32_t *dest,
                         const float *w, int64_t T, int k, uint16_t *dy, float *dw, uint32_t *d_status,
@@ -227,7 +349,7 @@ extern "C" ap_status ap_combine_backward(const void *dout, const void *y, int64_
     const uint16_t *yy = static_cast<const uint16_t *>(y);
     uint16_t *d = static_cast<uint16_t *>(dy);
     if (H % 8 == 0 && (al & 15) == 0)
-        launch_combine_bwd<8>(g, yy, y_rows, H, dest, w, T, k, d, dw, d_status, st);
+        launch_combine_bwd_pieces<1, 4>(g, yy, y_rows, H, dest, w, T, k, d, dw, d_status, st);
     else
         launch_combine_bwd<1>(g, yy, y_rows, H, dest, w, T, k, d, dw, d_status, st);
     AP_CHECK_LAUNCH("combine_backward launch");

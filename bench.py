@@ -363,11 +363,11 @@ class Step:
         return h2d, d2h
 
 
-def backward_report(step, device, reps=50):
+def backward_report(step, device, reps=30):
     """The backward pair on one chunk of the step: combine backward (dy rows
     and dw from dout, y, dest, w) and dispatch backward (dx from the k row
-    gradients of each token), each timed with CUDA events on the paging
-    stream over `reps` calls, against their algorithmic bytes."""
+    gradients of each token), each call timed alone with CUDA events on the
+    paging stream after an L2 scrub, against its algorithmic bytes."""
     import torch
     ap, wl, s = step.ap, step.wl, step.stream
     h, d = step.chunks[0]
@@ -386,23 +386,26 @@ def backward_report(step, device, reps=50):
     }
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
+    scrub_buf = torch.ones(256 << 20, device=device, dtype=torch.float16)  # 512 MB, four times L2
     out = {}
     with torch.cuda.stream(s):
         for name, (fn, nbytes) in calls.items():
             for _ in range(3):
                 fn()
-            torch.cuda.synchronize(device)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s)
+            times = []
             for _ in range(reps):
+                scrub_buf.sum()  # no input left in L2 from the call before
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
                 fn()
-            b.record(s)
-            torch.cuda.synchronize(device)
-            ms = a.elapsed_time(b) / reps
+                b.record(s)
+                torch.cuda.synchronize(device)
+                times.append(a.elapsed_time(b))
+            ms = sum(times) / len(times)
             gbs = nbytes / (ms / 1e3) / 1e9
             out[name] = {"ms": round(ms, 5), "bytes": nbytes, "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
-    out["note"] = (f"one chunk of the step (T={T}, H={H}, k={k}, {R} rows), mean over {reps} back-to-back calls "
-                   f"on the paging stream")
+    out["note"] = (f"one chunk of the step (T={T}, H={H}, k={k}, {R} rows), mean over {reps} calls, each after an "
+                   f"L2 scrub, on the paging stream")
     return out
 
 

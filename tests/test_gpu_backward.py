@@ -35,6 +35,7 @@ def dw_bound(dout, y, dest):
     (1000, 2048, 128, 8, 0, False),
     (777, 264, 32, 6, 100, True),    # drops, H % 256 != 0
     (300, 30, 8, 2, 0, False),       # scalar path
+    (200, 4104, 16, 4, 0, False),    # rows wider than a lane's register batch: the one-vector loop
 ])
 def test_combine_backward_matches_oracle(T, H, E, k, C, padded):
     idx, w = oracle.route_topk(inputs.router_logits(T, T, E), k)
