@@ -59,7 +59,7 @@ ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, i
 // the stream may start launching once every block of this one has started,
 // and its blocks then wait in their own pdl_begin() until this grid has
 // finished and its memory is visible.  The chains of small dependent kernels
-// (route, count/rank, scan + plan, copy, pop plan, pop copy, combine) thereby
+// (route, count/rank, scan + plan, copy, pop copy, combine) thereby
 // overlap each launch with the end of the kernel before it; no kernel touches
 // memory before its wait, so results do not change.  After a kernel launched
 // without the attribute, or an event, the wait returns at once.

@@ -25,8 +25,10 @@
 //     read from the ring at head0 + ordinal; tile 0 of the page writes the
 //     page-table entry; the tile's rows are copied as one contiguous range per
 //     plane.
-// A pop is k_pop_plan (1 thread: tail snapshot, tail advance) and k_pop_copy
-// (tile 0 of a page writes its id back into the ring at tail0 + ordinal).
+// A pop is one launch, k_pop_copy: its CTAs copy the pages' live rows back,
+// and CTA 0 alone returns the record's pages (its page table, in ordinal
+// order) to the rings at their tails and advances the tails: no other CTA
+// reads or writes the rings or the counters.
 // Nothing here waits on the device: there are no spin loops.
 #include <stdlib.h>
 #include <string.h>
@@ -42,8 +44,8 @@ struct RecHdr {
     int32_t nseg;
     int32_t pad0;
     int64_t npages, ndev, nspill, nlost;
-    uint64_t head0, spill_head0, tail0, spill_tail0;
-    int64_t pad1[7];
+    uint64_t head0, spill_head0;
+    int64_t pad1[9];
 };
 static_assert(sizeof(RecHdr) == 128, "record header layout");
 static_assert(sizeof(ap_pool_state) == 128, "state layout");
@@ -442,21 +444,11 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_push_copy(ap_pool_state *st
     }
 }
 
-__global__ void k_pop_plan(ap_pool_state *__restrict__ st, RecHdr *__restrict__ hdr)
-{
-    pdl_begin();
-    if (blockIdx.x == 0 && threadIdx.x == 0) { // every load first: one round trip
-        const uint64_t tail = st->tail, stail = st->spill_tail;
-        const int64_t held = st->held;
-        const int64_t ndev = hdr->ndev, nspill = hdr->nspill, npages = hdr->npages;
-        hdr->tail0 = tail;
-        hdr->spill_tail0 = stail;
-        st->tail = tail + (uint64_t)ndev;
-        st->spill_tail = stail + (uint64_t)nspill;
-        st->held = held - npages;
-    }
-}
-
+// Pop of the slot's oldest record: its pages' live rows go back to the same
+// rows of the destination planes.  CTA 0 also returns the pages to the rings
+// they came from, in ordinal order at the tails as this pop found them
+// (device pages, then spill pages; a lost or invalid entry returns nothing),
+// advances the tails and releases the record's pages.
 __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st, RecPtr rec, PageSpace ps,
                                                             Planes dst, int64_t dst_rows, int rows_per_tile,
                                                             int tiles_per_page)
@@ -464,7 +456,35 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
     pdl_begin();
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
-    const uint64_t tail0 = rec.hdr->tail0, stail0 = rec.hdr->spill_tail0;
+    if (blockIdx.x == 0) {
+        const uint64_t tail0 = st->tail, stail0 = st->spill_tail;
+        const int64_t held = st->held;
+        constexpr int B = 4; // page-table loads in flight per thread
+        for (int64_t o0 = threadIdx.x; o0 < npages; o0 += (int64_t)B * blockDim.x) {
+            int32_t id[B];
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                const int64_t ord = o0 + (int64_t)u * blockDim.x;
+                id[u] = ord < npages ? rec.page_table[ord] : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                const int64_t ord = o0 + (int64_t)u * blockDim.x;
+                if (ord >= npages) break;
+                if (ord < ndev) {
+                    if (id[u] >= 0 && id[u] < ps.N) ps.ring[(tail0 + (uint64_t)ord) % (uint64_t)ps.N] = id[u];
+                } else if (ord < ndev + nspill && id[u] >= ps.SB && id[u] < ps.SB + ps.SP) {
+                    ps.spill_ring[(stail0 + (uint64_t)(ord - ndev)) % (uint64_t)ps.SP] = (int32_t)(id[u] - ps.SB);
+                }
+            }
+        }
+        __syncthreads(); // every thread has read the tails
+        if (threadIdx.x == 0) {
+            st->tail = tail0 + (uint64_t)ndev;
+            st->spill_tail = stail0 + (uint64_t)nspill;
+            st->held = held - npages;
+        }
+    }
     const int64_t tiles = npages * tiles_per_page;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t ord = tile / tiles_per_page;
@@ -479,11 +499,6 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
         if (!ok) {
             if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
             continue;
-        }
-        if (sub == 0 && threadIdx.x == 0) { // first tile recycles the page
-            if (ord < ndev) ps.ring[(tail0 + (uint64_t)ord) % (uint64_t)ps.N] = (int32_t)id;
-            else if (id >= 0)
-                ps.spill_ring[(stail0 + (uint64_t)(ord - ndev)) % (uint64_t)ps.SP] = (int32_t)(id - ps.SB);
         }
         if (id < 0) continue;
         if (d.row0 + d.nrows > dst_rows) {
@@ -1161,8 +1176,6 @@ extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, voi
     plane_fit(p, h.nplanes, h.rb, page_off);
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *st = reinterpret_cast<ap_pool_state *>(p->dev_meta);
-    ap::launch(ap::k_pop_plan, 1, 32, 0, p->stream, st, rec.hdr);
-    AP_CHECK_LAUNCH("stash pop plan launch");
     ap::Planes pl;
     for (int i = 0; i < 2; ++i) {
         pl.p[i] = (i < nplanes) ? static_cast<uint8_t *>(dst_planes[i]) : nullptr;

@@ -692,6 +692,65 @@ class ScheduleStep:
                                                                 stream=s))
 
 
+def fill_rate(device, nbytes=2 << 30, reps=5):
+    """Write-only HBM rate (GB/s): a fill of `nbytes` on the device, timed with
+    CUDA events.  The fused dispatch + push writes 16 bytes for each byte it
+    reads, so this rate, not the 1:1 copy peak, is the ceiling it approaches."""
+    import torch
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s = torch.cuda.Stream(device)
+    with torch.cuda.stream(s):
+        buf.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for i in range(reps):
+            buf.fill_(i)
+        b.record(s)
+        b.synchronize()
+    del buf
+    return round(reps * nbytes / (a.elapsed_time(b) / 1e3) / 1e9, 1)
+
+
+def link_rates(device, nbytes=1 << 30, reps=3):
+    """Host-link copy rates (GB/s), host to device and device to host, of
+    one pinned-memory copy of `nbytes` timed with CUDA events."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s = torch.cuda.Stream(device)
+    rates = {}
+    with torch.cuda.stream(s):
+        for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+            dst.copy_(src, non_blocking=True)  # warm-up
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            b.record(s)
+            b.synchronize()
+            rates[name] = round(reps * nbytes / (a.elapsed_time(b) / 1e3) / 1e9, 1)
+    del d
+    return rates
+
+
+def link_bound(st, link, peak, pass_s, device):
+    """Bound of a schedule whose spilled pages cross the host link: the HBM
+    bytes at the HBM copy peak plus the spilled bytes at the measured link
+    rates (each spilled byte is written to the host at its push and read back
+    at its pop, so half the link bytes go each way)."""
+    per_pass = sum(st.bytes["route"] + st.bytes["dispatch_stash"] if op == "push"
+                   else st.bytes["pop"] + st.bytes["combine"] for op, _ in st.sched)
+    rates = link_rates(device)
+    d2h = h2d = link // 2
+    hbm = per_pass - link  # a spilled byte moves once through HBM and once over the link each way
+    bound_s = hbm / (peak * 1e9) + d2h / (rates["d2h"] * 1e9) + h2d / (rates["h2d"] * 1e9)
+    return {"link_gbs": rates, "hbm_bytes": int(hbm), "link_bytes": {"d2h": d2h, "h2d": h2d},
+            "bound_ms": round(bound_s * 1e3, 3), "frac": round(bound_s / pass_s, 3),
+            "note": "bound = HBM bytes / HBM copy peak + spilled bytes / pinned-copy link rate, each way"}
+
+
 def native_schedule(args):
     """Time one other workload's schedule (graph replay) and its per-call rates."""
     import torch
@@ -736,6 +795,7 @@ def native_schedule(args):
     ops = ops_table(events, st.bytes, peak)
     flags = st.pool.overflow()
     link = st.spilled_bytes() if wl.spill_pages else 0
+    bound = link_bound(st, link, peak, el / steps, device) if link else None
     line = {"metric": METRIC, "workload": wl.name, "value": round(st.tokens * steps / el, 1), "unit": "tokens/s",
             "rows_kept_per_record": round(st.rows_kept, 1), "host_link_bytes_per_step": link,
             "ms_per_step": round(el * 1e3 / steps, 4), "steps": steps, "tokens_per_step": st.tokens,
@@ -744,6 +804,8 @@ def native_schedule(args):
                        "spill_pages": wl.spill_pages, "schedule": [f"{op} {n}" for op, n in st.sched][:12]},
             "ops": ops, "pool_flags": flags, "gpu_launches": launches_per_pass * steps, "clocks": clocks,
             "note": "ops: mean CUDA-event time per call over eager passes; pops of spilled records read host memory"}
+    if bound:
+        line["link_bound"] = bound
     print(json.dumps(line), flush=True)
 
 
@@ -917,6 +979,7 @@ def native(args):
                 "achieved": ops[dom]["copy_gbs" if timed else "gbs"], "peak": peak, "unit": "GB/s",
                 "frac": ops[dom]["copy_frac" if timed else "frac"], "traffic": traffic, "peak_source": peak_src,
                 "bytes_per_launch": step.bytes[kcall],
+                "write_only_gbs": fill_rate(device),
                 "note": (f"achieved = the call's algorithmic bytes / mean CUDA-event time of its copy kernel, events "
                          f"recorded by the library on the paging stream around the kernel, over {op_steps} eager "
                          f"steps; the whole call (with its plan kernels) is under ops")}
