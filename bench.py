@@ -697,7 +697,7 @@ def fill_rate(device, nbytes=2 << 30, reps=5):
     CUDA events.  The fused dispatch + push writes 16 bytes for each byte it
     reads, so this rate, not the 1:1 copy peak, is the ceiling it approaches."""
     import torch
-    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    buf = torch.empty(nbytes // 8, dtype=torch.int64, device=device)  # 8-byte elements: 16-byte vector stores
     s = torch.cuda.Stream(device)
     with torch.cuda.stream(s):
         buf.fill_(1)
