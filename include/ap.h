@@ -418,8 +418,9 @@ ap_status ap_stash_pop(ap_pool *pool, int32_t slot, int32_t nplanes,
 /* Copy-kernel timing without a profiler.  While set, every push, fused
  * dispatch + push and pop records `before` and `after` (CUDA events, as
  * void *) on the paging stream immediately around its copy kernel, so their
- * elapsed time after the call is that kernel's duration (the call's small
- * plan kernels fall outside).  Passing NULL, NULL stops it.  The events stay
+ * elapsed time after the call is that kernel's duration (a push's small
+ * plan kernels fall outside; a pop is its copy kernel alone).  Passing NULL,
+ * NULL stops it.  The events stay
  * owned by the caller and must outlive the calls that record them. */
 ap_status ap_pool_time_copies(ap_pool *pool, void *before, void *after);
 
