@@ -33,18 +33,22 @@ ap_status dispatch_check(const char *who, const void *x, int64_t T, int32_t H, c
                          const void *scratch, int64_t scratch_bytes);
 ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
                             int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, void *scratch,
-                            uint32_t *d_status, cudaStream_t st);
+                            uint32_t *d_status, cudaStream_t st, const void *x = nullptr, int64_t x_rb = 0);
 // The count/rank stage alone (block histograms into scratch, in-block ranks
 // into dest), and the number of count/rank blocks; the fused dispatch + stash
-// runs its own scan (see dispatch_scan.cuh).
+// runs its own scan (see dispatch_scan.cuh).  x / x_rb (here, in
+// dispatch_metadata and in dispatch_route_count_rank): the input rows the row
+// copy after these kernels reads; each count/rank block prefetches its own
+// rows into L2 (nullptr: none).
 ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
-                              uint32_t *d_status, cudaStream_t st);
+                              uint32_t *d_status, cudaStream_t st, const void *x = nullptr, int64_t x_rb = 0);
 int dispatch_blocks(int64_t T);
 // Route (as ap_route_topk, into idx and w) and count/rank in one launch: the
 // same outputs as ap_route_topk followed by dispatch_count_rank.  Arguments
 // are checked by the caller.
 ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
-                                    void *scratch, int32_t *dest, cudaStream_t st);
+                                    void *scratch, int32_t *dest, cudaStream_t st, const void *x = nullptr,
+                                    int64_t x_rb = 0);
 
 #define AP_CHECK_LAUNCH(what)                                   \
     do {                                                        \

@@ -95,12 +95,39 @@ __device__ __forceinline__ bool block_count_rank(const int32_t *pidx, int64_t p0
     return bad;
 }
 
+// Input rows a later kernel of the call reads, brought into L2 ahead of it.
+// The metadata kernels that run before a row copy leave HBM idle; a bulk
+// prefetch of their block's rows [t0, t0 + ntok) then lets the copy read its
+// input from L2 while it streams its writes.  A hint only: nothing waits on
+// it and no result depends on it.  x and rb are 16-byte multiples (the caller
+// passes x = nullptr otherwise).
+struct RowPrefetch {
+    const uint8_t *x;
+    int64_t rb;
+};
+
+__device__ __forceinline__ void prefetch_rows_l2(RowPrefetch pf, int64_t t0, int64_t ntok)
+{
+    if (!pf.x || ntok <= 0) return;
+    constexpr int64_t kPiece = 64 << 10;
+    const int64_t begin = t0 * pf.rb, bytes = ntok * pf.rb;
+    for (int64_t i = threadIdx.x; i * kPiece < bytes; i += blockDim.x) {
+        const int64_t off = i * kPiece;
+        const uint32_t n = (uint32_t)(bytes - off < kPiece ? bytes - off : kPiece);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(pf.x + begin + off), "r"(n) : "memory");
+    }
+}
+
 // Count/rank blocks of kTokPerBlk tokens reading idx from global memory.
 __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
                                                              int32_t *__restrict__ blk, int32_t *__restrict__ dest,
-                                                             uint32_t *d_status)
+                                                             uint32_t *d_status, RowPrefetch pf)
 {
     pdl_begin();
+    {
+        const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
+        prefetch_rows_l2(pf, t0, (T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
+    }
     extern __shared__ int32_t cnt[]; // [kRankWarps][E]
     const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
     const int64_t p1 = (p0 + (int64_t)kTokPerBlk * k < T * k) ? p0 + (int64_t)kTokPerBlk * k : T * k;
@@ -118,7 +145,7 @@ constexpr int kRouteRankWarps = 32;
 template <int NV>
 __global__ void __launch_bounds__(kRouteRankWarps * kWarp) k_route_count_rank(
     const float *__restrict__ logits, int64_t T, int E, int k, int32_t *__restrict__ idx, float *__restrict__ w,
-    int32_t *__restrict__ blk, int32_t *__restrict__ dest)
+    int32_t *__restrict__ blk, int32_t *__restrict__ dest, RowPrefetch pf)
 {
     pdl_begin();
     extern __shared__ int32_t smem[]; // cnt [32][E], then the block's ids [kTokPerBlk * k]
@@ -127,6 +154,7 @@ __global__ void __launch_bounds__(kRouteRankWarps * kWarp) k_route_count_rank(
     const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
     const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
     const int ntok = (int)((T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
+    prefetch_rows_l2(pf, t0, ntok);
     for (int tt = wid; tt < ntok; tt += kRouteRankWarps) {
         int e;
         float wt;
@@ -423,14 +451,21 @@ ap_status dispatch_check(const char *who, const void *x, int64_t T, int32_t H, c
     return AP_OK;
 }
 
+// The row prefetch of the copy that follows: only for 16-byte aligned rows.
+static RowPrefetch row_prefetch(const void *x, int64_t x_rb)
+{
+    const bool ok = x && ((reinterpret_cast<uintptr_t>(x) | (uintptr_t)x_rb) & 15) == 0;
+    return RowPrefetch{ok ? static_cast<const uint8_t *>(x) : nullptr, x_rb};
+}
+
 ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
-                              uint32_t *d_status, cudaStream_t st)
+                              uint32_t *d_status, cudaStream_t st, const void *x, int64_t x_rb)
 {
     const int64_t nb = nblocks(T);
     if (nb == 0) return AP_OK;
     const size_t smem = (size_t)kRankWarps * E * sizeof(int32_t);
     launch(k_count_rank, (unsigned)nb, kRankThreads, smem, st, idx, T, k, E, static_cast<int32_t *>(scratch), dest,
-                                                           d_status);
+                                                           d_status, row_prefetch(x, x_rb));
     AP_CHECK_LAUNCH("dispatch count/rank launch");
     return AP_OK;
 }
@@ -439,7 +474,7 @@ int dispatch_blocks(int64_t T) { return (int)nblocks(T); }
 
 template <int NV>
 ap_status launch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
-                                  int32_t *blk, int32_t *dest, cudaStream_t st)
+                                  int32_t *blk, int32_t *dest, cudaStream_t st, RowPrefetch pf)
 {
     const size_t smem = ((size_t)kRouteRankWarps * E + (size_t)kTokPerBlk * k) * sizeof(int32_t);
     static const cudaError_t attr = cudaFuncSetAttribute((const void *)k_route_count_rank<NV>,
@@ -448,32 +483,33 @@ ap_status launch_route_count_rank(const float *logits, int64_t T, int32_t E, int
                                                                sizeof(int32_t)));
     if (attr != cudaSuccess) return cuda_fail(attr, "route + count/rank: shared memory limit");
     launch(k_route_count_rank<NV>, (unsigned)nblocks(T), kRouteRankWarps * kWarp, smem, st, logits, T, E, k, idx, w,
-           blk, dest);
+           blk, dest, pf);
     AP_CHECK_LAUNCH("route + count/rank launch");
     return AP_OK;
 }
 
 ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
-                                    void *scratch, int32_t *dest, cudaStream_t st)
+                                    void *scratch, int32_t *dest, cudaStream_t st, const void *x, int64_t x_rb)
 {
     if (nblocks(T) == 0) return AP_OK;
     int32_t *blk = static_cast<int32_t *>(scratch);
-    if (E <= 32) return launch_route_count_rank<1>(logits, T, E, k, idx, w, blk, dest, st);
-    if (E <= 64) return launch_route_count_rank<2>(logits, T, E, k, idx, w, blk, dest, st);
-    if (E <= 128) return launch_route_count_rank<4>(logits, T, E, k, idx, w, blk, dest, st);
-    if (E <= 256) return launch_route_count_rank<8>(logits, T, E, k, idx, w, blk, dest, st);
+    const RowPrefetch pf = row_prefetch(x, x_rb);
+    if (E <= 32) return launch_route_count_rank<1>(logits, T, E, k, idx, w, blk, dest, st, pf);
+    if (E <= 64) return launch_route_count_rank<2>(logits, T, E, k, idx, w, blk, dest, st, pf);
+    if (E <= 128) return launch_route_count_rank<4>(logits, T, E, k, idx, w, blk, dest, st, pf);
+    if (E <= 256) return launch_route_count_rank<8>(logits, T, E, k, idx, w, blk, dest, st, pf);
     // more than 8 candidates per lane do not fit a 1024-thread block's
     // registers: route and count/rank as two launches
     ap_status s = ap_route_topk(logits, T, E, k, idx, w, st);
     if (s != AP_OK) return s;
-    return dispatch_count_rank(T, idx, k, E, scratch, dest, nullptr, st);
+    return dispatch_count_rank(T, idx, k, E, scratch, dest, nullptr, st, x, x_rb);
 }
 
 ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
                             int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest, void *scratch,
-                            uint32_t *d_status, cudaStream_t st)
+                            uint32_t *d_status, cudaStream_t st, const void *x, int64_t x_rb)
 {
-    ap_status s = dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
+    ap_status s = dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, x_rb);
     if (s != AP_OK) return s;
     launch(k_scan, 1, 1024, 0, st, static_cast<int32_t *>(scratch), (int)nblocks(T), E, capacity, padded, counts, live,
                                seg_off);
@@ -498,7 +534,8 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
     if (out_dtype == AP_DTYPE_E4M3 && T > 0 && !xd_scale)
         return fail(AP_EINVAL, "dispatch_permute: E4M3 needs xd_scale");
     cudaStream_t st = (cudaStream_t)stream;
-    s = dispatch_metadata(T, idx, k, E, capacity, padded, counts, live, seg_off, dest, scratch, d_status, st);
+    s = dispatch_metadata(T, idx, k, E, capacity, padded, counts, live, seg_off, dest, scratch, d_status, st, x,
+                          (int64_t)H * 2);
     if (s != AP_OK || T == 0) return s;
     const Ranks ranks{idx, dest, k, E, capacity, static_cast<const int32_t *>(scratch), seg_off, src_tok};
     if (out_dtype == AP_DTYPE_BF16) {

@@ -1065,8 +1065,8 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     if (logits && k > E) return fail(AP_EINVAL, "route_dispatch_stash: k=%d > E=%d", k, E);
     if (logits && T > 0 && !w) return fail(AP_EINVAL, "route_dispatch_stash: NULL weights");
     cudaStream_t st = p->stream;
-    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st)
-               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st);
+    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, (int64_t)H * 2)
+               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, (int64_t)H * 2);
     if (s != AP_OK) return s;
 
     const int32_t pos = (p->q_head[slot] + p->q_count[slot]) % p->cfg.max_records_per_slot;
