@@ -114,7 +114,10 @@ __device__ __forceinline__ void st_stream(char *p, char v) { __stcs(p, v); }
 // Copy n bytes from src to dst with all threads of the block, vectorised to the
 // widest width both pointers share (16, 8, 4, 2 or 1 bytes), with byte-wise
 // heads and tails.  Eight loads are issued before their stores so each
-// thread keeps 128 bytes in flight.
+// thread keeps 128 bytes in flight, and the last, partial pass goes in
+// predicated groups rather than one vector at a time, so ranges that are not
+// a multiple of 8 vectors per thread (e.g. 15 rows of 2056 bytes) keep
+// several loads in flight too.
 template <typename V>
 __device__ __forceinline__ void block_copy_vec(uint8_t *dst, const uint8_t *src, int64_t nvec)
 {
@@ -130,7 +133,19 @@ __device__ __forceinline__ void block_copy_vec(uint8_t *dst, const uint8_t *src,
 #pragma unroll
         for (int u = 0; u < U; ++u) st_stream(d + i + u * nt, r[u]);
     }
-    for (; i < nvec; i += nt) st_stream(d + i, ld_stream(s + i));
+    // the partial pass, in predicated groups of 2 (larger groups spill
+    // registers in the copy kernels, and 2 measured faster than 4 on rows of
+    // 2056 bytes); narrower vectors (rare, short ranges) one at a time
+    constexpr int UT = sizeof(V) >= 8 ? 2 : 1;
+    for (; i < nvec; i += UT * nt) {
+        V r[UT];
+#pragma unroll
+        for (int u = 0; u < UT; ++u)
+            if (i + u * nt < nvec) r[u] = ld_stream(s + i + u * nt);
+#pragma unroll
+        for (int u = 0; u < UT; ++u)
+            if (i + u * nt < nvec) st_stream(d + i + u * nt, r[u]);
+    }
 }
 
 __device__ __forceinline__ void block_copy(uint8_t *dst, const uint8_t *src, int64_t n)
