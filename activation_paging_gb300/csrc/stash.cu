@@ -9,7 +9,9 @@
 // host spill and a sticky overflow flag; a grid bound (default 2048) that
 // changes neither the capacity nor the rows copied.  "Verification": wrapped
 // allocation and recycling, device counts that change under CUDA-graph replay,
-// BF16/FP8 payloads, host spill and overflow.
+// BF16/FP8 payloads, host spill and overflow.  (Here a pop recycles its pages
+// from the record's page table in one CTA instead of each page's first tile;
+// see k_pop_copy.)
 //
 // A fused dispatch + push (k_scan_plan, then k_dispatch_stash_copy or its
 // E4M3 form) plans the same way but leaves the page descriptors to the copy
