@@ -247,7 +247,8 @@ ap_status ap_dispatch_backward(const void *dxd, int64_t rows, int32_t H,
  * A pop takes the slot's oldest record, copies every page back to the same
  * rows of the destination planes (rows outside the live prefixes are not
  * touched) and returns the pages to the free ring in page order.
- * "Exactly full" is not an overflow.  Flags stay set until ap_pool_reset.
+ * A pool filled exactly to its last page has not overflowed.  Flags stay set
+ * until ap_pool_reset.
  * ========================================================================== */
 typedef struct ap_pool ap_pool; /* opaque host object */
 
