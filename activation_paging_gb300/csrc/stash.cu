@@ -786,6 +786,18 @@ void mark(const ap_pool *p, cudaEvent_t ev)
     if (ev) (void)cudaEventRecord(ev, p->stream);
 }
 
+// Rows per copy tile: about 32 KB of plane 0, rounded to the nearest whole
+// row (so that rows just over a divisor of 32 KB, such as 2056-byte E4M3
+// rows, fill the copy's full eight-vector passes rather than leaving most of
+// a pass to its tail), at least one row and at most a page.
+int64_t tile_rows(int64_t rb0, int64_t P)
+{
+    int64_t rpt = (32768 + rb0 / 2) / rb0;
+    if (rpt < 1) rpt = 1;
+    if (rpt > P) rpt = P;
+    return rpt;
+}
+
 ap::PageSpace page_space(const ap_pool *p)
 {
     ap::PageSpace ps;
@@ -991,9 +1003,7 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
     h.rb[0] = rb[0];
     h.rb[1] = rb[1];
     const int64_t P = p->cfg.page_tokens;
-    int64_t rpt = 32768 / rb[0];
-    if (rpt < 1) rpt = 1;
-    if (rpt > P) rpt = P;
+    const int64_t rpt = tile_rows(rb[0], P);
     h.rows_per_tile = (int32_t)rpt;
     h.tiles_per_page = (int32_t)((P + rpt - 1) / rpt);
     int64_t bound = nseg + (src_rows + P - 1) / P;
@@ -1080,9 +1090,7 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     h.rb[0] = rb[0];
     h.rb[1] = rb[1];
     const int64_t P = p->cfg.page_tokens;
-    int64_t rpt = 32768 / rb[0];
-    if (rpt < 1) rpt = 1;
-    if (rpt > P) rpt = P;
+    const int64_t rpt = tile_rows(rb[0], P);
     h.rows_per_tile = (int32_t)rpt;
     h.tiles_per_page = (int32_t)((P + rpt - 1) / rpt);
     int64_t bound = E + (xd_rows + P - 1) / P;
