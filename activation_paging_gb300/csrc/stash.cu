@@ -598,96 +598,121 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
     }
 }
 
-// Fused dispatch + push for E4M3 payloads: the token row is held in registers
-// (NR 16-byte vectors per lane, H <= 256 * NR), quantised once with its row
-// scale (same arithmetic as the E4M3 dispatch), and each kept pair's codes and
-// scale go to its dispatch row and to its page (codes at row r, scale in the
-// page's second plane).  The pair holding row 0 of a page records the page.
-template <int NR>
-__global__ void __launch_bounds__(256, 3) k_dispatch_stash_e4m3(
+// Fused dispatch + push for E4M3 payloads, two warps per token: warp h of a
+// warp pair holds half h of the row (16-byte vectors [h * half0, ...), at
+// most NRH per lane), so twice as many warps share a record's rows.  The two
+// warps meet once per token at a named barrier: by then warp 0 has resolved
+// the token's pairs (finalize_dest, page ids, page-table entries and
+// descriptors of a page's row 0) and both have put their half's amax in
+// shared memory (double-buffered by token parity, so a warp that runs ahead
+// never overwrites what its partner still reads).  Both then quantise with
+// the row's scale (same arithmetic as the E4M3 dispatch) and write their half
+// of every kept pair's codes to its dispatch row and page row; warp 0 writes
+// the scales (dispatch scale and the page's second plane).
+__device__ __forceinline__ void pair_barrier(int id)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(2 * kWarp) : "memory");
+}
+
+template <int NRH>
+__global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
     const uint16_t *__restrict__ x, int64_t T, int H, const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
     int k, int E, int capacity, const int32_t *__restrict__ blk, const int32_t *__restrict__ seg_off,
     int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd, float *__restrict__ xd_scale, ap_pool_state *st,
     RecPtr rec, PageSpace ps, int P, int64_t plane1_off)
 {
     pdl_begin();
-    const int lane = (int)lane_id();
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    constexpr int kPairs = 256 / (2 * kWarp); // warp pairs per block
+    __shared__ uint32_t s_amax[2][kPairs][2];
+    __shared__ int32_t s_d[2][kPairs][kWarp];
+    __shared__ unsigned long long s_prow[2][kPairs][kWarp];
+    const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
+    const int pr = wid >> 1, h = wid & 1;
     const int nstep = H / 8;
+    const int half0 = (nstep + 1) / 2;
+    const int s_begin = h ? half0 : 0, s_end = h ? nstep : half0;
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
     const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
-    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+    int buf = 0;
+    for (int64_t t = (int64_t)blockIdx.x * kPairs + pr; t < T; t += (int64_t)gridDim.x * kPairs, buf ^= 1) {
+        // this half's vectors first: their latency overlaps the lookups below
+        const int4 *row = reinterpret_cast<const int4 *>(x + t * H);
+        int4 v[NRH];
+#pragma unroll
+        for (int i = 0; i < NRH; ++i) {
+            const int s = s_begin + lane + i * kWarp;
+            v[i] = (s < s_end) ? ld_stream(row + s) : make_int4(0, 0, 0, 0);
+        }
         int32_t my_d = -1;
-        uint8_t *my_row = nullptr;   // this lane's pair: codes row in its page
-        float *my_scale = nullptr;   // and its scale slot in the page's second plane
-        if (lane < k) {
-            my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
-            const int e = idx[t * k + lane];
-            if (my_d >= 0 && e >= 0 && e < E) {
-                const int64_t so = rec.seg_off[e], lv = rec.live[e];
-                const int64_t r = (int64_t)my_d - so;
-                if (r >= 0 && r < lv) {
-                    const int64_t ord = rec.pg_base[e] + r / P;
-                    if (ord < npages) {
-                        bool corrupt;
-                        const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
-                        if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                        if (r % P == 0) { // row 0 of the page records it and its descriptor
-                            rec.page_table[ord] = (int32_t)id;
-                            PageDesc pd;
-                            pd.row0 = so + r;
-                            pd.nrows = (int32_t)(lv - r < P ? lv - r : P);
-                            pd.pad = 0;
-                            rec.desc[ord] = pd;
-                        }
-                        if (id >= 0) {
-                            uint8_t *page = page_addr(ps, id);
-                            my_row = page + (r % P) * H;
-                            my_scale = reinterpret_cast<float *>(page + plane1_off + (r % P) * 4);
+        float *my_scale = nullptr;
+        if (h == 0) {
+            uint8_t *my_row = nullptr;
+            if (lane < k) {
+                my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
+                const int e = idx[t * k + lane];
+                if (my_d >= 0 && e >= 0 && e < E) {
+                    const int64_t so = rec.seg_off[e], lv = rec.live[e];
+                    const int64_t r = (int64_t)my_d - so;
+                    if (r >= 0 && r < lv) {
+                        const int64_t ord = rec.pg_base[e] + r / P;
+                        if (ord < npages) {
+                            bool corrupt;
+                            const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
+                            if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+                            if (r % P == 0) { // row 0 of the page records it and its descriptor
+                                rec.page_table[ord] = (int32_t)id;
+                                PageDesc pd;
+                                pd.row0 = so + r;
+                                pd.nrows = (int32_t)(lv - r < P ? lv - r : P);
+                                pd.pad = 0;
+                                rec.desc[ord] = pd;
+                            }
+                            if (id >= 0) {
+                                uint8_t *page = page_addr(ps, id);
+                                my_row = page + (r % P) * H;
+                                my_scale = reinterpret_cast<float *>(page + plane1_off + (r % P) * 4);
+                            }
                         }
                     }
                 }
             }
-        }
-        const int4 *row = reinterpret_cast<const int4 *>(x + t * H);
-        int4 v[NR];
-#pragma unroll
-        for (int i = 0; i < NR; ++i) {
-            const int s = lane + i * kWarp;
-            v[i] = (s < nstep) ? ld_stream(row + s) : make_int4(0, 0, 0, 0);
+            s_d[buf][pr][lane] = my_d;
+            s_prow[buf][pr][lane] = (unsigned long long)reinterpret_cast<uintptr_t>(my_row);
         }
         uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < NR; ++i) {
+        for (int i = 0; i < NRH; ++i) {
             m = absmax_bf16x2(m, (uint32_t)v[i].x);
             m = absmax_bf16x2(m, (uint32_t)v[i].y);
             m = absmax_bf16x2(m, (uint32_t)v[i].z);
             m = absmax_bf16x2(m, (uint32_t)v[i].w);
         }
+        const uint32_t half_amax = __reduce_max_sync(0xffffffffu, absmax_bits(m));
+        if (lane == 0) s_amax[buf][pr][h] = half_amax;
+        pair_barrier(1 + pr);
+        const uint32_t a0 = s_amax[buf][pr][0], a1 = s_amax[buf][pr][1];
         float scale, inv;
-        e4m3_scales(__reduce_max_sync(0xffffffffu, absmax_bits(m)), scale, inv);
-        if (my_d >= 0) {
+        e4m3_scales(a0 > a1 ? a0 : a1, scale, inv);
+        if (h == 0 && my_d >= 0) {
             xd_scale[my_d] = scale;
             if (my_scale) *my_scale = scale;
         }
 #pragma unroll
-        for (int i = 0; i < NR; ++i) { // codes replace the values in place (first 8 bytes)
+        for (int i = 0; i < NRH; ++i) { // codes replace the values in place (first 8 bytes)
             const int2 c = quantize8_e4m3(v[i], inv);
             v[i].x = c.x;
             v[i].y = c.y;
         }
         for (int j = 0; j < k; ++j) {
-            const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
-            const unsigned long long pg =
-                __shfl_sync(0xffffffffu, (unsigned long long)reinterpret_cast<uintptr_t>(my_row), j);
+            const int32_t d = s_d[buf][pr][j];
             if (d < 0) continue;
             uint8_t *drow = xd + (int64_t)d * H;
-            uint8_t *prow = reinterpret_cast<uint8_t *>(static_cast<uintptr_t>(pg));
+            uint8_t *prow = reinterpret_cast<uint8_t *>(static_cast<uintptr_t>(s_prow[buf][pr][j]));
 #pragma unroll
-            for (int i = 0; i < NR; ++i) {
-                const int s = lane + i * kWarp;
-                if (s < nstep) {
+            for (int i = 0; i < NRH; ++i) {
+                const int s = s_begin + lane + i * kWarp;
+                if (s < s_end) {
                     const int2 c = make_int2(v[i].x, v[i].y);
                     st_stream(reinterpret_cast<int2 *>(drow + (int64_t)s * 8), c);
                     if (prow) st_stream(reinterpret_cast<int2 *>(prow + (int64_t)s * 8), c);
@@ -1114,14 +1139,16 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
         const int32_t *blk = static_cast<const int32_t *>(scratch);
         if (fp8) {
             const uint16_t *xs16 = static_cast<const uint16_t *>(x);
-#define AP_LAUNCH_E4M3(NRV)                                                                                       \
-    ap::launch(ap::k_dispatch_stash_e4m3<NRV>, grid, 256, 0, st,                                                          \
-        xs16, T, H, idx, dest, k, E, capacity, blk, seg_off, src_tok, xo, xd_scale, stt, rec, ps,                  \
-        p->cfg.page_tokens, page_off[1])
-            if (H <= 256 * 4) AP_LAUNCH_E4M3(4);
-            else if (H <= 256 * 8) AP_LAUNCH_E4M3(8);
-            else if (H <= 256 * 9) AP_LAUNCH_E4M3(9);
-            else AP_LAUNCH_E4M3(16);
+            const int64_t want2 = (T + 3) / 4; // four tokens (warp pairs) per block
+            const int grid2 = (int)(want2 < cap ? want2 : cap);
+#define AP_LAUNCH_E4M3(NRH)                                                                                       \
+    ap::launch(ap::k_dispatch_stash_e4m3<NRH>, grid2, 256, 0, st, xs16, T, H, idx, dest, k, E, capacity, blk,       \
+               seg_off, src_tok, xo, xd_scale, stt, rec, ps, p->cfg.page_tokens, page_off[1])
+            if (H <= 512) AP_LAUNCH_E4M3(1);
+            else if (H <= 1024) AP_LAUNCH_E4M3(2);
+            else if (H <= 2048) AP_LAUNCH_E4M3(4);
+            else if (H <= 2304) AP_LAUNCH_E4M3(5);
+            else AP_LAUNCH_E4M3(8);
 #undef AP_LAUNCH_E4M3
         } else if ((al & 15) == 0)
             ap::launch(ap::k_dispatch_stash_copy<int4>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,
