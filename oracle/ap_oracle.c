@@ -23,9 +23,36 @@
  * Where the sources are silent the oracle takes one stated reading; the
  * readings are listed beside each function.
  *
- * Parity status: every function below is pinned by CPU tests against closed
- * forms, brute force, independent library routines or invariants; none is
- * "parity unpinned".
+ * Parity status: each function is pinned by CPU tests that do not re-run its
+ * own arithmetic (tests/test_oracle_*.py):
+ *   or_route_topk           closed forms, numpy's stable sort and scipy's
+ *                           softmax, ties, shift invariance, k = E and
+ *                           E = k = 1 (test_oracle_route.py);
+ *   or_dispatch_plan        brute-force counting, stable ranks, capacity and
+ *                           both layouts, sum rules (test_oracle_dispatch.py);
+ *   or_permute_rows         rows at dest, canary rows untouched
+ *                           (test_oracle_dispatch.py);
+ *   or_e4m3_encode(_n),
+ *   or_e4m3_decode          an independent OCP E4M3 decoder: every code,
+ *                           every midpoint, nearest on a grid, saturation
+ *                           (test_oracle_fp8.py);
+ *   or_quantize_rows_e4m3   scale = amax/448 in single precision, the largest
+ *                           element at +-448, dequantisation error within
+ *                           half a step (test_oracle_fp8.py);
+ *   or_permute_rows_fp8     a numpy restatement of the row and scale
+ *                           placement on hand-built dest maps with drops,
+ *                           and the padded FP8 dispatch (test_oracle_fp8.py);
+ *   or_combine, or_f32_to_bf16  exact double sums within the FP32 bound,
+ *                           k = 1, all-dropped tokens, identity experts
+ *                           (test_oracle_combine.py);
+ *   or_combine_backward,
+ *   or_dispatch_backward    exact gradients in rationals, unit weights,
+ *                           dropped pairs, bad rows (test_oracle_backward.py);
+ *   or_pool_*               FIFO order, byte survival, page conservation,
+ *                           wrap-around, spill and loss, sticky flags, P = 1
+ *                           (test_oracle_pool.py); calibration demand and
+ *                           growth (test_oracle_calibrate.py).
+ * None is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>

@@ -97,3 +97,78 @@ def test_quantize_rows():
     err = np.abs(deq - xf)
     bound = 2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * s[:, None] * 1.0001 + 1e-30
     assert np.all(err <= bound * (1 + 2 ** -20))
+
+
+def _expected_fp8_rows(q, scale, dest, rows, fill):
+    """The FP8 dispatch buffer restated with numpy: every kept pair (t, j)
+    places token t's H code bytes at row dest[t, j] and its scale bits at the
+    same row of the scale plane; rows no pair maps to keep the canary."""
+    T, H = q.shape
+    xd = np.full((rows, H), fill, np.uint8)
+    xs = np.full(rows, fill * 0x01010101, np.uint32)
+    tok = np.repeat(np.arange(T), dest.shape[1]).reshape(dest.shape)
+    kept = dest >= 0
+    xd[dest[kept]] = q[tok[kept]]
+    xs[dest[kept]] = scale.view(np.uint32)[tok[kept]]
+    return xd, xs
+
+
+def _run_oracle_fp8(q, scale, dest, rows, fill):
+    xd = np.full((rows, q.shape[1]), fill, np.uint8)
+    xs = np.full(rows, fill * 0x01010101, np.uint32).view(np.float32)
+    oracle.permute_rows_fp8(q, scale, dest, xd, xs)
+    return xd, xs.view(np.uint32)
+
+
+@pytest.mark.parametrize("T,H,k,rows,drop", [(5, 8, 2, 16, 0.0), (37, 24, 3, 200, 0.3), (64, 16, 6, 384, 0.5)])
+def test_permute_rows_fp8_places_codes_and_scales(T, H, k, rows, drop):
+    """Hand-built injective dest maps (some pairs dropped): the oracle's FP8
+    permute matches the numpy restatement byte for byte, scales included."""
+    rng = np.random.default_rng(T * 1000 + H)
+    q = rng.integers(0, 256, (T, H), dtype=np.uint8)
+    # distinct scales per token, so a scale taken from the wrong token or row shows
+    scale = (np.arange(T, dtype=np.float32) + 1.0) * np.float32(0.375)
+    dest = rng.permutation(rows)[:T * k].astype(np.int32).reshape(T, k)
+    dest[rng.random((T, k)) < drop] = -1
+    xd, xs = _run_oracle_fp8(q, scale, dest, rows, 0x5C)
+    exd, exs = _expected_fp8_rows(q, scale, dest, rows, 0x5C)
+    assert np.array_equal(xd, exd)
+    assert np.array_equal(xs, exs)
+    # every untouched row still holds the canary (a write past the row would show here)
+    untouched = np.setdiff1d(np.arange(rows), dest[dest >= 0])
+    assert np.all(xd[untouched] == 0x5C) and np.all(xs[untouched] == 0x5C5C5C5C)
+
+
+def test_permute_rows_fp8_catches_swapped_scale_and_row():
+    """The restatement is sharp enough to catch a plausible slip: a scale
+    written for the wrong token or a code row shifted by one differ from it."""
+    rng = np.random.default_rng(3)
+    T, H, k, rows = 9, 8, 2, 40
+    q = rng.integers(0, 256, (T, H), dtype=np.uint8)
+    scale = (np.arange(T, dtype=np.float32) + 2.0)
+    dest = rng.permutation(rows)[:T * k].astype(np.int32).reshape(T, k)
+    exd, exs = _expected_fp8_rows(q, scale, dest, rows, 0)
+    wrong_s = exs.copy()
+    wrong_s[dest[0, 0]] = scale.view(np.uint32)[1]
+    assert not np.array_equal(wrong_s, exs)
+    wrong_x = exd.copy()
+    wrong_x[dest[2, 1]] = q[3]
+    assert not np.array_equal(wrong_x, exd)
+    xd, xs = _run_oracle_fp8(q, scale, dest, rows, 0)
+    assert np.array_equal(xd, exd) and np.array_equal(xs, exs)
+
+
+def test_fp8_dispatch_padded_ragged_with_drops():
+    """The whole FP8 dispatch of the oracle on a padded layout with a ragged
+    expert count and drops: codes and scales are the row quantisation of each
+    kept pair's token, placed at the plan's rows; padding and drops keep the
+    canary."""
+    T, H, E, k, C = 50, 40, 7, 3, 12   # 150 pairs into 7 x 12 rows: many drops
+    x = inputs.normal_bf16(11, 0, (T, H))
+    idx = np.stack([np.random.default_rng(t).choice(E, k, replace=False) for t in range(T)]).astype(np.int32)
+    plan = oracle.dispatch(x, idx, E, C, True, fp8=True, fill=0x77)
+    assert plan["rows"] == E * C and np.any(plan["dest"] < 0) and np.all(plan["live"] <= C)
+    q, s = oracle.quantize_rows_e4m3(x)
+    exd, exs = _expected_fp8_rows(q, s, plan["dest"], plan["rows"], 0x77)
+    assert np.array_equal(plan["xd"], exd)
+    assert np.array_equal(plan["xd_scale"].view(np.uint32), exs)
