@@ -480,6 +480,15 @@ class Pool:
                     high_water=s.high_water, spill_high_water=s.spill_high_water, held=s.held,
                     held_high_water=s.held_high_water, num_pages=s.num_pages)
 
+    def stats(self, wait: bool = True) -> dict:
+        """Device pages in use, their high-water mark and spill pages in use
+        (``ap_pool_stats``).  ``wait=False`` touches no GPU and returns the
+        figures of the last synchronising read-out."""
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        check(self.lib.ap_pool_stats(self.handle, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), int(wait)),
+              "pool_stats")
+        return dict(pages_in_use=a.value, high_water=b.value, spill_in_use=c.value)
+
     def rings(self):
         import numpy as np
         ring = np.empty(self.N, np.int32)

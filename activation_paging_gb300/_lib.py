@@ -63,6 +63,7 @@ SIGNATURES = {
     "ap_pool_flags_device_ptr": (i32, [P, P]),
     "ap_overflow_query": (i32, [P, P, i32]),
     "ap_pool_read_state": (i32, [P, P]),
+    "ap_pool_stats": (i32, [P, P, P, P, i32]),
     "ap_pool_read_rings": (i32, [P, P, P]),
     "ap_pool_read_record": (i32, [P, i32, i32, P, P, P, P, i64]),
     "ap_cast_e4m3": (i32, [P, P, i64, P]),

@@ -20,6 +20,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libap.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["common.cu", "route.cu", "dispatch.cu", "combine.cu", "stash.cu", "noalloc.cu", "arena.cu"]
+# bench-only synthetic compute (whole-SM busy blocks for the overlap measurement), not part of libap.so
+BENCH_SOURCES = ["bench/busy.cu"]
+BENCH_LIB = os.path.join(HERE, "libap_bench.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -35,16 +38,17 @@ def _sources():
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if os.path.isfile(os.path.join(CSRC, f))]
+    files += [os.path.join(CSRC, s) for s in BENCH_SOURCES]
     files.append(os.path.join(INCLUDE, "ap.h"))
     files.append(os.path.abspath(__file__))
     return files
 
 
 def stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(BENCH_LIB):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(BENCH_LIB))
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
@@ -58,9 +62,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         flags += ["-Xptxas", "-v"]
     procs = []
     objs = []
-    for src in _sources():
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        objs.append(obj)
+    bench_objs = []
+    for src in _sources() + BENCH_SOURCES:
+        obj = os.path.join(BUILD, src.replace("/", "_").replace(".cu", ".o"))
+        (bench_objs if src in BENCH_SOURCES else objs).append(obj)
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -76,10 +81,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stdout.write(text)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    for lib, lib_objs in ((LIB, objs), (BENCH_LIB, bench_objs)):
+        tmp = lib + f".tmp{os.getpid()}"
+        subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *lib_objs], check=True)
+        os.replace(tmp, lib)
     return LIB
 
 

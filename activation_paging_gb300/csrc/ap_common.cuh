@@ -50,6 +50,25 @@ ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, i
                                     void *scratch, int32_t *dest, cudaStream_t st, const void *x = nullptr,
                                     int64_t x_rb = 0);
 
+// ---- NVTX ranges ---------------------------------------------------------------
+// Every entry point that enqueues GPU work or waits on the GPU opens a range
+// named after itself (domain "activation_paging") for the length of the host
+// call, so a trace of a step attributes each call's launches and waits to
+// route, dispatch, push, pop or combine.  AP_NVTX=0 in the environment turns
+// the ranges off; without a tool attached a range costs one call into an
+// empty stub.
+class NvtxRange {
+  public:
+    explicit NvtxRange(const char *name);
+    ~NvtxRange();
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+
+  private:
+    bool on_;
+};
+#define AP_NVTX_RANGE(name) ::ap::NvtxRange ap_nvtx_range_(name)
+
 #define AP_CHECK_LAUNCH(what)                                   \
     do {                                                        \
         cudaError_t e_ = cudaGetLastError();                    \

@@ -90,6 +90,7 @@ struct ap_arena {
 
 extern "C" ap_status ap_arena_create(ap_arena **out, int64_t max_bytes, int32_t device)
 {
+    AP_NVTX_RANGE("ap_arena_create");
     if (!out) return fail(AP_EINVAL, "arena_create: out is NULL");
     *out = nullptr;
     if (max_bytes <= 0) return fail(AP_EINVAL, "arena_create: max_bytes must be > 0");
@@ -121,6 +122,7 @@ extern "C" ap_status ap_arena_create(ap_arena **out, int64_t max_bytes, int32_t 
 
 extern "C" ap_status ap_arena_grow(ap_arena *a, int64_t bytes)
 {
+    AP_NVTX_RANGE("ap_arena_grow");
     if (!a) return fail(AP_EINVAL, "arena_grow: NULL arena");
     if (bytes < 0 || (size_t)bytes > a->reserved)
         return fail(AP_EINVAL, "arena_grow: %lld bytes outside the %lld reserved", (long long)bytes,
@@ -164,6 +166,7 @@ extern "C" ap_status ap_arena_info(const ap_arena *a, void **base, int64_t *mapp
 
 extern "C" ap_status ap_arena_destroy(ap_arena *a)
 {
+    AP_NVTX_RANGE("ap_arena_destroy");
     if (!a) return AP_OK;
     const Vmm &v = vmm();
     ap_status s = AP_OK;

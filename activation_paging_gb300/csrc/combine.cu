@@ -336,6 +336,7 @@ extern "C" ap_status ap_combine_backward(const void *dout, const void *y, int64_
                                          const int32_t *dest, const float *w, int64_t T, int32_t k, void *dy,
                                          float *dw, uint32_t *d_status, void *stream)
 {
+    AP_NVTX_RANGE("ap_combine_backward");
     using namespace ap;
     if (T < 0 || H < 1 || k < 1 || k > 32 || y_rows < 0)
         return fail(AP_EINVAL, "combine_backward: bad sizes T=%lld H=%d k=%d", (long long)T, H, k);
@@ -359,6 +360,7 @@ extern "C" ap_status ap_combine_backward(const void *dout, const void *y, int64_
 extern "C" ap_status ap_dispatch_backward(const void *dxd, int64_t rows, int32_t H, const int32_t *dest, int64_t T,
                                           int32_t k, void *dx, uint32_t *d_status, void *stream)
 {
+    AP_NVTX_RANGE("ap_dispatch_backward");
     using namespace ap;
     if (T < 0 || H < 1 || k < 1 || k > 32 || rows < 0)
         return fail(AP_EINVAL, "dispatch_backward: bad sizes T=%lld H=%d k=%d", (long long)T, H, k);
@@ -383,6 +385,7 @@ extern "C" ap_status ap_dispatch_backward(const void *dxd, int64_t rows, int32_t
 extern "C" ap_status ap_combine_unpermute(const void *y, int64_t y_rows, int32_t H, const int32_t *dest, const float *w,
                                           int64_t T, int32_t k, void *out, uint32_t *d_status, void *stream)
 {
+    AP_NVTX_RANGE("ap_combine_unpermute");
     using namespace ap;
     if (T < 0 || H < 1 || k < 1 || k > 32 || y_rows < 0)
         return fail(AP_EINVAL, "combine_unpermute: bad sizes T=%lld H=%d k=%d", (long long)T, H, k);

@@ -2,7 +2,12 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <atomic>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "ap_common.cuh"
 
@@ -31,6 +36,35 @@ ap_status cuda_fail(cudaError_t e, const char *what)
 {
     set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
     return AP_ECUDA;
+}
+
+static nvtxDomainHandle_t nvtx_domain()
+{
+    // created once, on first use; nullptr when AP_NVTX=0
+    static const nvtxDomainHandle_t d = [] {
+        const char *env = getenv("AP_NVTX");
+        if (env && strcmp(env, "0") == 0) return (nvtxDomainHandle_t) nullptr;
+        return nvtxDomainCreateA("activation_paging");
+    }();
+    return d;
+}
+
+NvtxRange::NvtxRange(const char *name) : on_(false)
+{
+    nvtxDomainHandle_t d = nvtx_domain();
+    if (!d) return;
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(d, &a);
+    on_ = true;
+}
+
+NvtxRange::~NvtxRange()
+{
+    if (on_) nvtxDomainRangePop(nvtx_domain());
 }
 
 static std::atomic<uint64_t> g_launches{0};

@@ -525,6 +525,7 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
                                          int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
                                          int64_t scratch_bytes, uint32_t *d_status, void *stream)
 {
+    AP_NVTX_RANGE("ap_dispatch_permute");
     using namespace ap;
     if (out_dtype != AP_DTYPE_BF16 && out_dtype != AP_DTYPE_E4M3)
         return fail(AP_EINVAL, "dispatch_permute: unknown out_dtype %d", out_dtype);
@@ -576,6 +577,7 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
 
 extern "C" ap_status ap_cast_e4m3(const float *in, uint8_t *out, int64_t n, void *stream)
 {
+    AP_NVTX_RANGE("ap_cast_e4m3");
     using namespace ap;
     if (n < 0) return fail(AP_EINVAL, "cast_e4m3: n < 0");
     if (n == 0) return AP_OK;

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(256) k_route_topk(const float *__restrict__ lo
 extern "C" ap_status ap_route_topk(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
                                    void *stream)
 {
+    AP_NVTX_RANGE("ap_route_topk");
     using namespace ap;
     if (T < 0 || T >= (int64_t(1) << 31) || E < 1 || E > 1024 || k < 1 || k > E || k > 32)
         return fail(AP_EINVAL, "route_topk: bad sizes T=%lld E=%d k=%d", (long long)T, E, k);

@@ -753,6 +753,8 @@ struct ap_pool {
     uint64_t next_id = 1;
     void *pinned = nullptr; // small pinned host buffer for read-outs
     uint32_t last_flags = 0;
+    ap_pool_state last_state{}; // the last synchronising read-out of the state block (ap_pool_stats)
+    bool have_state = false;
     cudaEvent_t copy_before = nullptr, copy_after = nullptr; // ap_pool_time_copies
 };
 
@@ -862,6 +864,7 @@ extern "C" ap_status ap_pool_required_bytes(const ap_pool_config *cfg, int64_t *
 extern "C" ap_status ap_pool_init(ap_pool **out, const ap_pool_config *cfg, void *dev_pool, void *dev_meta,
                                   void *host_spill, void *paging_stream)
 {
+    AP_NVTX_RANGE("ap_pool_init");
     if (!out) return fail(AP_EINVAL, "pool_init: out is NULL");
     *out = nullptr;
     ap_status s = check_config(cfg);
@@ -920,6 +923,7 @@ extern "C" ap_status ap_pool_init(ap_pool **out, const ap_pool_config *cfg, void
 
 extern "C" ap_status ap_pool_reset(ap_pool *p, void *stream)
 {
+    AP_NVTX_RANGE("ap_pool_reset");
     if (!p) return fail(AP_EINVAL, "pool_reset: NULL pool");
     if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "pool_reset: not the paging stream");
     for (int32_t s = 0; s < p->cfg.num_slots; ++s) {
@@ -943,6 +947,7 @@ extern "C" ap_status ap_pool_reset(ap_pool *p, void *stream)
 
 extern "C" ap_status ap_pool_grow(ap_pool *p, int64_t num_pages, void *dev_pool, void *stream)
 {
+    AP_NVTX_RANGE("ap_pool_grow");
     if (!p) return fail(AP_EINVAL, "pool_grow: NULL pool");
     if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "pool_grow: not the paging stream");
     const int64_t n0 = p->cfg.num_pages, nmax = ap::max_pages_of(p->cfg);
@@ -1003,6 +1008,7 @@ extern "C" ap_status ap_stash_push(ap_pool *p, int32_t slot, int32_t nplanes, co
                                    const int32_t *d_seg_off, const int32_t *d_live, uint64_t *record_id,
                                    void *stream)
 {
+    AP_NVTX_RANGE("ap_stash_push");
     if (!p) return fail(AP_EINVAL, "stash_push: NULL pool");
     if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "stash_push: not the paging stream");
     if (slot < 0 || slot >= p->cfg.num_slots) return fail(AP_EINVAL, "stash_push: slot %d out of range", slot);
@@ -1176,6 +1182,7 @@ extern "C" ap_status ap_dispatch_stash(ap_pool *p, int32_t slot, const void *x, 
                                        int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
                                        uint64_t *record_id, void *stream)
 {
+    AP_NVTX_RANGE("ap_dispatch_stash");
     return dispatch_stash_impl(p, slot, nullptr, nullptr, x, T, H, const_cast<int32_t *>(idx), k, E, capacity,
                                padded, out_dtype, xd, xd_scale, xd_rows, counts, live, seg_off, dest, src_tok,
                                scratch, scratch_bytes, d_status, record_id, stream);
@@ -1189,6 +1196,7 @@ extern "C" ap_status ap_route_dispatch_stash(ap_pool *p, int32_t slot, const flo
                                              int64_t scratch_bytes, uint32_t *d_status, uint64_t *record_id,
                                              void *stream)
 {
+    AP_NVTX_RANGE("ap_route_dispatch_stash");
     if (T > 0 && !logits) return ap::fail(AP_EINVAL, "route_dispatch_stash: NULL logits");
     static const float kNoLogits = 0.f; // T == 0: nothing to route, still the routing variant
     return dispatch_stash_impl(p, slot, logits ? logits : &kNoLogits, w, x, T, H, idx, k, E, capacity, padded,
@@ -1199,6 +1207,7 @@ extern "C" ap_status ap_route_dispatch_stash(ap_pool *p, int32_t slot, const flo
 extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, void *const *dst_planes,
                                   int64_t dst_rows, uint64_t *record_id, void *stream)
 {
+    AP_NVTX_RANGE("ap_stash_pop");
     if (!p) return fail(AP_EINVAL, "stash_pop: NULL pool");
     if (static_cast<cudaStream_t>(stream) != p->stream) return fail(AP_ESTREAM, "stash_pop: not the paging stream");
     if (slot < 0 || slot >= p->cfg.num_slots) return fail(AP_EINVAL, "stash_pop: slot %d out of range", slot);
@@ -1251,6 +1260,7 @@ extern "C" ap_status ap_pool_flags_device_ptr(const ap_pool *p, uint32_t **d_fla
 
 extern "C" ap_status ap_overflow_query(ap_pool *p, uint32_t *flags, int32_t wait)
 {
+    AP_NVTX_RANGE("ap_overflow_query");
     if (!p || !flags) return fail(AP_EINVAL, "overflow_query: NULL argument");
     if (wait) {
         ap_status s = sync_read(p, p->pinned, &reinterpret_cast<ap_pool_state *>(p->dev_meta)->flags, 4);
@@ -1263,16 +1273,38 @@ extern "C" ap_status ap_overflow_query(ap_pool *p, uint32_t *flags, int32_t wait
 
 extern "C" ap_status ap_pool_read_state(ap_pool *p, ap_pool_state *state)
 {
+    AP_NVTX_RANGE("ap_pool_read_state");
     if (!p || !state) return fail(AP_EINVAL, "pool_read_state: NULL argument");
     ap_status s = sync_read(p, p->pinned, p->dev_meta, sizeof(ap_pool_state));
     if (s != AP_OK) return s;
     memcpy(state, p->pinned, sizeof(ap_pool_state));
     p->last_flags = state->flags;
+    p->last_state = *state;
+    p->have_state = true;
+    return AP_OK;
+}
+
+extern "C" ap_status ap_pool_stats(ap_pool *p, int64_t *pages_in_use, int64_t *high_water, int64_t *spill_in_use,
+                                   int32_t wait)
+{
+    AP_NVTX_RANGE("ap_pool_stats");
+    if (!p) return fail(AP_EINVAL, "pool_stats: NULL pool");
+    if (wait) {
+        ap_pool_state st;
+        ap_status s = ap_pool_read_state(p, &st);
+        if (s != AP_OK) return s;
+    }
+    const ap_pool_state &st = p->last_state;
+    const bool h = p->have_state; // zeros before the first read-out
+    if (pages_in_use) *pages_in_use = h ? st.num_pages - (int64_t)(st.tail - st.head) : 0;
+    if (high_water) *high_water = h ? st.high_water : 0;
+    if (spill_in_use) *spill_in_use = h ? p->cfg.spill_pages - (int64_t)(st.spill_tail - st.spill_head) : 0;
     return AP_OK;
 }
 
 extern "C" ap_status ap_pool_read_rings(ap_pool *p, int32_t *ring, int32_t *spill_ring)
 {
+    AP_NVTX_RANGE("ap_pool_read_rings");
     if (!p || !ring) return fail(AP_EINVAL, "pool_read_rings: NULL argument");
     ap_status s = sync_read(p, ring, p->dev_meta + p->M.ring, 4 * (size_t)p->cfg.num_pages);
     if (s == AP_OK && spill_ring && p->cfg.spill_pages > 0)
@@ -1283,6 +1315,7 @@ extern "C" ap_status ap_pool_read_rings(ap_pool *p, int32_t *ring, int32_t *spil
 extern "C" ap_status ap_pool_read_record(ap_pool *p, int32_t slot, int32_t qpos, ap_record_info *info,
                                          int32_t *page_table, int64_t *row0, int32_t *nrows, int64_t cap)
 {
+    AP_NVTX_RANGE("ap_pool_read_record");
     if (!p) return fail(AP_EINVAL, "pool_read_record: NULL pool");
     if (slot < 0 || slot >= p->cfg.num_slots || qpos < 0 || qpos >= p->q_count[slot])
         return fail(AP_EINVAL, "pool_read_record: no record at slot %d position %d", slot, qpos);

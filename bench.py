@@ -61,8 +61,12 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["qwen3_moe", "skewed", "spill", "dsv2_lite_fp8", "dsv2_lite_fp8_h2056"],
                     help="qwen3_moe (default) is the benchmark; the others time that workload's stash schedule")
-    ap.add_argument("--overlap", action="store_true",
-                    help="also measure reload (pop) overlapped with a bf16 GEMM on another stream")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="skip the reload-overlap measurements (pops beside a bf16 GEMM on another stream, and "
+                         "beside whole-SM busy blocks that leave a known number of SMs free)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other workloads' stash schedules (skewed, FP8 layer stack at H=2048 and "
+                         "H=2056, host spill) in the default run")
     ap.add_argument("--backward", action="store_true",
                     help="also time the backward pair (combine backward, dispatch backward) on the step's shapes")
     ap.add_argument("--calibrate", action="store_true",
@@ -102,6 +106,33 @@ def barrier(world: int):
 def whole_job_rate(units_per_rank: float, world: int, max_seconds: float) -> float:
     """Units processed by all ranks divided by the slowest rank's time."""
     return units_per_rank * world / max_seconds
+
+
+def hold_gpu(stream, seconds: float):
+    """Enqueue a sleep kernel of about `seconds` on `stream`, so that the host
+    enqueues the calls behind it before the GPU reaches them.  The events
+    around each call then time the GPU's work on the call (its kernels back
+    to back), not the host's launch latency between them."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(seconds * 2.1e9))  # cycles at the highest SM clock: at least `seconds`
+
+
+def timed_passes(run_pass, stream, passes: int):
+    """Run `passes` eager passes with per-call events, each behind a hold long
+    enough for the host to enqueue the whole pass first."""
+    import torch
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    run_pass(None)  # host time of one pass (warm)
+    host_s = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    events = {}
+    for _ in range(passes):
+        hold_gpu(stream, 2.0 * host_s + 2e-3)
+        run_pass(events)
+    torch.cuda.synchronize()
+    return events
 
 
 # ----------------------------------------------------------------------------------
@@ -494,14 +525,10 @@ def overlap_report(step, device, grid_bounds=(64, 152, 304, 608, 1216, 2048), re
             torch.matmul(a, b, out=c)
 
     def push_all():
-        with torch.cuda.stream(paging):
-            for h, d in step.chunks:
-                step.pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"], d["disp"]["live"])
+        push_records(step)
 
     def pop_all():
-        with torch.cuda.stream(paging):
-            for h, d in step.chunks:
-                step.pool.pop(0, [d["dst"]])
+        pop_records(step)
 
     saved = step.pool.max_ctas
     gemm()
@@ -553,6 +580,110 @@ def overlap_report(step, device, grid_bounds=(64, 152, 304, 608, 1216, 2048), re
     step.pool.max_ctas = saved
     torch.cuda.synchronize(device)
     return out
+
+
+def sm_split_report(step, device, free_sms=(0, 8, 19, 38, 76, 114), reps=7, busy_ms=1.0):
+    """Exposed reload time when the compute leaves a known number of SMs free.
+
+    A GEMM's blocks fill every SM, so reloads beside it mostly run between
+    its blocks rather than beside them.  Here the compute is synthetic
+    (bench-only libap_bench.so): whole-SM busy blocks, each holding one SM for
+    about `busy_ms`, on all but f SMs; the step's pops start on the paging
+    stream just after them.  For each f: the busy blocks alone, the reloads
+    alone, both together, the exposed time (both - busy alone) and the
+    reloads' own duration beside the busy blocks."""
+    import ctypes
+    import torch
+    from activation_paging_gb300 import build as cuda_build
+    lib = ctypes.CDLL(cuda_build.BENCH_LIB)
+    lib.apb_busy_sms.restype = ctypes.c_int
+    lib.apb_busy_sms.argtypes = [ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_void_p]
+    nsm = torch.cuda.get_device_properties(device).multi_processor_count
+    compute = torch.cuda.Stream(device=device, priority=0)
+    paging = step.stream
+    sink = torch.zeros(nsm, dtype=torch.float32, device=device)
+    scrub_buf = torch.ones(256 << 20, device=device, dtype=torch.float16)  # 512 MB, four times L2
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def busy(n, iters):
+        rc = lib.apb_busy_sms(n, iters, sink.data_ptr(), compute.cuda_stream)
+        if rc:
+            raise RuntimeError(f"busy-block launch failed with CUDA error {rc}")
+
+    def timed(stream, fn):
+        a, b = ev(), ev()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b)
+
+    def scrub():
+        with torch.cuda.stream(compute):
+            scrub_buf.sum()
+        torch.cuda.synchronize(device)
+
+    # iterations for about busy_ms
+    probe = 20000
+    busy(nsm, probe)
+    t = timed(compute, lambda: busy(nsm, probe))
+    iters = max(1000, int(probe * busy_ms / max(t, 1e-3)))
+    saved = step.pool.max_ctas
+    step.pool.max_ctas = 0  # the default grid bound
+    samples = {f: ([], [], [], []) for f in free_sms if f < nsm}
+    for _ in range(reps):
+        for f, (t_busy, t_pop, t_both, t_beside) in samples.items():
+            n = nsm - f
+            scrub()
+            t_busy.append(timed(compute, lambda: busy(n, iters)))
+            push_records(step)
+            scrub()
+            t_pop.append(timed(paging, lambda: pop_records(step)))
+            push_records(step)
+            scrub()
+            b0, p0, done, b1 = ev(), ev(), ev(), ev()
+            b0.record(compute)
+            busy(n, iters)            # the busy blocks take their SMs first
+            time.sleep(5e-5)
+            paging.wait_event(b0)
+            p0.record(paging)
+            pop_records(step)         # then the reloads, on the SMs left free
+            done.record(paging)
+            compute.wait_event(done)  # late wait
+            b1.record(compute)
+            torch.cuda.synchronize(device)
+            t_both.append(b0.elapsed_time(b1))
+            t_beside.append(p0.elapsed_time(done))
+    step.pool.max_ctas = saved
+    out = {"compute": f"whole-SM busy blocks (1024 threads, all shared memory) on all but f of {nsm} SMs, "
+                      f"{iters} iterations (about {busy_ms} ms)",
+           "reload": f"{len(step.chunks)} pops of the step on the high-priority paging stream, default grid bound",
+           "method": f"median of {reps} rounds; each part after an L2 scrub with nothing else in flight; the "
+                     "reloads are enqueued about 50 us after the busy blocks",
+           "by_free_sms": {}}
+    for f, (t_busy, t_pop, t_both, t_beside) in samples.items():
+        mb, mp, mboth, mbes = (statistics.median(v) for v in (t_busy, t_pop, t_both, t_beside))
+        out["by_free_sms"][str(f)] = {"busy_ms": round(mb, 4), "reload_ms": round(mp, 4),
+                                      "both_ms": round(mboth, 4), "exposed_ms": round(max(0.0, mboth - mb), 4),
+                                      "reload_beside_ms": round(mbes, 4),
+                                      "hidden_frac": round(min(1.0, 1 - max(0.0, mboth - mb) / mp), 3)}
+    return out
+
+
+def push_records(step):
+    """Stash every chunk's dispatch rows again (on the paging stream)."""
+    import torch
+    with torch.cuda.stream(step.stream):
+        for h, d in step.chunks:
+            step.pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"], d["disp"]["live"])
+
+
+def pop_records(step):
+    """Reload every chunk's record (on the paging stream)."""
+    import torch
+    with torch.cuda.stream(step.stream):
+        for h, d in step.chunks:
+            step.pool.pop(0, [d["dst"]])
 
 
 class ScheduleStep:
@@ -751,6 +882,94 @@ def link_bound(st, link, peak, pass_s, device):
             "note": "bound = HBM bytes / HBM copy peak + spilled bytes / pinned-copy link rate, each way"}
 
 
+def measure_schedule(wl, device, passes=None, op_passes=1, warmup=3, target_s=0.4):
+    """One other workload's whole stash schedule as one CUDA graph: graph
+    replays timed with CUDA events (`passes` of them, or as many as fill about
+    `target_s`), clocks sampled meanwhile, per-call rates from eager passes
+    run behind a hold (so they time the GPU, not the host), and for a
+    workload with host spill the bound of its host link.  Returns the
+    workload's result dict; the pool and buffers are released before it
+    returns."""
+    import torch
+    st = ScheduleStep(wl, device)
+    try:
+        for _ in range(max(warmup, 3)):
+            st.run()
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        n0 = st.ap.launch_count()
+        with torch.cuda.graph(g, stream=st.stream):
+            st.run()
+        launches_per_pass = st.ap.launch_count() - n0  # library kernels one replay runs
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st.stream)
+        for _ in range(2):
+            with torch.cuda.stream(st.stream):
+                g.replay()
+        b.record(st.stream)
+        torch.cuda.synchronize(device)
+        if passes is None:
+            est = a.elapsed_time(b) / 2e3
+            passes = int(min(400, max(3, target_s / max(est, 1e-6))))
+        sampler = ClockSampler(device.index or 0)
+        time.sleep(0.3)
+        a.record(st.stream)
+        for _ in range(passes):
+            with torch.cuda.stream(st.stream):
+                g.replay()
+        b.record(st.stream)
+        torch.cuda.synchronize(device)
+        clocks = sampler.stop()
+        el = a.elapsed_time(b) / 1e3
+        del g
+        events = timed_passes(lambda ev: st.run(ev), st.stream, max(1, op_passes))
+        peaks = measured_peaks()
+        peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
+        ops = ops_table(events, st.bytes, peak)
+        flags = st.pool.overflow()
+        link = st.spilled_bytes() if wl.spill_pages else 0
+        bound = link_bound(st, link, peak, el / passes, device) if link else None
+        pass_bytes = sum(st.bytes["route"] + st.bytes["dispatch_stash"] if op == "push"
+                         else st.bytes["pop"] + st.bytes["combine"] for op, _ in st.sched)
+        ideal_s = pass_bytes / (peak * 1e9)
+        res = {"value": round(st.tokens * passes / el, 1), "unit": "tokens/s", "ms_per_pass": round(el * 1e3 / passes, 4),
+               "passes": passes, "tokens_per_pass": st.tokens, "bytes_per_pass": int(pass_bytes),
+               "ideal_ms_per_pass": round(ideal_s * 1e3, 4), "frac_of_ideal": round(ideal_s / (el / passes), 4),
+               "rows_kept_per_record": round(st.rows_kept, 1), "host_link_bytes_per_pass": link,
+               "config": {"T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "capacity": wl.capacity, "padded": wl.padded,
+                          "fp8": wl.fp8, "page_tokens": wl.page_tokens, "num_pages": wl.num_pages,
+                          "spill_pages": wl.spill_pages, "records_per_pass": sum(1 for op, _ in st.sched
+                                                                                 if op == "push")},
+               "ops": ops, "pool_flags": flags, "gpu_launches_per_pass": launches_per_pass, "clocks": clocks}
+        if bound:
+            res["link_bound"] = bound
+        return res
+    finally:
+        st.pool.close()
+        del st
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+
+
+OTHER_WORKLOADS = ("skewed", "dsv2_lite_fp8", "dsv2_lite_fp8_h2056", "spill")
+
+
+def workloads_report(device):
+    """The other workloads of the method, each timed as one CUDA graph of its
+    whole stash schedule (measure_schedule)."""
+    from activation_paging_gb300 import inputs
+    out = {}
+    for name in OTHER_WORKLOADS:
+        out[name] = measure_schedule(inputs.WORKLOADS[name], device)
+    out["note"] = ("each workload's whole schedule replayed as one CUDA graph (every push the fused dispatch + push); "
+                   "value = tokens pushed per pass / pass time; frac_of_ideal = algorithmic bytes of the pass at the "
+                   "measured HBM copy peak / pass time; ops = per-call CUDA-event times from eager passes behind a "
+                   "hold (GPU time of each call, not host launch time), copy_* = the call's copy kernel alone; "
+                   "the spill workload is bound by the host link (link_bound)")
+    return out
+
+
 def native_schedule(args):
     """Time one other workload's schedule (graph replay) and its per-call rates."""
     import torch
@@ -760,52 +979,11 @@ def native_schedule(args):
     device = torch.device("cuda", 0)
     cuda_build.build()
     wl = inputs.WORKLOADS[args.workload]
-    st = ScheduleStep(wl, device)
-    for _ in range(max(args.warmup, 3)):
-        st.run()
-    torch.cuda.synchronize(device)
-    g = torch.cuda.CUDAGraph()
-    n0 = st.ap.launch_count()
-    with torch.cuda.graph(g, stream=st.stream):
-        st.run()
-    launches_per_pass = st.ap.launch_count() - n0  # library kernels one replay runs
-    for _ in range(2):
-        with torch.cuda.stream(st.stream):
-            g.replay()
-    torch.cuda.synchronize(device)
-    steps = max(1, args.steps)
-    sampler = ClockSampler(0)
-    time.sleep(0.3)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(st.stream)
-    for _ in range(steps):
-        with torch.cuda.stream(st.stream):
-            g.replay()
-    b.record(st.stream)
-    torch.cuda.synchronize(device)
-    clocks = sampler.stop()
-    el = a.elapsed_time(b) / 1e3
-    events = {}
-    for _ in range(max(1, min(args.op_steps, steps))):
-        st.run(events)
-    torch.cuda.synchronize(device)
-    peaks = measured_peaks()
-    peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
-    ops = ops_table(events, st.bytes, peak)
-    flags = st.pool.overflow()
-    link = st.spilled_bytes() if wl.spill_pages else 0
-    bound = link_bound(st, link, peak, el / steps, device) if link else None
-    line = {"metric": METRIC, "workload": wl.name, "value": round(st.tokens * steps / el, 1), "unit": "tokens/s",
-            "rows_kept_per_record": round(st.rows_kept, 1), "host_link_bytes_per_step": link,
-            "ms_per_step": round(el * 1e3 / steps, 4), "steps": steps, "tokens_per_step": st.tokens,
-            "config": {"T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "capacity": wl.capacity, "padded": wl.padded,
-                       "fp8": wl.fp8, "page_tokens": wl.page_tokens, "num_pages": wl.num_pages,
-                       "spill_pages": wl.spill_pages, "schedule": [f"{op} {n}" for op, n in st.sched][:12]},
-            "ops": ops, "pool_flags": flags, "gpu_launches": launches_per_pass * steps, "clocks": clocks,
-            "note": "ops: mean CUDA-event time per call over eager passes; pops of spilled records read host memory"}
-    if bound:
-        line["link_bound"] = bound
+    res = measure_schedule(wl, device, passes=max(1, args.steps), op_passes=max(1, min(args.op_steps, args.steps)),
+                           warmup=args.warmup)
+    line = {"metric": METRIC, "workload": wl.name, **res,
+            "note": "ops: CUDA-event time per call over eager passes behind a hold; pops of spilled records read "
+                    "host memory"}
     print(json.dumps(line), flush=True)
 
 
@@ -929,12 +1107,10 @@ def native(args):
     max_elapsed = aggregate_max(elapsed, world)
     value = whole_job_rate(tokens_per_step * args.steps, world, max_elapsed)
 
-    # per-call times: eager steps with CUDA events around every call
-    events = {}
+    # per-call times: eager steps with CUDA events around every call, each
+    # step behind a hold so the events time the GPU, not the host's launches
     op_steps = max(1, min(args.op_steps, args.steps))
-    for _ in range(op_steps):
-        step.run(events, fused=fused_main)
-    torch.cuda.synchronize(device)
+    events = timed_passes(lambda ev: step.run(ev, fused=fused_main), step.stream, op_steps)
 
     # the other step variant (fused <-> separate dispatch and push), for comparison
     alt = None
@@ -983,6 +1159,19 @@ def native(args):
                 "note": (f"achieved = the call's algorithmic bytes / mean CUDA-event time of its copy kernel, events "
                          f"recorded by the library on the paging stream around the kernel, over {op_steps} eager "
                          f"steps; the whole call (with its plan kernels) is under ops")}
+    if timed and kcall in ("dispatch_stash",):
+        # the count/rank launch before the copy prefetches the token rows x into
+        # L2, so the copy kernel reads most of x from L2: its fraction without
+        # those bytes, and the whole call's (count/rank, scan + plan, copy)
+        x_bytes = wl.T * wl.H * 2
+        kb = step.bytes[kcall] - x_bytes
+        roofline["frac_without_prefetched_x"] = round(kb / (ops[dom]["copy_ms"] / 1e3) / 1e9 / peak, 4)
+        roofline["bytes_without_prefetched_x"] = kb
+        roofline["call_frac"] = ops[dom]["frac"]
+        roofline["call_note"] = (f"frac counts all {step.bytes[kcall]} algorithmic bytes against the copy kernel, "
+                                 f"including the {x_bytes} bytes of token rows the count/rank launch prefetched into "
+                                 f"L2; frac_without_prefetched_x leaves them out; call_frac is the whole {dom} call "
+                                 f"(routing, count/rank, scan + plan and the copy) over its own bytes")
 
     e2e = None
     if not args.no_e2e:
@@ -1015,9 +1204,25 @@ def native(args):
                "note": "inputs copied from pinned host memory and output copied back inside the timed region, "
                        "pipelined per chunk on separate copy streams"}
 
-    overlap = overlap_report(step, device) if args.overlap else None
+    launched_as = ("eager" if graph is None else
+                   "CUDA graph of one step, replayed" + ("" if (args.serial or not fused_main)
+                                                         else "; chunk 1 routing and chunk 0 combine on a second "
+                                                              "stream"))
+    overlap = None
+    if not args.no_overlap and world == 1:
+        overlap = {"beside_gemm": overlap_report(step, device), "sm_split": sm_split_report(step, device)}
     calibration = calibration_report(step, device) if args.calibrate and world == 1 else None
     backward = backward_report(step, device) if args.backward else None
+
+    workloads = None
+    if not args.no_workloads and world == 1:
+        del graph
+        graph = None
+        step.pool.close()
+        del step
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+        workloads = workloads_report(device)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1034,14 +1239,11 @@ def native(args):
                            "hbm_gbs_step": round(total_bytes / (ms_per_step / 1e3) / 1e9, 1),
                            "l2": "working set per step ~1.4 GB > 126 MB L2: no flush",
                            "parallelism": f"replicas x{world}", "stream": "one high-priority stream",
-                           "launch": ("eager" if graph is None else
-                                      "CUDA graph of one step, replayed" + ("" if (args.serial or not fused_main)
-                                                                            else "; chunk 1 routing and chunk 0 "
-                                                                                 "combine on a second stream")),
+                           "launch": launched_as,
                            "step": ("route, fused dispatch + push, pop, combine per chunk" if fused_main
                                     else "route, dispatch, push, pop, combine per chunk")},
                 "roofline": roofline, "ops": ops, "alt": alt, "cpu_baseline": cpu, "e2e": e2e, "overlap": overlap,
-                "calibration": calibration, "backward": backward,
+                "calibration": calibration, "backward": backward, "workloads": workloads,
                 "gpu_launches": timed_launches,
                 "clocks": clocks}
         print(json.dumps(line), flush=True)

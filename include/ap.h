@@ -157,7 +157,9 @@ ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H,
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any stream
- * capture.  All calls share the one array, so calls that overlap on the GPU
+ * capture.  The cached address belongs to the device's context: after
+ * cudaDeviceReset the next call looks it up again in the new context (make
+ * that call, too, before any capture).  All calls share the one array, so calls that overlap on the GPU
  * (on different streams without ordering between them) race: order them on
  * one stream or with events.  Contents left by a previous call do not matter;
  * every entry a call reads is first written by that call.
@@ -439,6 +441,20 @@ ap_status ap_pool_flags_device_ptr(const ap_pool *pool, uint32_t **d_flags);
 ap_status ap_overflow_query(ap_pool *pool, uint32_t *flags, int32_t wait);
 /* Whole state block (synchronises). */
 ap_status ap_pool_read_state(ap_pool *pool, ap_pool_state *state);
+/* Pool occupancy, read outside the CUDA callable like the overflow flags
+ * (torchtitan pull 5541, "AI-Generated Details", last paragraph: overflow
+ * and pool state are handled later, not inside the copy).
+ *   pages_in_use  device pages taken and not yet returned
+ *                 (num_pages - free device pages)
+ *   high_water    most device pages ever in use since the last reset
+ *   spill_in_use  spill pages taken and not yet returned
+ * wait = 1 synchronises the paging stream and reads the state block;
+ * wait = 0 touches no GPU and returns the figures of the last synchronising
+ * read-out (ap_pool_stats with wait = 1, or ap_pool_read_state), zeros
+ * before the first.  Any of the three pointers may be NULL. */
+ap_status ap_pool_stats(ap_pool *pool, int64_t *pages_in_use,
+                        int64_t *high_water, int64_t *spill_in_use,
+                        int32_t wait);
 /* Free rings: ring [num_pages now] int32 and spill_ring [spill_pages] int32
  * (host, written; spill_ring may be NULL).  Synchronises. */
 ap_status ap_pool_read_rings(ap_pool *pool, int32_t *ring,

@@ -154,6 +154,9 @@ def test_pool_calls_reject_null_pool(lib):
     assert lib.ap_pool_destroy(None) == 0
     f = ctypes.c_uint32()
     assert lib.ap_overflow_query(None, ctypes.byref(f), 0) == -1
+    n = ctypes.c_int64()
+    assert lib.ap_pool_stats(None, ctypes.byref(n), None, None, 0) == -1
+    assert lib.ap_pool_stats(None, None, None, None, 1) == -1
 
 
 def test_product_package_never_imports_the_oracle():

@@ -109,11 +109,15 @@ def test_fused_host_errors():
     assert rc == -5  # not the paging stream
 
 
+# Two warps per token, each holding half the row's 16-byte vectors (8 bf16):
+# a row of H values is H/8 vectors, warp 0 takes the first ceil(H/16).
 @pytest.mark.parametrize("T,H,E,k,P,N,SP", [
-    (4096, 2048, 64, 6, 128, 120, 0),    # the FP8 layer-stack shape (register path, 8 vectors per lane)
-    (999, 2056, 64, 6, 128, 40, 64),     # odd hidden size, ragged tail, spill
-    (300, 1024, 16, 4, 32, 20, 4),       # 4 vectors per lane; lost pages
-    (175000, 64, 64, 6, 128, 8300, 100),  # a record of 1.05 M pairs; spills
+    (4096, 2048, 64, 6, 128, 120, 0),    # the FP8 layer-stack shape: 128 vectors per warp, 4 per lane
+    (999, 2056, 64, 6, 128, 40, 64),     # odd hidden size: 129 / 128 vectors (a fifth round on one lane); spill
+    (300, 1024, 16, 4, 32, 20, 4),       # 64 vectors per warp, 2 per lane; lost pages
+    (600, 4096, 32, 4, 32, 100, 16),     # the widest rows: 256 vectors per warp, 8 per lane; spill
+    (700, 2312, 48, 5, 64, 70, 40),      # 145 / 144 vectors: the 8-per-lane kernel with ragged rounds; spill
+    (175000, 64, 64, 6, 128, 8300, 100),  # a record of 1.05 M pairs, 4 vectors per warp; spills
 ])
 def test_fused_e4m3_matches_oracle(T, H, E, k, P, N, SP):
     rb = (H, 4)

@@ -183,3 +183,36 @@ def test_cast_e4m3_matches_oracle_encoder():
     got = host(ap.cast_e4m3(to_dev(allv)))
     exp = oracle.e4m3_encode(allv)
     assert np.array_equal(got, exp)
+
+
+def test_cast_e4m3_matches_oracle_encoder_1e8():
+    """The E4M3 conversion the FP8 dispatch uses against the oracle's own
+    encoder on about 10^8 floats, in chunks: random signs, exponents and
+    mantissas across and beyond the format's range (2^-14 .. 2^10), scaled
+    normals, values next to every rounding midpoint, and arbitrary finite bit
+    patterns."""
+    rnd = np.random.default_rng(7)
+    mags = [oracle.e4m3_decode_one(c) for c in range(0x7F)]
+    mids = np.array([(a + b) / 2 for a, b in zip(mags[:-1], mags[1:])], np.float32)
+    chunk = 1 << 24
+    total = 0
+    for i in range(6):
+        if i < 2:  # uniform exponent over the format's range and a little beyond
+            sign = rnd.integers(0, 2, chunk, dtype=np.uint32) << 31
+            expo = (rnd.integers(-14, 11, chunk) + 127).astype(np.uint32) << 23
+            mant = rnd.integers(0, 1 << 23, chunk, dtype=np.uint32)
+            v = (sign | expo | mant).view(np.float32)
+        elif i < 4:  # normals over six decades
+            v = (rnd.standard_normal(chunk) * 10.0 ** rnd.uniform(-3, 3, chunk)).astype(np.float32)
+        elif i == 4:  # a few float ulps around every midpoint
+            m = mids[rnd.integers(0, mids.size, chunk)]
+            v = (m.view(np.int32) + rnd.integers(-3, 4, chunk).astype(np.int32)).view(np.float32)
+            v = np.where(rnd.integers(0, 2, chunk) == 1, -v, v).astype(np.float32)
+        else:  # any finite bit pattern
+            v = rnd.integers(0, 2 ** 32, chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+            v = v[np.isfinite(v)]
+        got = host(ap.cast_e4m3(to_dev(v)))
+        exp = oracle.e4m3_encode(v)
+        assert np.array_equal(got, exp), i
+        total += v.size
+    assert total > 10 ** 8 * 0.99

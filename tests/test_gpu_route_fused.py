@@ -111,3 +111,43 @@ def test_route_dispatch_stash_host_errors():
                                        idx.data_ptr(), 2, 8, 0, 0, 0, None, None, 64, None, None, None, None, None,
                                        None, 0, None, None, torch.cuda.Stream().cuda_stream)
     assert rc == -5  # not the paging stream
+
+
+def test_route_dispatch_stash_headline_shape_matches_oracle():
+    """Route + fused dispatch + push at the benchmark's chunk shape (T=8192,
+    H=2048, E=128, top-8, dropless, 64-token pages, the benchmark's pool)
+    against the oracle: ids exact, weights within the derived bound, every
+    dispatch output, the record's page table and descriptors, the pool state,
+    and every page's rows."""
+    wl = inputs.WORKLOADS["qwen3_moe"]
+    T, H, E, k, P = wl.T, wl.H, wl.E, wl.k, wl.page_tokens
+    rb = 2 * H
+    g = ap.Pool(P, wl.page_bytes, wl.num_pages, 1, 4, E, wl.num_pages, fill=FILL)
+    o = oracle.Pool(P, wl.page_bytes, wl.num_pages, 1, 4, E, wl.num_pages, 0, keep_bytes=False)
+    logits = inputs.router_logits(0, T, E)
+    x = inputs.normal_bf16(0, inputs.X_STREAM, (T, H))
+    idx_o, w_o = oracle.route_topk(logits, k)
+    plan = oracle.dispatch(x, idx_o, E, 0, False)
+    o.push_rb(0, (rb,), plan["rows"], plan["seg_off"], plan["live"])
+    with torch.cuda.stream(g.stream):
+        g.stream.wait_stream(torch.cuda.default_stream())
+        d = g.route_dispatch_stash(0, to_dev(logits), bf16_to_dev(x), k, E)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(d["idx"]), idx_o)
+    assert np.all(np.abs(host(d["w"]).astype(np.float64) - w_o) <= route_tolerance(logits, idx_o, w_o))
+    for key in ("counts", "live", "seg_off", "dest"):
+        assert np.array_equal(host(d[key]), plan[key]), key
+    assert np.array_equal(host(d["src_tok"])[:plan["rows"]], plan["src_tok"])
+    assert np.array_equal(bf16_to_host(d["xd"]), plan["xd"])
+    assert g.state() == o.state()
+    a, b = g.record(0), o.record(0)
+    for key in ("npages", "ndev", "nspill", "nlost"):
+        assert a[key] == b[key], key
+    for key in ("page_table", "row0", "nrows"):
+        assert np.array_equal(a[key], b[key]), key
+    # every page holds the dispatched rows it was given (the oracle's rows, checked above)
+    xd_bytes = d["xd"].view(torch.uint8).reshape(plan["rows"], rb)
+    for pid, r0, nr in zip(a["page_table"].tolist(), a["row0"].tolist(), a["nrows"].tolist()):
+        assert 0 <= pid < g.N
+        page = g.pool[pid * wl.page_bytes: pid * wl.page_bytes + nr * rb]
+        assert torch.equal(page, xd_bytes[r0:r0 + nr].reshape(-1))

@@ -62,6 +62,14 @@ class Twin:
     def check(self, images=False):
         sg, so = self.g.state(), self.o.state()
         assert sg == so, (sg, so)
+        # occupancy read-out: the oracle's ring counters, and the pages its queued records hold
+        held_dev = sum(self.o.record(s, q)["ndev"] for s in range(self.S) for q in range(self.o.queue_len(s)))
+        held_sp = sum(self.o.record(s, q)["nspill"] for s in range(self.S) for q in range(self.o.queue_len(s)))
+        want = dict(pages_in_use=so["num_pages"] - (so["tail"] - so["head"]), high_water=so["high_water"],
+                    spill_in_use=self.o.SP - (so["spill_tail"] - so["spill_head"]))
+        assert want["pages_in_use"] == held_dev and want["spill_in_use"] == held_sp
+        assert self.g.stats() == want
+        assert self.g.stats(wait=False) == want  # the same figures, without touching the GPU
         rg, sgr = self.g.rings()
         ro, sro = self.o.rings()
         assert np.array_equal(rg, ro)
@@ -276,3 +284,23 @@ def test_page_size_extremes(P, rb, N, SP):
                 assert int(rec["npages"]) == int(live.sum())  # one page per live row
         t.check()
     t.check(images=True)
+
+
+def test_pool_stats_wait_and_cached_readouts():
+    """ap_pool_stats: zeros before any read-out; wait = 0 returns the last
+    synchronising read-out (it does not see later pushes); wait = 1 reads the
+    current occupancy, which matches the oracle."""
+    P, rb = 4, (32,)
+    t = Twin(P, rb, N=10, S=1, R=4, segs=4, SP=6)
+    assert t.g.stats(wait=False) == dict(pages_in_use=0, high_water=0, spill_in_use=0)
+    src = rows_np(5, 48, rb[0])
+    t.push(0, [src], [0, 16, 32], [16, 9, 16])  # 4 + 3 + 4 = 11 pages: 10 device, 1 spill
+    t.check()
+    first = t.g.stats(wait=False)
+    assert first == dict(pages_in_use=10, high_water=10, spill_in_use=1)
+    t.pop(0, [src.shape])
+    assert t.g.stats(wait=False) == first  # no read-out since the pop
+    assert t.g.stats() == dict(pages_in_use=0, high_water=10, spill_in_use=0)
+    t.g.reset()
+    t.o.reset()
+    assert t.g.stats() == dict(pages_in_use=0, high_water=0, spill_in_use=0)

@@ -86,7 +86,7 @@ def test_noalloc_refuses_sizes_beyond_its_work_space():
     lib = ap.lib()
     dummy = torch.empty(16, dtype=torch.int32, device="cuda")
     p = _p(dummy)
-    T, E, k = 1 << 20, 1024, 8  # (T/256)*E*4 bytes = 16 MiB > 1 MiB
+    T, E, k = 1 << 20, 1024, 8  # (T/64)*E*4 bytes = 64 MiB > 1 MiB (count/rank blocks of 64 tokens)
     rc = lib.ap_dispatch_permute_noalloc(p, T, 64, p, k, E, 0, 0, 0, p, None, T * k, p, p, p, p, None, None, None)
     assert rc == -1
     assert b"work space" in lib.ap_last_error()
