@@ -456,6 +456,14 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
                                                             int tiles_per_page)
 {
     pdl_begin();
+    // The first tile's descriptor and page id are loaded together with the
+    // record header, before the page count is known: the grid never exceeds
+    // the record's page bound times the tiles per page, and that bound is at
+    // most the page-table capacity, so the entry exists (it is used only if
+    // the tile turns out to be live).
+    int64_t tile = blockIdx.x;
+    PageDesc d = rec.desc[tile / tiles_per_page];
+    int64_t id = rec.page_table[tile / tiles_per_page];
     const int64_t npages = rec.hdr->npages;
     const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
     if (blockIdx.x == 0) {
@@ -488,32 +496,78 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
         }
     }
     const int64_t tiles = npages * tiles_per_page;
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    for (; tile < tiles; tile += gridDim.x) {
         const int64_t ord = tile / tiles_per_page;
         const int sub = (int)(tile - ord * tiles_per_page);
-        const PageDesc d = rec.desc[ord];
+        const PageDesc cur = d;
+        const int64_t cur_id = id;
+        // the next tile's metadata, in flight while this tile copies
+        const int64_t next = tile + gridDim.x;
+        if (next < tiles) {
+            d = rec.desc[next / tiles_per_page];
+            id = rec.page_table[next / tiles_per_page];
+        }
         const int64_t r0 = (int64_t)sub * rows_per_tile;
-        if (r0 >= d.nrows) continue;
-        const int64_t nr = (d.nrows - r0 < rows_per_tile) ? d.nrows - r0 : rows_per_tile;
-        const int64_t id = rec.page_table[ord];
-        const bool ok = (ord < ndev) ? (id >= 0 && id < ps.N)
-                                     : (ord < ndev + nspill) ? (id >= ps.SB && id < ps.SB + ps.SP) : (id == -1);
+        if (r0 >= cur.nrows) continue;
+        const int64_t nr = (cur.nrows - r0 < rows_per_tile) ? cur.nrows - r0 : rows_per_tile;
+        const bool ok = (ord < ndev) ? (cur_id >= 0 && cur_id < ps.N)
+                                     : (ord < ndev + nspill) ? (cur_id >= ps.SB && cur_id < ps.SB + ps.SP)
+                                                             : (cur_id == -1);
         if (!ok) {
             if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_CORRUPT);
             continue;
         }
-        if (id < 0) continue;
-        if (d.row0 + d.nrows > dst_rows) {
+        if (cur_id < 0) continue;
+        if (cur.row0 + cur.nrows > dst_rows) {
             if (threadIdx.x == 0) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
             continue;
         }
-        const uint8_t *page = page_addr(ps, id);
+        const uint8_t *page = page_addr(ps, cur_id);
 #pragma unroll
         for (int p = 0; p < 2; ++p)
             if (p < dst.n)
-                block_copy(dst.p[p] + (d.row0 + r0) * dst.rb[p], page + dst.page_off[p] + r0 * dst.rb[p],
+                block_copy(dst.p[p] + (cur.row0 + r0) * dst.rb[p], page + dst.page_off[p] + r0 * dst.rb[p],
                            nr * dst.rb[p]);
     }
+}
+
+// A pair's dispatch row and, for a kept pair, its place in the record being
+// pushed, from the in-block rank k_count_rank left in dest and the block
+// bases the scan left in blk (as finalize_dest), in two dependent batches of
+// loads: the rank and the expert id, then everything that depends only on
+// the expert (block base, segment offset, the record's live count and first
+// page ordinal).  The pair's row within its expert segment is its rank.
+// Writes the final dest and, for a kept pair, src_tok.
+struct PairPlace {
+    int32_t d;   // dispatch row, or -1
+    int64_t r;   // row within the expert segment (kept pairs)
+    int64_t ord; // page ordinal in the record, or -1 (dropped, or past the record's live rows)
+    int64_t lv;  // live rows of the expert segment in the record
+};
+
+__device__ __forceinline__ PairPlace resolve_pair(const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
+                                                  int32_t *__restrict__ src_tok, const int32_t *__restrict__ blk,
+                                                  const int32_t *__restrict__ seg_off, const RecPtr &rec,
+                                                  int64_t t, int j, int k, int E, int capacity, int P)
+{
+    PairPlace pp{-1, 0, -1, 0};
+    const int64_t p = t * k + j;
+    const int32_t lr = dest[p];
+    const int e = idx[p];
+    if (lr < 0 || e < 0 || e >= E) return pp; // an invalid expert id: dest is already -1
+    const int32_t base = blk[(t / kTokPerBlk) * E + e];
+    const int32_t so = seg_off[e];
+    const int64_t lv = rec.live[e], pg0 = rec.pg_base[e];
+    const int32_t r = base + lr;
+    if (capacity <= 0 || r < capacity) {
+        pp.d = so + r;
+        if (src_tok) src_tok[pp.d] = (int32_t)t;
+        pp.r = r;
+        pp.lv = lv;
+        if (r < lv) pp.ord = pg0 + r / P;
+    }
+    dest[p] = pp.d;
+    return pp;
 }
 
 // Fused dispatch + push: one warp per token reads its BF16 row once and writes
@@ -542,30 +596,23 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
         int32_t my_d = -1;
         uint8_t *my_page = nullptr; // where this lane's pair lands in the pool (row start), or null
         if (lane < k) {
-            my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
-            const int e = idx[t * k + lane];
-            if (my_d >= 0 && e >= 0 && e < E) {
-                const int64_t so = rec.seg_off[e], lv = rec.live[e];
-                const int64_t r = (int64_t)my_d - so; // row within the expert segment
-                if (r >= 0 && r < lv) {
-                    const int64_t ord = rec.pg_base[e] + r / P;
-                    if (ord < npages) {
-                        bool corrupt;
-                        const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
-                        if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                        if (r % P == 0) { // row 0 of the page records it and its descriptor
-                            rec.page_table[ord] = (int32_t)id;
-                            PageDesc pd;
-                            pd.row0 = so + r;
-                            pd.nrows = (int32_t)(lv - r < P ? lv - r : P);
-                            pd.pad = 0;
-                            rec.desc[ord] = pd;
-                        }
-                        if (id >= 0) {
-                            uint8_t *page = page_addr(ps, id);
-                            my_page = page + (r % P) * rb;
-                        }
-                    }
+            const PairPlace pp = resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+            my_d = pp.d;
+            if (pp.ord >= 0 && pp.ord < npages) {
+                bool corrupt;
+                const int64_t id = pushed_page_id(ps, pp.ord, ndev, nspill, head0, sh0, &corrupt);
+                if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+                if (pp.r % P == 0) { // row 0 of the page records it and its descriptor
+                    rec.page_table[pp.ord] = (int32_t)id;
+                    PageDesc pd;
+                    pd.row0 = pp.d;
+                    pd.nrows = (int32_t)(pp.lv - pp.r < P ? pp.lv - pp.r : P);
+                    pd.pad = 0;
+                    rec.desc[pp.ord] = pd;
+                }
+                if (id >= 0) {
+                    uint8_t *page = page_addr(ps, id);
+                    my_page = page + (pp.r % P) * rb;
                 }
             }
         }
@@ -649,31 +696,24 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
         if (h == 0) {
             uint8_t *my_row = nullptr;
             if (lane < k) {
-                my_d = finalize_dest(idx, dest, src_tok, blk, seg_off, t, lane, k, E, capacity);
-                const int e = idx[t * k + lane];
-                if (my_d >= 0 && e >= 0 && e < E) {
-                    const int64_t so = rec.seg_off[e], lv = rec.live[e];
-                    const int64_t r = (int64_t)my_d - so;
-                    if (r >= 0 && r < lv) {
-                        const int64_t ord = rec.pg_base[e] + r / P;
-                        if (ord < npages) {
-                            bool corrupt;
-                            const int64_t id = pushed_page_id(ps, ord, ndev, nspill, head0, sh0, &corrupt);
-                            if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
-                            if (r % P == 0) { // row 0 of the page records it and its descriptor
-                                rec.page_table[ord] = (int32_t)id;
-                                PageDesc pd;
-                                pd.row0 = so + r;
-                                pd.nrows = (int32_t)(lv - r < P ? lv - r : P);
-                                pd.pad = 0;
-                                rec.desc[ord] = pd;
-                            }
-                            if (id >= 0) {
-                                uint8_t *page = page_addr(ps, id);
-                                my_row = page + (r % P) * H;
-                                my_scale = reinterpret_cast<float *>(page + plane1_off + (r % P) * 4);
-                            }
-                        }
+                const PairPlace pp = resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+                my_d = pp.d;
+                if (pp.ord >= 0 && pp.ord < npages) {
+                    bool corrupt;
+                    const int64_t id = pushed_page_id(ps, pp.ord, ndev, nspill, head0, sh0, &corrupt);
+                    if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+                    if (pp.r % P == 0) { // row 0 of the page records it and its descriptor
+                        rec.page_table[pp.ord] = (int32_t)id;
+                        PageDesc pd;
+                        pd.row0 = pp.d;
+                        pd.nrows = (int32_t)(pp.lv - pp.r < P ? pp.lv - pp.r : P);
+                        pd.pad = 0;
+                        rec.desc[pp.ord] = pd;
+                    }
+                    if (id >= 0) {
+                        uint8_t *page = page_addr(ps, id);
+                        my_row = page + (pp.r % P) * H;
+                        my_scale = reinterpret_cast<float *>(page + plane1_off + (pp.r % P) * 4);
                     }
                 }
             }
@@ -1129,10 +1169,9 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     h.bound_pages = bound;
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
-    ap::launch(ap::k_scan_plan, 1, ap::kPlanThreads, 0, st, static_cast<int32_t *>(scratch), dispatch_blocks(T), E, capacity,
-                                                    padded, counts, live, seg_off, stt, rec, xd_rows,
-                                                    p->cfg.page_tokens, p->cfg.max_pages_per_record,
-                                                    p->cfg.num_pages, p->cfg.spill_pages);
+    ap::launch(ap::k_scan_plan, 1, ap::kPlanThreads, 0, st, static_cast<int32_t *>(scratch), dispatch_blocks(T), E,
+               capacity, padded, counts, live, seg_off, stt, rec, xd_rows, p->cfg.page_tokens,
+               p->cfg.max_pages_per_record, p->cfg.num_pages, p->cfg.spill_pages);
     AP_CHECK_LAUNCH("dispatch_stash scan + plan launch");
     if (T > 0) {
         const int64_t want = (T + 7) / 8;
@@ -1158,12 +1197,10 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
 #undef AP_LAUNCH_E4M3
         } else if ((al & 15) == 0)
             ap::launch(ap::k_dispatch_stash_copy<int4>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,
-                                                                  seg_off, src_tok, xo, stt, rec, ps,
-                                                                  p->cfg.page_tokens);
+                       seg_off, src_tok, xo, stt, rec, ps, p->cfg.page_tokens);
         else
             ap::launch(ap::k_dispatch_stash_copy<int2>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,
-                                                                  seg_off, src_tok, xo, stt, rec, ps,
-                                                                  p->cfg.page_tokens);
+                       seg_off, src_tok, xo, stt, rec, ps, p->cfg.page_tokens);
         AP_CHECK_LAUNCH("dispatch_stash copy launch");
         mark(p, p->copy_after);
     }
