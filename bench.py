@@ -119,19 +119,26 @@ def hold_gpu(stream, seconds: float):
 
 
 def timed_passes(run_pass, stream, passes: int):
-    """Run `passes` eager passes with per-call events, each behind a hold long
-    enough for the host to enqueue the whole pass first."""
+    """Run eager passes with per-call events, each behind a hold long enough
+    for the host to enqueue the whole pass first.  `passes` passes time the
+    whole calls; as many more time the pool calls' copy kernels alone (the
+    library records events right around them, which would cut the
+    programmatic launch between a call's plan and copy kernels, so those
+    passes do not time whole calls)."""
     import torch
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     run_pass(None)  # host time of one pass (warm)
     host_s = time.perf_counter() - t0
     torch.cuda.synchronize()
-    events = {}
-    for _ in range(passes):
-        hold_gpu(stream, 2.0 * host_s + 2e-3)
-        run_pass(events)
+    events = {"__copy__": False}
+    for copy in (False, True):
+        events["__copy__"] = copy
+        for _ in range(passes):
+            hold_gpu(stream, 2.0 * host_s + 2e-3)
+            run_pass(events)
     torch.cuda.synchronize()
+    del events["__copy__"]
     return events
 
 
@@ -251,18 +258,20 @@ class Step:
                 return
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
-            pool_call = name in COPY_KERNEL
-            if pool_call:  # also time the call's copy kernel alone
+            # in copy passes the library also times the pool call's copy kernel alone
+            pool_call = name in COPY_KERNEL and events.get("__copy__", False)
+            if pool_call:
                 ca = torch.cuda.Event(enable_timing=True)
                 cb = torch.cuda.Event(enable_timing=True)
                 self.pool.time_copies(ca, cb)
             a.record(s)
             fn()
             b.record(s)
-            events.setdefault(name, []).append((a, b))
             if pool_call:
                 self.pool.time_copies(None, None)
                 events.setdefault(name + ":copy", []).append((ca, cb))
+            else:
+                events.setdefault(name, []).append((a, b))
 
         with torch.cuda.stream(s):
             for c, (h, d) in enumerate(self.chunks):
@@ -824,18 +833,20 @@ class ScheduleStep:
                 return
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
-            pool_call = name in COPY_KERNEL
-            if pool_call:  # also time the call's copy kernel alone
+            # in copy passes the library also times the pool call's copy kernel alone
+            pool_call = name in COPY_KERNEL and events.get("__copy__", False)
+            if pool_call:
                 ca = torch.cuda.Event(enable_timing=True)
                 cb = torch.cuda.Event(enable_timing=True)
                 self.pool.time_copies(ca, cb)
             a.record(s)
             fn()
             b.record(s)
-            events.setdefault(name, []).append((a, b))
             if pool_call:
                 self.pool.time_copies(None, None)
                 events.setdefault(name + ":copy", []).append((ca, cb))
+            else:
+                events.setdefault(name, []).append((a, b))
 
         with torch.cuda.stream(s):
             for op, name in self.sched:

@@ -113,6 +113,7 @@ def test_fused_host_errors():
 # a row of H values is H/8 vectors, warp 0 takes the first ceil(H/16).
 @pytest.mark.parametrize("T,H,E,k,P,N,SP", [
     (4096, 2048, 64, 6, 128, 120, 0),    # the FP8 layer-stack shape: 128 vectors per warp, 4 per lane
+    (4096, 2056, 64, 6, 128, 120, 0),    # its non-divisible variant: 129 / 128 vectors
     (999, 2056, 64, 6, 128, 40, 64),     # odd hidden size: 129 / 128 vectors (a fifth round on one lane); spill
     (300, 1024, 16, 4, 32, 20, 4),       # 64 vectors per warp, 2 per lane; lost pages
     (600, 4096, 32, 4, 32, 100, 16),     # the widest rows: 256 vectors per warp, 8 per lane; spill
