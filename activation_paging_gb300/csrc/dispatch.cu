@@ -119,11 +119,23 @@ __device__ __forceinline__ void prefetch_rows_l2(RowPrefetch pf, int64_t t0, int
 }
 
 // Count/rank blocks of kTokPerBlk tokens reading idx from global memory.
+// snap_src / snap_dst (a fused dispatch + push whose copy kernel plans the
+// record itself): block 0 copies the pool's free-ring counters (head, tail,
+// spill head, spill tail) into the record header (head0, spill_head0,
+// tail0, spill_tail0) after its wait, when no kernel changes them.
 __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
                                                              int32_t *__restrict__ blk, int32_t *__restrict__ dest,
-                                                             uint32_t *d_status, RowPrefetch pf)
+                                                             uint32_t *d_status, RowPrefetch pf,
+                                                             const uint64_t *snap_src, uint64_t *snap_dst)
 {
     pdl_begin();
+    if (snap_dst && blockIdx.x == 0 && threadIdx.x == 0) {
+        const uint64_t head = snap_src[0], tail = snap_src[1], sh = snap_src[2], stl = snap_src[3];
+        snap_dst[0] = head;
+        snap_dst[1] = sh;
+        snap_dst[2] = tail;
+        snap_dst[3] = stl;
+    }
     {
         const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
         prefetch_rows_l2(pf, t0, (T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
@@ -459,13 +471,14 @@ static RowPrefetch row_prefetch(const void *x, int64_t x_rb)
 }
 
 ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
-                              uint32_t *d_status, cudaStream_t st, const void *x, int64_t x_rb)
+                              uint32_t *d_status, cudaStream_t st, const void *x, int64_t x_rb,
+                              const uint64_t *snap_src, uint64_t *snap_dst)
 {
     const int64_t nb = nblocks(T);
     if (nb == 0) return AP_OK;
     const size_t smem = (size_t)kRankWarps * E * sizeof(int32_t);
     launch(k_count_rank, (unsigned)nb, kRankThreads, smem, st, idx, T, k, E, static_cast<int32_t *>(scratch), dest,
-                                                           d_status, row_prefetch(x, x_rb));
+           d_status, row_prefetch(x, x_rb), snap_src, snap_dst);
     AP_CHECK_LAUNCH("dispatch count/rank launch");
     return AP_OK;
 }

@@ -16,7 +16,12 @@
 // A fused dispatch + push (k_scan_plan, then k_dispatch_stash_copy or its
 // E4M3 form) plans the same way but leaves the page descriptors to the copy
 // kernel: the pair that holds row 0 of a page writes its descriptor with its
-// page-table entry.
+// page-table entry.  A small record (at most kInlineMaxCounts count/rank
+// block counts) skips k_scan_plan: count/rank copies the free-ring counters
+// into the record header, every copy block derives the expert scan and the
+// page plan it needs from the block counts (inline_plan), and copy block 0
+// writes the dispatch outputs, the record and the pool state (inline_commit)
+// with exactly the values k_scan_plan would write.
 // A push is two launches on the paging stream:
 //   k_push_plan (1 CTA): snapshot live/seg_off, page ordinals by a prefix sum of
 //     ceil(live/P), one (first row, rows) descriptor per page, and the
@@ -47,7 +52,8 @@ struct RecHdr {
     int32_t pad0;
     int64_t npages, ndev, nspill, nlost;
     uint64_t head0, spill_head0;
-    int64_t pad1[9];
+    uint64_t tail0, spill_tail0; // free-ring tails at the push (written with head0 by an inline-planned push)
+    int64_t pad1[7];
 };
 static_assert(sizeof(RecHdr) == 128, "record header layout");
 static_assert(sizeof(ap_pool_state) == 128, "state layout");
@@ -531,6 +537,204 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
     }
 }
 
+// ---- small records: the expert scan and page plan inside the copy kernel -------
+// When the block counts of a record are few (count/rank blocks x experts <=
+// kInlineMaxCounts), every copy block derives what the one-CTA scan + plan
+// kernel would have written, from the count/rank output, in a prologue: its
+// own base rank per expert (the counts of the earlier count/rank blocks), the
+// expert totals, live counts, segment offsets, the record's page ordinals
+// and the allocation (from the free-ring counters count/rank copied into the
+// record header).  Block 0 then writes the dispatch outputs, the record and
+// the pool state; no other block reads those, and the kernel after this one
+// on the paging stream waits for it.  Each block's tokens lie in one
+// count/rank block (its first token is a multiple of its token count, which
+// divides kTokPerBlk) and the grid covers every token in one pass.
+constexpr int kInlineMaxE = 256;
+constexpr int kInlineMaxCounts = 4096;
+
+struct InlineArgs {
+    int enabled; // 0: k_scan_plan ran before the copy
+    int nblk, padded;
+    int32_t *counts, *live; // dispatch outputs (seg_off is the copy kernel's own argument)
+    int64_t src_rows, max_pages;
+};
+
+struct InlinePlan {
+    int32_t base[kInlineMaxE];  // this block's base rank per expert
+    int32_t off[kInlineMaxE];   // segment offsets
+    int32_t lrec[kInlineMaxE];  // the record's live counts (0 for a segment outside the rows)
+    int32_t tot[kInlineMaxE];   // expert totals (counts)
+    int32_t ldisp[kInlineMaxE]; // live = min(count, capacity)
+    int64_t pg[kInlineMaxE + 1];
+    int64_t npages, kept, ndev, nspill;
+    uint64_t head0, sh0, tail0, stail0;
+    uint32_t bad;
+};
+
+// Exclusive scan of v over the threads of a 256-thread block (8 warps);
+// returns the thread's exclusive prefix and *total the block's sum.  ws: 8
+// shared slots, free again when the call returns.
+template <typename V>
+__device__ __forceinline__ V block_exclusive_scan256(V v, V *ws, V *total)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    V x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const V y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[wid] = x;
+    __syncthreads();
+    V before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const V c = ws[w];
+        if (w < wid) before += c;
+        all += c;
+    }
+    __syncthreads();
+    *total = all;
+    return before + x - v;
+}
+
+// The prologue every copy block runs (256 threads).  b: the count/rank block
+// of this block's tokens.  Ends with a barrier: pl is complete for the block.
+__device__ __forceinline__ void inline_plan(InlinePlan &pl, const int32_t *__restrict__ blk, int b, int E,
+                                            int capacity, const InlineArgs &ia, const RecPtr &rec, int P)
+{
+    __shared__ int32_t s_lt[256], s_all[256]; // partial sums: [row group][expert]
+    __shared__ int64_t s_ws[8];
+    const int tid = threadIdx.x;
+    const int nblk = ia.nblk;
+    const int Q = blockDim.x / E; // row groups per expert column (>= 1)
+    const int e = tid % E, q = tid / E;
+    if (tid == 0) {
+        pl.bad = 0;
+        pl.head0 = rec.hdr->head0;
+        pl.sh0 = rec.hdr->spill_head0;
+        pl.tail0 = rec.hdr->tail0;
+        pl.stail0 = rec.hdr->spill_tail0;
+    }
+    // each thread sums one expert column over a strided set of rows: the
+    // counts of the rows before b (this block's base) and of all rows (totals)
+    int32_t lt = 0, all = 0;
+    if (q < Q) {
+        int r = q;
+        for (; r + 15 * Q < nblk; r += 16 * Q) { // sixteen loads in flight (one round for 64 x 64 counts)
+            int32_t c[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) c[u] = blk[(int64_t)(r + u * Q) * E + e];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                all += c[u];
+                if (r + u * Q < b) lt += c[u];
+            }
+        }
+        for (; r < nblk; r += Q) {
+            const int32_t c = blk[(int64_t)r * E + e];
+            all += c;
+            if (r < b) lt += c;
+        }
+        s_lt[q * E + e] = lt;
+        s_all[q * E + e] = all;
+    }
+    __syncthreads();
+    int32_t total = 0, base = 0;
+    if (tid < E) {
+        for (int qq = 0; qq < Q; ++qq) {
+            base += s_lt[qq * E + tid];
+            total += s_all[qq * E + tid];
+        }
+    }
+    const int32_t l = (tid < E) ? ((capacity > 0 && total > capacity) ? capacity : total) : 0;
+    // one scan for both prefix sums: live counts in the high half, pages in
+    // the low half (page totals stay below 2^31, so nothing carries between)
+    const int64_t n0 = (tid < E) ? ((int64_t)l + P - 1) / P : 0;
+    int64_t both_sum;
+    const int64_t both = block_exclusive_scan256<int64_t>(((int64_t)l << 32) | n0, s_ws, &both_sum);
+    const int32_t off = ia.padded ? tid * capacity : (int32_t)(both >> 32);
+    // the record's snapshot of the segment: one outside the rows is not copied
+    // (the fused call's host checks rule that out; the rescan keeps the rule)
+    int32_t lr = l;
+    const bool out = tid < E && (l < 0 || off < 0 || (int64_t)off + (int64_t)l > ia.src_rows);
+    if (out) {
+        atomicOr(&pl.bad, AP_FLAG_BAD_COUNT);
+        lr = 0;
+    }
+    int64_t pg = both & 0xffffffffll, npages = both_sum & 0xffffffffll;
+    if (__syncthreads_or(out)) {
+        const int64_t n = (tid < E) ? ((int64_t)lr + P - 1) / P : 0;
+        pg = block_exclusive_scan256<int64_t>(n, s_ws, &npages);
+    }
+    if (tid < E) {
+        pl.base[tid] = base;
+        pl.off[tid] = off;
+        pl.lrec[tid] = lr;
+        pl.tot[tid] = total;
+        pl.ldisp[tid] = l;
+        pl.pg[tid] = pg;
+    }
+    if (tid == 0) {
+        // the allocation of k_scan_plan: device pages from the ring, then
+        // spill pages, then lost; at most max_pages kept
+        pl.pg[E] = npages;
+        pl.npages = npages;
+        const int64_t kept = npages < ia.max_pages ? npages : ia.max_pages;
+        const int64_t avail = (int64_t)(pl.tail0 - pl.head0);
+        const int64_t savail = (int64_t)(pl.stail0 - pl.sh0);
+        const int64_t ndev = kept < avail ? kept : avail;
+        int64_t nspill = kept - ndev;
+        if (nspill > savail) nspill = savail;
+        pl.kept = kept;
+        pl.ndev = ndev;
+        pl.nspill = nspill;
+    }
+    __syncthreads();
+}
+
+// Block 0 of an inline-planned copy: the dispatch outputs, the record and the
+// pool state, exactly as k_scan_plan writes them.
+__device__ __forceinline__ void inline_commit(const InlinePlan &pl, int E, const InlineArgs &ia,
+                                              int32_t *__restrict__ seg_off, const RecPtr &rec, ap_pool_state *st,
+                                              const PageSpace &ps)
+{
+    const int tid = threadIdx.x;
+    if (tid < E) {
+        ia.counts[tid] = pl.tot[tid];
+        ia.live[tid] = pl.ldisp[tid];
+        seg_off[tid] = pl.off[tid];
+        rec.seg_off[tid] = pl.off[tid];
+        rec.live[tid] = pl.lrec[tid];
+        rec.pg_base[tid] = pl.pg[tid];
+    }
+    if (tid == 0) {
+        rec.pg_base[E] = pl.npages;
+        const int64_t kept = pl.kept, ndev = pl.ndev, nspill = pl.nspill;
+        const int64_t nlost = kept - ndev - nspill;
+        uint32_t f = pl.bad;
+        if (pl.npages > ia.max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
+        if (kept > ndev) f |= AP_FLAG_POOL_OVERFLOW;
+        if (nlost > 0) f |= AP_FLAG_SPILL_OVERFLOW;
+        rec.hdr->nseg = E;
+        rec.hdr->npages = kept;
+        rec.hdr->ndev = ndev;
+        rec.hdr->nspill = nspill;
+        rec.hdr->nlost = nlost;
+        const StateSnap snap = load_state(st);
+        st->head = pl.head0 + (uint64_t)ndev;
+        st->spill_head = pl.sh0 + (uint64_t)nspill;
+        const int64_t in_use = ps.N - (int64_t)(pl.tail0 - (pl.head0 + (uint64_t)ndev));
+        if (in_use > snap.hw) st->high_water = in_use;
+        const int64_t s_use = ps.SP - (int64_t)(pl.stail0 - (pl.sh0 + (uint64_t)nspill));
+        if (s_use > snap.shw) st->spill_high_water = s_use;
+        const int64_t held = snap.held + kept;
+        st->held = held;
+        if (held > snap.hhw) st->held_high_water = held;
+        st->flags = snap.flags | f;
+    }
+}
+
 // A pair's dispatch row and, for a kept pair, its place in the record being
 // pushed, from the in-block rank k_count_rank left in dest and the block
 // bases the scan left in blk (as finalize_dest), in two dependent batches of
@@ -570,6 +774,30 @@ __device__ __forceinline__ PairPlace resolve_pair(const int32_t *__restrict__ id
     return pp;
 }
 
+// resolve_pair for an inline-planned copy: the block base, segment offset,
+// live count and first page ordinal of the pair's expert come from the
+// block's plan in shared memory, so only the rank and the expert id are
+// loaded.
+// lr and e: the pair's in-block rank (dest) and expert id, already loaded.
+__device__ __forceinline__ PairPlace resolve_pair_inline(int32_t lr, int e, int32_t *__restrict__ dest,
+                                                         int32_t *__restrict__ src_tok, const InlinePlan &pl,
+                                                         int64_t t, int j, int k, int E, int capacity, int P)
+{
+    PairPlace pp{-1, 0, -1, 0};
+    const int64_t p = t * k + j;
+    if (lr < 0 || e < 0 || e >= E) return pp; // an invalid expert id: dest is already -1
+    const int32_t r = pl.base[e] + lr;
+    if (capacity <= 0 || r < capacity) {
+        pp.d = pl.off[e] + r;
+        if (src_tok) src_tok[pp.d] = (int32_t)t;
+        pp.r = r;
+        pp.lv = pl.lrec[e];
+        if (r < pp.lv) pp.ord = pl.pg[e] + r / P;
+    }
+    dest[p] = pp.d;
+    return pp;
+}
+
 // Fused dispatch + push: one warp per token reads its BF16 row once and writes
 // it both to the dispatch buffer row dest(t, j) and, for a kept pair, to row
 // (rank mod P) of page pg_base[e] + rank / P of the record (rank = the pair's
@@ -580,23 +808,32 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
                                                              const int32_t *__restrict__ idx,
                                                              int32_t *__restrict__ dest, int k, int E, int capacity,
                                                              const int32_t *__restrict__ blk,
-                                                             const int32_t *__restrict__ seg_off,
+                                                             int32_t *__restrict__ seg_off,
                                                              int32_t *__restrict__ src_tok,
                                                              uint8_t *__restrict__ xd, ap_pool_state *st, RecPtr rec,
-                                                             PageSpace ps, int P)
+                                                             PageSpace ps, int P, InlineArgs ia)
 {
     pdl_begin();
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     const int64_t nvec = rb / (int64_t)sizeof(V);
-    const int64_t npages = rec.hdr->npages;
-    const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
-    const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
+    __shared__ InlinePlan pl;
+    if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
+        inline_plan(pl, blk, (int)(((int64_t)blockIdx.x * (blockDim.x / kWarp)) / kTokPerBlk), E, capacity, ia,
+                    rec, P);
+        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
+    }
+    const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;
+    const int64_t ndev = ia.enabled ? pl.ndev : rec.hdr->ndev, nspill = ia.enabled ? pl.nspill : rec.hdr->nspill;
+    const uint64_t head0 = ia.enabled ? pl.head0 : rec.hdr->head0, sh0 = ia.enabled ? pl.sh0 : rec.hdr->spill_head0;
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
         int32_t my_d = -1;
         uint8_t *my_page = nullptr; // where this lane's pair lands in the pool (row start), or null
         if (lane < k) {
-            const PairPlace pp = resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+            const PairPlace pp =
+                ia.enabled ? resolve_pair_inline(dest[t * k + lane], idx[t * k + lane], dest, src_tok, pl, t, lane, k,
+                                                 E, capacity, P)
+                           : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
             my_d = pp.d;
             if (pp.ord >= 0 && pp.ord < npages) {
                 bool corrupt;
@@ -664,23 +901,28 @@ __device__ __forceinline__ void pair_barrier(int id)
 template <int NRH>
 __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
     const uint16_t *__restrict__ x, int64_t T, int H, const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
-    int k, int E, int capacity, const int32_t *__restrict__ blk, const int32_t *__restrict__ seg_off,
+    int k, int E, int capacity, const int32_t *__restrict__ blk, int32_t *__restrict__ seg_off,
     int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd, float *__restrict__ xd_scale, ap_pool_state *st,
-    RecPtr rec, PageSpace ps, int P, int64_t plane1_off)
+    RecPtr rec, PageSpace ps, int P, int64_t plane1_off, InlineArgs ia)
 {
     pdl_begin();
     constexpr int kPairs = 256 / (2 * kWarp); // warp pairs per block
     __shared__ uint32_t s_amax[2][kPairs][2];
     __shared__ int32_t s_d[2][kPairs][kWarp];
     __shared__ unsigned long long s_prow[2][kPairs][kWarp];
+    __shared__ InlinePlan pl;
     const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
     const int pr = wid >> 1, h = wid & 1;
     const int nstep = H / 8;
     const int half0 = (nstep + 1) / 2;
     const int s_begin = h ? half0 : 0, s_end = h ? nstep : half0;
-    const int64_t npages = rec.hdr->npages;
-    const int64_t ndev = rec.hdr->ndev, nspill = rec.hdr->nspill;
-    const uint64_t head0 = rec.hdr->head0, sh0 = rec.hdr->spill_head0;
+    if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
+        inline_plan(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
+        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
+    }
+    const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;
+    const int64_t ndev = ia.enabled ? pl.ndev : rec.hdr->ndev, nspill = ia.enabled ? pl.nspill : rec.hdr->nspill;
+    const uint64_t head0 = ia.enabled ? pl.head0 : rec.hdr->head0, sh0 = ia.enabled ? pl.sh0 : rec.hdr->spill_head0;
     int buf = 0;
     for (int64_t t = (int64_t)blockIdx.x * kPairs + pr; t < T; t += (int64_t)gridDim.x * kPairs, buf ^= 1) {
         // this half's vectors first: their latency overlaps the lookups below
@@ -696,7 +938,10 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
         if (h == 0) {
             uint8_t *my_row = nullptr;
             if (lane < k) {
-                const PairPlace pp = resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+                const PairPlace pp =
+                    ia.enabled ? resolve_pair_inline(dest[t * k + lane], idx[t * k + lane], dest, src_tok, pl, t,
+                                                     lane, k, E, capacity, P)
+                               : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
                 my_d = pp.d;
                 if (pp.ord >= 0 && pp.ord < npages) {
                     bool corrupt;
@@ -1148,12 +1393,18 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     if (logits && k > E) return fail(AP_EINVAL, "route_dispatch_stash: k=%d > E=%d", k, E);
     if (logits && T > 0 && !w) return fail(AP_EINVAL, "route_dispatch_stash: NULL weights");
     cudaStream_t st = p->stream;
-    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, (int64_t)H * 2)
-               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, (int64_t)H * 2);
-    if (s != AP_OK) return s;
-
     const int32_t pos = (p->q_head[slot] + p->q_count[slot]) % p->cfg.max_records_per_slot;
     const int64_t index = (int64_t)slot * p->cfg.max_records_per_slot + pos;
+    ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
+    ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
+    // few block counts: the copy kernel plans the record itself (no scan + plan launch)
+    const bool inl = !logits && T > 0 && (int64_t)dispatch_blocks(T) * E <= ap::kInlineMaxCounts &&
+                     E <= ap::kInlineMaxE;
+    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, (int64_t)H * 2)
+               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, (int64_t)H * 2,
+                                     inl ? &stt->head : nullptr, inl ? &rec.hdr->head0 : nullptr);
+    if (s != AP_OK) return s;
+
     HostRec &h = p->q[index];
     h.id = p->next_id;
     h.index = index;
@@ -1167,15 +1418,27 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     int64_t bound = E + (xd_rows + P - 1) / P;
     if (bound > p->cfg.max_pages_per_record) bound = p->cfg.max_pages_per_record;
     h.bound_pages = bound;
-    ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
-    ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
-    ap::launch(ap::k_scan_plan, 1, ap::kPlanThreads, 0, st, static_cast<int32_t *>(scratch), dispatch_blocks(T), E,
-               capacity, padded, counts, live, seg_off, stt, rec, xd_rows, p->cfg.page_tokens,
-               p->cfg.max_pages_per_record, p->cfg.num_pages, p->cfg.spill_pages);
-    AP_CHECK_LAUNCH("dispatch_stash scan + plan launch");
+    ap::InlineArgs ia{};
+    if (inl) {
+        ia.enabled = 1;
+        ia.nblk = dispatch_blocks(T);
+        ia.padded = padded;
+        ia.counts = counts;
+        ia.live = live;
+        ia.src_rows = xd_rows;
+        ia.max_pages = p->cfg.max_pages_per_record;
+    } else {
+        ap::launch(ap::k_scan_plan, 1, ap::kPlanThreads, 0, st, static_cast<int32_t *>(scratch), dispatch_blocks(T),
+                   E, capacity, padded, counts, live, seg_off, stt, rec, xd_rows, p->cfg.page_tokens,
+                   p->cfg.max_pages_per_record, p->cfg.num_pages, p->cfg.spill_pages);
+        AP_CHECK_LAUNCH("dispatch_stash scan + plan launch");
+    }
     if (T > 0) {
+        // an inline-planned copy covers every token in one pass (each block's
+        // tokens in one count/rank block); otherwise the grid is capped and
+        // blocks stride over the tokens
         const int64_t want = (T + 7) / 8;
-        const int64_t cap = (int64_t)sm_count() * 16;
+        const int64_t cap = inl ? want : (int64_t)sm_count() * 16;
         const int grid = (int)(want < cap ? want : cap);
         const ap::PageSpace ps = page_space(p);
         const uint8_t *xs = static_cast<const uint8_t *>(x);
@@ -1185,10 +1448,11 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
         if (fp8) {
             const uint16_t *xs16 = static_cast<const uint16_t *>(x);
             const int64_t want2 = (T + 3) / 4; // four tokens (warp pairs) per block
-            const int grid2 = (int)(want2 < cap ? want2 : cap);
+            const int64_t cap2 = inl ? want2 : (int64_t)sm_count() * 16;
+            const int grid2 = (int)(want2 < cap2 ? want2 : cap2);
 #define AP_LAUNCH_E4M3(NRH)                                                                                       \
     ap::launch(ap::k_dispatch_stash_e4m3<NRH>, grid2, 256, 0, st, xs16, T, H, idx, dest, k, E, capacity, blk,       \
-               seg_off, src_tok, xo, xd_scale, stt, rec, ps, p->cfg.page_tokens, page_off[1])
+               seg_off, src_tok, xo, xd_scale, stt, rec, ps, p->cfg.page_tokens, page_off[1], ia)
             if (H <= 512) AP_LAUNCH_E4M3(1);
             else if (H <= 1024) AP_LAUNCH_E4M3(2);
             else if (H <= 2048) AP_LAUNCH_E4M3(4);
@@ -1197,10 +1461,10 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
 #undef AP_LAUNCH_E4M3
         } else if ((al & 15) == 0)
             ap::launch(ap::k_dispatch_stash_copy<int4>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,
-                       seg_off, src_tok, xo, stt, rec, ps, p->cfg.page_tokens);
+                       seg_off, src_tok, xo, stt, rec, ps, p->cfg.page_tokens, ia);
         else
             ap::launch(ap::k_dispatch_stash_copy<int2>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,
-                       seg_off, src_tok, xo, stt, rec, ps, p->cfg.page_tokens);
+                       seg_off, src_tok, xo, stt, rec, ps, p->cfg.page_tokens, ia);
         AP_CHECK_LAUNCH("dispatch_stash copy launch");
         mark(p, p->copy_after);
     }
