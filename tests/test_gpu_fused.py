@@ -177,7 +177,20 @@ def test_launch_counter_counts_enqueued_kernels():
         y = torch.empty_like(d["xd"])
         g.pop(0, [y])
     torch.cuda.synchronize()
-    assert ap.launch_count() - n1 == 4  # count/rank, scan + plan, fused copy, pop copy
+    assert ap.launch_count() - n1 == 3  # a small record: count/rank, fused copy (which plans it), pop copy
+    # a record with more block counts than the copy kernel plans itself (T/64 blocks x E > 4096):
+    # count/rank, scan + plan, fused copy, pop copy
+    T2, E2 = 4160, 64
+    x2 = bf16_to_dev(inputs.normal_bf16(4, inputs.X_STREAM, (T2, H)))
+    idx2 = torch.randint(0, E2, (T2, 2), dtype=torch.int32, device="cuda")
+    g2 = ap.Pool(16, ap.page_bytes_for(16, (2 * H,)), T2 * 2 // 16 + E2, 1, 2, E2)
+    n2 = ap.launch_count()
+    with torch.cuda.stream(g2.stream):
+        g2.stream.wait_stream(torch.cuda.default_stream())
+        d2 = g2.dispatch_stash(0, x2, idx2, E2)
+        g2.pop(0, [torch.empty_like(d2["xd"])])
+    torch.cuda.synchronize()
+    assert ap.launch_count() - n2 == 4
     graph = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -266,3 +279,56 @@ def test_fused_empty_record_matches_oracle(padded):
         assert np.array_equal(host(dst), dst_np[0])
     assert g.state() == o.state()
     assert np.array_equal(host(g.pool), o.pool_bytes())
+
+
+@pytest.mark.parametrize("T,E,fp8", [
+    (512, 16, False),   # a small record: the copy kernel plans it
+    (5000, 64, False),  # 79 count/rank blocks x 64 experts: the scan + plan kernel plans it
+    (600, 32, True),    # E4M3 codes and scales, planned by the copy kernel
+])
+def test_fused_record_overflow_matches_oracle(T, E, fp8):
+    """A record that needs more pages than its page table holds: the first
+    max_pages_per_record pages are kept (device pages, then spill), the rest
+    are dropped and AP_FLAG_RECORD_OVERFLOW is set, exactly as the oracle's
+    push of the same dispatch; the pop brings back the kept pages' rows."""
+    H, k, P, N, SP, maxp = 64, 4, 16, 12, 6, 15
+    rb = (H, 4) if fp8 else (2 * H,)
+    page_bytes = ap.page_bytes_for(P, rb)
+    g = ap.Pool(P, page_bytes, N, 1, 2, E, maxp, SP, fill=FILL)
+    o = oracle.Pool(P, page_bytes, N, 1, 2, E, maxp, SP, keep_bytes=True, fill=FILL)
+    logits = inputs.router_logits(T + 7, T, E)
+    x = inputs.normal_bf16(T + 7, inputs.X_STREAM, (T, H))
+    idx, _ = oracle.route_topk(logits, k)
+    plan = oracle.dispatch(x, idx, E, 0, False, fp8=fp8)
+    if fp8:
+        planes_o = [plan["xd"], plan["xd_scale"].view(np.uint8).reshape(-1, 4)]
+    else:
+        planes_o = [plan["xd"].view(np.uint8).reshape(plan["rows"], 2 * H)]
+    o.push(0, planes_o, plan["rows"], plan["seg_off"], plan["live"])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(g.stream):
+        g.stream.wait_stream(torch.cuda.default_stream())
+        d = g.dispatch_stash(0, bf16_to_dev(x), to_dev(idx), E, fp8=fp8)
+    torch.cuda.synchronize()
+    for key in ("counts", "live", "seg_off", "dest"):
+        assert np.array_equal(host(d[key]), plan[key]), key
+    st = g.state()
+    assert st == o.state()
+    assert st["flags"] & ap.FLAG_RECORD_OVERFLOW
+    a, b = g.record(0), o.record(0)
+    for key in ("npages", "ndev", "nspill", "nlost"):
+        assert a[key] == b[key], key
+    assert a["npages"] == maxp
+    for key in ("page_table", "row0", "nrows"):
+        assert np.array_equal(a[key], b[key]), key
+    assert np.array_equal(host(g.pool), o.pool_bytes())
+    assert np.array_equal(g.spill.numpy(), o.spill_bytes())
+    dq = [np.full(p_.shape, 0x3C, np.uint8) for p_ in planes_o]
+    dg = [to_dev(q_) for q_ in dq]
+    torch.cuda.synchronize()
+    g.pop(0, dg)
+    o.pop(0, dq, plan["rows"])
+    torch.cuda.synchronize()
+    for a_, b_ in zip(dg, dq):
+        assert np.array_equal(host(a_).reshape(b_.shape), b_)
+    assert g.state() == o.state()
