@@ -51,7 +51,8 @@ int dispatch_blocks(int64_t T);
 // are checked by the caller.
 ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
                                     void *scratch, int32_t *dest, cudaStream_t st, const void *x = nullptr,
-                                    int64_t x_rb = 0);
+                                    int64_t x_rb = 0, const uint64_t *snap_src = nullptr,
+                                    uint64_t *snap_dst = nullptr);
 
 // ---- NVTX ranges ---------------------------------------------------------------
 // Every entry point that enqueues GPU work or waits on the GPU opens a range

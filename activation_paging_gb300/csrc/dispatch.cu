@@ -157,9 +157,17 @@ constexpr int kRouteRankWarps = 32;
 template <int NV>
 __global__ void __launch_bounds__(kRouteRankWarps * kWarp) k_route_count_rank(
     const float *__restrict__ logits, int64_t T, int E, int k, int32_t *__restrict__ idx, float *__restrict__ w,
-    int32_t *__restrict__ blk, int32_t *__restrict__ dest, RowPrefetch pf)
+    int32_t *__restrict__ blk, int32_t *__restrict__ dest, RowPrefetch pf, const uint64_t *snap_src,
+    uint64_t *snap_dst)
 {
     pdl_begin();
+    if (snap_dst && blockIdx.x == 0 && threadIdx.x == 0) { // as k_count_rank
+        const uint64_t head = snap_src[0], tail = snap_src[1], sh = snap_src[2], stl = snap_src[3];
+        snap_dst[0] = head;
+        snap_dst[1] = sh;
+        snap_dst[2] = tail;
+        snap_dst[3] = stl;
+    }
     extern __shared__ int32_t smem[]; // cnt [32][E], then the block's ids [kTokPerBlk * k]
     int32_t *cnt = smem;
     int32_t *sidx = smem + kRouteRankWarps * E;
@@ -487,7 +495,8 @@ int dispatch_blocks(int64_t T) { return (int)nblocks(T); }
 
 template <int NV>
 ap_status launch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
-                                  int32_t *blk, int32_t *dest, cudaStream_t st, RowPrefetch pf)
+                                  int32_t *blk, int32_t *dest, cudaStream_t st, RowPrefetch pf,
+                                  const uint64_t *snap_src, uint64_t *snap_dst)
 {
     const size_t smem = ((size_t)kRouteRankWarps * E + (size_t)kTokPerBlk * k) * sizeof(int32_t);
     static const cudaError_t attr = cudaFuncSetAttribute((const void *)k_route_count_rank<NV>,
@@ -496,26 +505,27 @@ ap_status launch_route_count_rank(const float *logits, int64_t T, int32_t E, int
                                                                sizeof(int32_t)));
     if (attr != cudaSuccess) return cuda_fail(attr, "route + count/rank: shared memory limit");
     launch(k_route_count_rank<NV>, (unsigned)nblocks(T), kRouteRankWarps * kWarp, smem, st, logits, T, E, k, idx, w,
-           blk, dest, pf);
+           blk, dest, pf, snap_src, snap_dst);
     AP_CHECK_LAUNCH("route + count/rank launch");
     return AP_OK;
 }
 
 ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
-                                    void *scratch, int32_t *dest, cudaStream_t st, const void *x, int64_t x_rb)
+                                    void *scratch, int32_t *dest, cudaStream_t st, const void *x, int64_t x_rb,
+                                    const uint64_t *snap_src, uint64_t *snap_dst)
 {
     if (nblocks(T) == 0) return AP_OK;
     int32_t *blk = static_cast<int32_t *>(scratch);
     const RowPrefetch pf = row_prefetch(x, x_rb);
-    if (E <= 32) return launch_route_count_rank<1>(logits, T, E, k, idx, w, blk, dest, st, pf);
-    if (E <= 64) return launch_route_count_rank<2>(logits, T, E, k, idx, w, blk, dest, st, pf);
-    if (E <= 128) return launch_route_count_rank<4>(logits, T, E, k, idx, w, blk, dest, st, pf);
-    if (E <= 256) return launch_route_count_rank<8>(logits, T, E, k, idx, w, blk, dest, st, pf);
+    if (E <= 32) return launch_route_count_rank<1>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
+    if (E <= 64) return launch_route_count_rank<2>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
+    if (E <= 128) return launch_route_count_rank<4>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
+    if (E <= 256) return launch_route_count_rank<8>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
     // more than 8 candidates per lane do not fit a 1024-thread block's
     // registers: route and count/rank as two launches
     ap_status s = ap_route_topk(logits, T, E, k, idx, w, st);
     if (s != AP_OK) return s;
-    return dispatch_count_rank(T, idx, k, E, scratch, dest, nullptr, st, x, x_rb);
+    return dispatch_count_rank(T, idx, k, E, scratch, dest, nullptr, st, x, x_rb, snap_src, snap_dst);
 }
 
 ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,

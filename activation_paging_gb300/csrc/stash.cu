@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
 // count/rank block (its first token is a multiple of its token count, which
 // divides kTokPerBlk) and the grid covers every token in one pass.
 constexpr int kInlineMaxE = 256;
-constexpr int kInlineMaxCounts = 4096;
+constexpr int kInlineMaxCounts = 16384;
 
 struct InlineArgs {
     int enabled; // 0: k_scan_plan ran before the copy
@@ -1398,11 +1398,13 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     ap::RecPtr rec = ap::rec_ptr(p->dev_meta, p->M, index);
     ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
     // few block counts: the copy kernel plans the record itself (no scan + plan launch)
-    const bool inl = !logits && T > 0 && (int64_t)dispatch_blocks(T) * E <= ap::kInlineMaxCounts &&
-                     E <= ap::kInlineMaxE;
-    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, (int64_t)H * 2)
-               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, (int64_t)H * 2,
-                                     inl ? &stt->head : nullptr, inl ? &rec.hdr->head0 : nullptr);
+    const bool inl = T > 0 && (int64_t)dispatch_blocks(T) * E <= ap::kInlineMaxCounts && E <= ap::kInlineMaxE;
+    const uint64_t *snap_src = inl ? &stt->head : nullptr;
+    uint64_t *snap_dst = inl ? &rec.hdr->head0 : nullptr;
+    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, (int64_t)H * 2, snap_src,
+                                           snap_dst)
+               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, (int64_t)H * 2, snap_src,
+                                     snap_dst);
     if (s != AP_OK) return s;
 
     HostRec &h = p->q[index];

@@ -178,9 +178,9 @@ def test_launch_counter_counts_enqueued_kernels():
         g.pop(0, [y])
     torch.cuda.synchronize()
     assert ap.launch_count() - n1 == 3  # a small record: count/rank, fused copy (which plans it), pop copy
-    # a record with more block counts than the copy kernel plans itself (T/64 blocks x E > 4096):
+    # a record with more block counts than the copy kernel plans itself (T/64 blocks x E > 16384):
     # count/rank, scan + plan, fused copy, pop copy
-    T2, E2 = 4160, 64
+    T2, E2 = 4160, 256
     x2 = bf16_to_dev(inputs.normal_bf16(4, inputs.X_STREAM, (T2, H)))
     idx2 = torch.randint(0, E2, (T2, 2), dtype=torch.int32, device="cuda")
     g2 = ap.Pool(16, ap.page_bytes_for(16, (2 * H,)), T2 * 2 // 16 + E2, 1, 2, E2)
@@ -283,7 +283,7 @@ def test_fused_empty_record_matches_oracle(padded):
 
 @pytest.mark.parametrize("T,E,fp8", [
     (512, 16, False),   # a small record: the copy kernel plans it
-    (5000, 64, False),  # 79 count/rank blocks x 64 experts: the scan + plan kernel plans it
+    (17000, 64, False),  # 266 count/rank blocks x 64 experts: the scan + plan kernel plans it
     (600, 32, True),    # E4M3 codes and scales, planned by the copy kernel
 ])
 def test_fused_record_overflow_matches_oracle(T, E, fp8):
