@@ -1207,7 +1207,7 @@ def native(args):
     if timed and kcall in ("dispatch_stash",):
         # the count/rank launch before the copy prefetches the token rows x into
         # L2, so the copy kernel reads most of x from L2: its fraction without
-        # those bytes, and the whole call's (count/rank, scan + plan, copy)
+        # those bytes, and the whole call's (routing, count/rank, plan, copy)
         x_bytes = wl.T * wl.H * 2
         kb = step.bytes[kcall] - x_bytes
         roofline["frac_without_prefetched_x"] = round(kb / (ops[dom]["copy_ms"] / 1e3) / 1e9 / peak, 4)
@@ -1216,7 +1216,9 @@ def native(args):
         roofline["call_note"] = (f"frac counts all {step.bytes[kcall]} algorithmic bytes against the copy kernel, "
                                  f"including the {x_bytes} bytes of token rows the count/rank launch prefetched into "
                                  f"L2; frac_without_prefetched_x leaves them out; call_frac is the whole {dom} call "
-                                 f"(routing, count/rank, scan + plan and the copy) over its own bytes")
+                                 f"(routing, count/rank, the plan and the copy) over its own bytes; a record of at "
+                                 f"most 16384 count/rank block counts is planned in the copy kernel's prologue, so "
+                                 f"then the kernel's time includes its plan")
 
     e2e = None
     if not args.no_e2e:
