@@ -1007,6 +1007,199 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
     }
 }
 
+// The same for rows that may start 8 bytes off a 16-byte boundary (H not a
+// multiple of 16, or a base only 8-byte aligned).  A row of H codes is cut into 16-code units (two 16-byte input vectors each) and, when
+// H / 8 is odd, one lone last vector; warp 0 of a warp pair holds the first
+// half of the units, warp 1 the rest, one unit per lane per round (at most
+// NRU rounds).  Each warp also holds the vector just past its units (its
+// lookahead: warp 1's first vector, or the lone last one).  The two warps
+// meet once per token at a named barrier: by then warp 0 has resolved the
+// token's pairs (finalize_dest, page ids, page-table entries and descriptors
+// of a page's row 0) and both have put their half's amax in shared memory
+// (double-buffered by token parity, so a warp that runs ahead never
+// overwrites what its partner still reads).  Both then quantise with the
+// row's scale (same arithmetic as the E4M3 dispatch) and write their units
+// of every kept pair's codes to its dispatch row and page row with 16-byte
+// stores.  Rows are 8-byte aligned; a destination row 8 bytes off a 16-byte
+// boundary gets the aligned 16 bytes that straddle two units (the upper half
+// of one unit and the lower half of the next, taken from the next lane or
+// the lookahead), plus one 8-byte store at its start.  Warp 1 hands its
+// first vector and the lone one to the lookaheads through shared memory at
+// the pair barrier.  Warp 0 writes the scales (dispatch scale and the page's
+// second plane).
+template <int NRU>
+__global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3_units(
+    const uint16_t *__restrict__ x, int64_t T, int H, const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
+    int k, int E, int capacity, const int32_t *__restrict__ blk, int32_t *__restrict__ seg_off,
+    int32_t *__restrict__ src_tok, uint8_t *__restrict__ xd, float *__restrict__ xd_scale, ap_pool_state *st,
+    RecPtr rec, PageSpace ps, int P, int64_t plane1_off, InlineArgs ia)
+{
+    pdl_begin();
+    constexpr int kPairs = 256 / (2 * kWarp); // warp pairs per block
+    __shared__ uint32_t s_amax[2][kPairs][2];
+    __shared__ int32_t s_d[2][kPairs][kWarp];
+    __shared__ unsigned long long s_prow[2][kPairs][kWarp];
+    __shared__ int4 s_look[2][kPairs][2]; // raw vectors for the lookaheads: warp 1's first, the lone one
+    __shared__ InlinePlan pl;
+    const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
+    const int pr = wid >> 1, h = wid & 1;
+    const int nstep = H / 8;                           // 16-byte input vectors of a row
+    const int nu = nstep >> 1, lone = nstep & 1;       // 16-code units; a lone last vector
+    const int u0 = (nu + 1) >> 1;                      // warp 0's units
+    const int ub = h ? u0 : 0, un = h ? nu - u0 : u0; // this warp's first unit and unit count
+    const int la = h ? (lone ? nstep - 1 : -1) : (2 * u0 < nstep ? 2 * u0 : -1); // lookahead vector
+    if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
+        inline_plan(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
+        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
+    }
+    const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;
+    const int64_t ndev = ia.enabled ? pl.ndev : rec.hdr->ndev, nspill = ia.enabled ? pl.nspill : rec.hdr->nspill;
+    const uint64_t head0 = ia.enabled ? pl.head0 : rec.hdr->head0, sh0 = ia.enabled ? pl.sh0 : rec.hdr->spill_head0;
+    const int4 zero = make_int4(0, 0, 0, 0);
+    int buf = 0;
+    for (int64_t t = (int64_t)blockIdx.x * kPairs + pr; t < T; t += (int64_t)gridDim.x * kPairs, buf ^= 1) {
+        // this warp's vectors first: their latency overlaps the lookups below
+        const int4 *row = reinterpret_cast<const int4 *>(x + t * H);
+        int4 v[2 * NRU];
+#pragma unroll
+        for (int i = 0; i < NRU; ++i) {
+            const int w = lane + i * kWarp;
+            v[2 * i] = (w < un) ? ld_stream(row + 2 * (ub + w)) : zero;
+            v[2 * i + 1] = (w < un) ? ld_stream(row + 2 * (ub + w) + 1) : zero;
+        }
+        int32_t my_d = -1;
+        float *my_scale = nullptr;
+        if (h == 0) {
+            uint8_t *my_row = nullptr;
+            if (lane < k) {
+                const PairPlace pp =
+                    ia.enabled ? resolve_pair_inline(dest[t * k + lane], idx[t * k + lane], dest, src_tok, pl, t,
+                                                     lane, k, E, capacity, P)
+                               : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+                my_d = pp.d;
+                if (pp.ord >= 0 && pp.ord < npages) {
+                    bool corrupt;
+                    const int64_t id = pushed_page_id(ps, pp.ord, ndev, nspill, head0, sh0, &corrupt);
+                    if (corrupt) atomicOr(&st->flags, AP_FLAG_CORRUPT);
+                    if (pp.r % P == 0) { // row 0 of the page records it and its descriptor
+                        rec.page_table[pp.ord] = (int32_t)id;
+                        PageDesc pd;
+                        pd.row0 = pp.d;
+                        pd.nrows = (int32_t)(pp.lv - pp.r < P ? pp.lv - pp.r : P);
+                        pd.pad = 0;
+                        rec.desc[pp.ord] = pd;
+                    }
+                    if (id >= 0) {
+                        uint8_t *page = page_addr(ps, id);
+                        my_row = page + (pp.r % P) * H;
+                        my_scale = reinterpret_cast<float *>(page + plane1_off + (pp.r % P) * 4);
+                    }
+                }
+            }
+            s_d[buf][pr][lane] = my_d;
+            s_prow[buf][pr][lane] = (unsigned long long)reinterpret_cast<uintptr_t>(my_row);
+        }
+        uint32_t m = 0;
+        if (h == 1 && lane == 0) { // warp 1 hands its first and lone vectors to the lookaheads
+            if (un > 0) s_look[buf][pr][0] = v[0];
+            if (lone) {
+                const int4 lv = ld_stream(row + nstep - 1);
+                s_look[buf][pr][1] = lv;
+                m = absmax_bf16x2(m, (uint32_t)lv.x);
+                m = absmax_bf16x2(m, (uint32_t)lv.y);
+                m = absmax_bf16x2(m, (uint32_t)lv.z);
+                m = absmax_bf16x2(m, (uint32_t)lv.w);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2 * NRU; ++i) {
+            m = absmax_bf16x2(m, (uint32_t)v[i].x);
+            m = absmax_bf16x2(m, (uint32_t)v[i].y);
+            m = absmax_bf16x2(m, (uint32_t)v[i].z);
+            m = absmax_bf16x2(m, (uint32_t)v[i].w);
+        }
+        const uint32_t half_amax = __reduce_max_sync(0xffffffffu, absmax_bits(m));
+        if (lane == 0) s_amax[buf][pr][h] = half_amax;
+        pair_barrier(1 + pr);
+        const uint32_t a0 = s_amax[buf][pr][0], a1 = s_amax[buf][pr][1];
+        float scale, inv;
+        e4m3_scales(a0 > a1 ? a0 : a1, scale, inv);
+        if (h == 0 && my_d >= 0) {
+            xd_scale[my_d] = scale;
+            if (my_scale) *my_scale = scale;
+        }
+#pragma unroll
+        for (int i = 0; i < 2 * NRU; ++i) { // codes replace the values in place (first 8 bytes)
+            const int2 c = quantize8_e4m3(v[i], inv);
+            v[i].x = c.x;
+            v[i].y = c.y;
+        }
+        // warp 0's lookahead is warp 1's first vector, or the lone one when
+        // warp 1 has no unit; warp 1's is the lone one
+        const int4 lav = (lane == 0 && la >= 0) ? s_look[buf][pr][(h == 1 || 2 * u0 == nstep - 1) ? 1 : 0] : zero;
+        const int2 lc = quantize8_e4m3(lav, inv);
+        const int la_x = __shfl_sync(0xffffffffu, lc.x, 0), la_y = __shfl_sync(0xffffffffu, lc.y, 0);
+        int2 nx[NRU];
+        // for a row 8 bytes off: the lower half of the unit after this lane's
+        // (next lane, lane 0 of the next round, or the lookahead)
+#pragma unroll
+        for (int i = 0; i < NRU; ++i) {
+            int nxx = __shfl_down_sync(0xffffffffu, v[2 * i].x, 1), nxy = __shfl_down_sync(0xffffffffu, v[2 * i].y, 1);
+            if (i + 1 < NRU) {
+                const int bx = __shfl_sync(0xffffffffu, v[2 * i + 2].x, 0), by = __shfl_sync(0xffffffffu, v[2 * i + 2].y, 0);
+                if (lane == kWarp - 1) {
+                    nxx = bx;
+                    nxy = by;
+                }
+            }
+            if (lane + i * kWarp + 1 == un) {
+                nxx = la_x;
+                nxy = la_y;
+            }
+            nx[i] = make_int2(nxx, nxy);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int32_t d = s_d[buf][pr][j];
+            if (d < 0) continue;
+            uint8_t *rows2[2] = {xd + (int64_t)d * H,
+                                 reinterpret_cast<uint8_t *>(static_cast<uintptr_t>(s_prow[buf][pr][j]))};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint8_t *A = rows2[q];
+                if (!A) continue;
+                if ((reinterpret_cast<uintptr_t>(A) & 8) == 0) { // 16-byte aligned row
+#pragma unroll
+                    for (int i = 0; i < NRU; ++i) {
+                        const int w = lane + i * kWarp;
+                        if (w < un)
+                            st_stream(reinterpret_cast<int4 *>(A + 16 * (int64_t)(ub + w)),
+                                      make_int4(v[2 * i].x, v[2 * i].y, v[2 * i + 1].x, v[2 * i + 1].y));
+                    }
+                    if (h == 1 && lane == 0 && lone)
+                        st_stream(reinterpret_cast<int2 *>(A + 16 * (int64_t)nu), make_int2(la_x, la_y));
+                } else { // 8 bytes off: aligned stores straddle two units
+#pragma unroll
+                    for (int i = 0; i < NRU; ++i) {
+                        const int w = lane + i * kWarp;
+                        if (w < un) {
+                            uint8_t *c = A + 16 * (int64_t)(ub + w) + 8;
+                            if (w + 1 < un || la >= 0)
+                                st_stream(reinterpret_cast<int4 *>(c),
+                                          make_int4(v[2 * i + 1].x, v[2 * i + 1].y, nx[i].x, nx[i].y));
+                            else
+                                st_stream(reinterpret_cast<int2 *>(c), make_int2(v[2 * i + 1].x, v[2 * i + 1].y));
+                        }
+                    }
+                    if (lane == 0) { // the row's first 8 bytes
+                        if (h == 0 && un > 0) st_stream(reinterpret_cast<int2 *>(A), make_int2(v[0].x, v[0].y));
+                        if (h == 1 && lone && nu == 0) st_stream(reinterpret_cast<int2 *>(A), make_int2(la_x, la_y));
+                    }
+                }
+            }
+        }
+    }
+}
+
 } // namespace
 } // namespace ap
 
@@ -1452,14 +1645,25 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
             const int64_t want2 = (T + 3) / 4; // four tokens (warp pairs) per block
             const int64_t cap2 = inl ? want2 : (int64_t)sm_count() * 16;
             const int grid2 = (int)(want2 < cap2 ? want2 : cap2);
-#define AP_LAUNCH_E4M3(NRH)                                                                                       \
-    ap::launch(ap::k_dispatch_stash_e4m3<NRH>, grid2, 256, 0, st, xs16, T, H, idx, dest, k, E, capacity, blk,       \
-               seg_off, src_tok, xo, xd_scale, stt, rec, ps, p->cfg.page_tokens, page_off[1], ia)
-            if (H <= 512) AP_LAUNCH_E4M3(1);
-            else if (H <= 1024) AP_LAUNCH_E4M3(2);
-            else if (H <= 2048) AP_LAUNCH_E4M3(4);
-            else if (H <= 2304) AP_LAUNCH_E4M3(5);
-            else AP_LAUNCH_E4M3(8);
+            // every row 16-byte aligned (H and every base are): one vector per
+            // lane and round, 8-byte code stores; otherwise 16-code units and
+            // aligned 16-byte stores (a warp holds at most 32 * NRU units, so
+            // H / 8 <= 128 * NRU + 1 vectors)
+            const bool aligned16 = H % 16 == 0 && (al & 15) == 0;
+            const int nvec = H / 8;
+#define AP_LAUNCH_E4M3(KERNEL)                                                                                    \
+    ap::launch(KERNEL, grid2, 256, 0, st, xs16, T, H, idx, dest, k, E, capacity, blk, seg_off, src_tok, xo,       \
+               xd_scale, stt, rec, ps, p->cfg.page_tokens, page_off[1], ia)
+            if (aligned16) {
+                if (H <= 512) AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3<1>);
+                else if (H <= 1024) AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3<2>);
+                else if (H <= 2048) AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3<4>);
+                else if (H <= 2304) AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3<5>);
+                else AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3<8>);
+            } else if (nvec <= 129) AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3_units<1>);
+            else if (nvec <= 257) AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3_units<2>);
+            else if (nvec <= 385) AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3_units<3>);
+            else AP_LAUNCH_E4M3(ap::k_dispatch_stash_e4m3_units<4>);
 #undef AP_LAUNCH_E4M3
         } else if ((al & 15) == 0)
             ap::launch(ap::k_dispatch_stash_copy<int4>, grid, 256, 0, st, xs, T, rb[0], idx, dest, k, E, capacity, blk,

@@ -109,18 +109,34 @@ def test_fused_host_errors():
     assert rc == -5  # not the paging stream
 
 
-# Two warps per token, each holding half the row's 16-byte vectors (8 bf16):
-# a row of H values is H/8 vectors, warp 0 takes the first ceil(H/16).
-@pytest.mark.parametrize("T,H,E,k,P,N,SP", [
-    (4096, 2048, 64, 6, 128, 120, 0),    # the FP8 layer-stack shape: 128 vectors per warp, 4 per lane
-    (4096, 2056, 64, 6, 128, 120, 0),    # its non-divisible variant: 129 / 128 vectors
-    (999, 2056, 64, 6, 128, 40, 64),     # odd hidden size: 129 / 128 vectors (a fifth round on one lane); spill
-    (300, 1024, 16, 4, 32, 20, 4),       # 64 vectors per warp, 2 per lane; lost pages
-    (600, 4096, 32, 4, 32, 100, 16),     # the widest rows: 256 vectors per warp, 8 per lane; spill
-    (700, 2312, 48, 5, 64, 70, 40),      # 145 / 144 vectors: the 8-per-lane kernel with ragged rounds; spill
-    (175000, 64, 64, 6, 128, 8300, 100),  # a record of 1.05 M pairs, 4 vectors per warp; spills
+# Two warps per token. A row of H values is H/8 16-byte vectors (8 bf16 each).
+# When every row is 16-byte aligned (H % 16 == 0 and aligned buffers), warp 0
+# takes the first ceil(H/16) vectors and warp 1 the rest, one per lane per
+# round. Otherwise the row is cut into 16-code units of two vectors and, for
+# odd H/8, one lone last vector; warp 0 takes the first ceil(units/2) units,
+# warp 1 the rest and the lone vector, and rows that start 8 bytes off a
+# 16-byte boundary get aligned 16-byte stores straddling two units. xd_off
+# starts the dispatch buffer 8 bytes into its allocation.
+@pytest.mark.parametrize("T,H,E,k,P,N,SP,xd_off", [
+    (4096, 2048, 64, 6, 128, 120, 0, 0),    # the FP8 layer-stack shape: 128 / 128 vectors, 4 rounds
+    (4096, 2056, 64, 6, 128, 120, 0, 0),    # its non-divisible variant: 64 / 64 units and the lone vector
+    (999, 2056, 64, 6, 128, 40, 64, 0),     # the same rows with spill
+    (300, 1024, 16, 4, 32, 20, 4, 0),       # 64 / 64 vectors, 2 rounds; lost pages
+    (600, 4096, 32, 4, 32, 100, 16, 0),     # the widest rows: 256 / 256 vectors, 8 rounds; spill
+    (500, 2304, 32, 4, 32, 100, 16, 0),     # 144 / 144 vectors: the 5-round instance; spill
+    (700, 2312, 48, 5, 64, 70, 40, 0),      # 72 / 72 units and a lone vector: 3 rounds, ragged; spill
+    (175000, 64, 64, 6, 128, 8300, 100, 0),  # a record of 1.05 M pairs, 4 / 4 vectors; spills
+    (257, 8, 8, 2, 16, 64, 8, 0),           # a lone vector and no unit: warp 1 writes the whole row
+    (300, 16, 8, 3, 16, 80, 8, 8),          # one unit, warp 1 idle; every dispatch row 8 bytes off
+    (300, 24, 8, 3, 16, 80, 8, 0),          # one unit and the lone vector (warp 0's lookahead)
+    (200, 40, 16, 4, 8, 120, 0, 0),         # 1 / 1 units and the lone vector
+    (333, 1024, 16, 4, 32, 50, 8, 8),       # 32 / 32 units, dispatch rows 8 bytes off, page rows aligned
+    (333, 1032, 16, 4, 32, 50, 8, 0),       # 32 / 32 units and the lone vector: the widest one-round rows
+    (333, 1040, 16, 4, 32, 50, 8, 0),       # 33 / 32 units: one lane of warp 0 takes a second round
+    (250, 3080, 16, 4, 32, 40, 8, 0),       # 96 / 96 units and the lone vector: the widest three-round rows
+    (250, 4088, 16, 4, 32, 40, 8, 0),       # 128 / 127 units and the lone vector: four rounds
 ])
-def test_fused_e4m3_matches_oracle(T, H, E, k, P, N, SP):
+def test_fused_e4m3_matches_oracle(T, H, E, k, P, N, SP, xd_off):
     rb = (H, 4)
     page_bytes = ap.page_bytes_for(P, rb)
     g = ap.Pool(P, page_bytes, N, 1, 4, E, N + SP + E, SP, fill=FILL)
@@ -131,7 +147,8 @@ def test_fused_e4m3_matches_oracle(T, H, E, k, P, N, SP):
     plan = oracle.dispatch(x, idx, E, 0, False, fp8=True)
     rid_o = o.push(0, [plan["xd"], plan["xd_scale"].view(np.uint8).reshape(-1, 4)], plan["rows"], plan["seg_off"],
                    plan["live"])
-    xd = torch.full((plan["rows"], H), 0xA5, dtype=torch.uint8, device="cuda")
+    xd = torch.full((plan["rows"] * H + xd_off,), 0xA5, dtype=torch.uint8, device="cuda")[xd_off:].view(plan["rows"], H)
+    assert xd.data_ptr() % 16 == xd_off
     xs = torch.from_numpy(np.full(plan["rows"] * 4, 0xA5, np.uint8).view(np.float32)).cuda()
     torch.cuda.synchronize()
     with torch.cuda.stream(g.stream):
