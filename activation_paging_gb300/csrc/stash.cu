@@ -600,15 +600,15 @@ __device__ __forceinline__ V block_exclusive_scan256(V v, V *ws, V *total)
 
 // The prologue every copy block runs (256 threads).  b: the count/rank block
 // of this block's tokens.  Ends with a barrier: pl is complete for the block.
+template <bool kVecReads>
 __device__ __forceinline__ void inline_plan(InlinePlan &pl, const int32_t *__restrict__ blk, int b, int E,
                                             int capacity, const InlineArgs &ia, const RecPtr &rec, int P)
 {
-    __shared__ int32_t s_lt[256], s_all[256]; // partial sums: [row group][expert]
+    constexpr int kPartials = kVecReads ? 1024 : 256;
+    __shared__ __align__(16) int32_t s_lt[kPartials], s_all[kPartials]; // partial sums: [row group][expert]
     __shared__ int64_t s_ws[8];
     const int tid = threadIdx.x;
     const int nblk = ia.nblk;
-    const int Q = blockDim.x / E; // row groups per expert column (>= 1)
-    const int e = tid % E, q = tid / E;
     if (tid == 0) {
         pl.bad = 0;
         pl.head0 = rec.hdr->head0;
@@ -616,28 +616,56 @@ __device__ __forceinline__ void inline_plan(InlinePlan &pl, const int32_t *__res
         pl.tail0 = rec.hdr->tail0;
         pl.stail0 = rec.hdr->spill_tail0;
     }
-    // each thread sums one expert column over a strided set of rows: the
-    // counts of the rows before b (this block's base) and of all rows (totals)
-    int32_t lt = 0, all = 0;
-    if (q < Q) {
-        int r = q;
-        for (; r + 15 * Q < nblk; r += 16 * Q) { // sixteen loads in flight (one round for 64 x 64 counts)
-            int32_t c[16];
+    // each thread sums expert columns over a strided set of rows: the counts
+    // of the rows before b (this block's base) and of all rows (totals).  One
+    // column per thread takes one round of sixteen loads in flight for up to
+    // 16 rows per thread (64 x 64 counts); more rows go four adjacent columns
+    // per 16-byte load, in predicated rounds of eight (128 x 128 counts: two),
+    // in kernels that can spare the shared memory (kVecReads)
+    const int Q1 = blockDim.x / E; // row groups of the one-column reading (>= 1)
+    const bool vec =
+        kVecReads && nblk > 16 * Q1 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(blk) & 15) == 0;
+    const int Q = vec ? blockDim.x / (E / 4) : Q1;
+    if (vec && tid / (E / 4) < Q) {
+        const int c = tid % (E / 4), q = tid / (E / 4);
+        int4 lt = make_int4(0, 0, 0, 0), all = lt;
+        for (int r = q; r < nblk; r += 8 * Q) {
+            int4 v[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) c[u] = blk[(int64_t)(r + u * Q) * E + e];
+            for (int u = 0; u < 8; ++u)
+                v[u] = (r + u * Q < nblk) ? reinterpret_cast<const int4 *>(blk + (int64_t)(r + u * Q) * E)[c]
+                                          : make_int4(0, 0, 0, 0);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                all += c[u];
-                if (r + u * Q < b) lt += c[u];
+            for (int u = 0; u < 8; ++u) {
+                all.x += v[u].x, all.y += v[u].y, all.z += v[u].z, all.w += v[u].w;
+                if (r + u * Q < b) lt.x += v[u].x, lt.y += v[u].y, lt.z += v[u].z, lt.w += v[u].w;
             }
         }
-        for (; r < nblk; r += Q) {
-            const int32_t c = blk[(int64_t)r * E + e];
-            all += c;
-            if (r < b) lt += c;
+        reinterpret_cast<int4 *>(s_lt + q * E)[c] = lt;
+        reinterpret_cast<int4 *>(s_all + q * E)[c] = all;
+    } else if (!vec) {
+        const int e = tid % E, q = tid / E;
+        int32_t lt = 0, all = 0;
+        if (q < Q) {
+            int r = q;
+            for (; r + 15 * Q < nblk; r += 16 * Q) { // sixteen loads in flight
+                int32_t c[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) c[u] = blk[(int64_t)(r + u * Q) * E + e];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    all += c[u];
+                    if (r + u * Q < b) lt += c[u];
+                }
+            }
+            for (; r < nblk; r += Q) {
+                const int32_t c = blk[(int64_t)r * E + e];
+                all += c;
+                if (r < b) lt += c;
+            }
+            s_lt[q * E + e] = lt;
+            s_all[q * E + e] = all;
         }
-        s_lt[q * E + e] = lt;
-        s_all[q * E + e] = all;
     }
     __syncthreads();
     int32_t total = 0, base = 0;
@@ -819,7 +847,7 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
     const int64_t nvec = rb / (int64_t)sizeof(V);
     __shared__ InlinePlan pl;
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan(pl, blk, (int)(((int64_t)blockIdx.x * (blockDim.x / kWarp)) / kTokPerBlk), E, capacity, ia,
+        inline_plan<true>(pl, blk, (int)(((int64_t)blockIdx.x * (blockDim.x / kWarp)) / kTokPerBlk), E, capacity, ia,
                     rec, P);
         if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
     }
@@ -917,7 +945,7 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
     const int half0 = (nstep + 1) / 2;
     const int s_begin = h ? half0 : 0, s_end = h ? nstep : half0;
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
+        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
         if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
     }
     const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;
@@ -1049,7 +1077,7 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3_units(
     const int ub = h ? u0 : 0, un = h ? nu - u0 : u0; // this warp's first unit and unit count
     const int la = h ? (lone ? nstep - 1 : -1) : (2 * u0 < nstep ? 2 * u0 : -1); // lookahead vector
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
+        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
         if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
     }
     const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;

@@ -25,6 +25,14 @@ FILL = 0xA5
     (300, 64, 8, 2, 0, False, 8, 10, 5),          # spill exhausted: lost pages
     (600, 64, 1024, 16, 0, False, 8, 3000, 0),    # the most experts
     (131100, 64, 64, 8, 0, False, 64, 16000, 2000),  # a record of 1.05 M pairs; spills
+    # records planned inside the copy kernel with more than sixteen count/rank
+    # blocks per reading thread: four-column reads (128 x 128 counts, the
+    # headline's; 94 x 48 with a ragged last row group), padded, and one-column
+    # reads for E % 4 != 0
+    (8192, 256, 128, 8, 0, False, 64, 2400, 0),
+    (6000, 64, 48, 4, 0, False, 16, 1600, 0),
+    (6000, 64, 48, 4, 560, True, 16, 1800, 0),
+    (6000, 64, 50, 4, 0, False, 16, 1600, 0),
 ])
 def test_fused_matches_oracle_dispatch_then_push(T, H, E, k, C, padded, P, N, SP):
     rb = H * 2
