@@ -99,7 +99,9 @@ __device__ __forceinline__ bool block_count_rank(const int32_t *pidx, int64_t p0
 // The metadata kernels that run before a row copy leave HBM idle; a bulk
 // prefetch of their block's rows [t0, t0 + ntok) then lets the copy read its
 // input from L2 while it streams its writes.  A hint only: nothing waits on
-// it and no result depends on it.  x and rb are 16-byte multiples (the caller
+// it and no result depends on it, and L2 is where global memory is coherent,
+// so the kernels issue it before their dependency wait, overlapping the tail
+// of the kernel before them.  x and rb are 16-byte multiples (the caller
 // passes x = nullptr otherwise).
 struct RowPrefetch {
     const uint8_t *x;
@@ -128,6 +130,10 @@ __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__re
                                                              uint32_t *d_status, RowPrefetch pf,
                                                              const uint64_t *snap_src, uint64_t *snap_dst)
 {
+    { // a hint that changes no value: issued before the wait, so it overlaps the previous kernel's tail
+        const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
+        prefetch_rows_l2(pf, t0, (T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
+    }
     pdl_begin();
     if (snap_dst && blockIdx.x == 0 && threadIdx.x == 0) {
         const uint64_t head = snap_src[0], tail = snap_src[1], sh = snap_src[2], stl = snap_src[3];
@@ -135,10 +141,6 @@ __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__re
         snap_dst[1] = sh;
         snap_dst[2] = tail;
         snap_dst[3] = stl;
-    }
-    {
-        const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
-        prefetch_rows_l2(pf, t0, (T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
     }
     extern __shared__ int32_t cnt[]; // [kRankWarps][E]
     const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
@@ -160,6 +162,10 @@ __global__ void __launch_bounds__(kRouteRankWarps * kWarp) k_route_count_rank(
     int32_t *__restrict__ blk, int32_t *__restrict__ dest, RowPrefetch pf, const uint64_t *snap_src,
     uint64_t *snap_dst)
 {
+    {
+        const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
+        prefetch_rows_l2(pf, t0, (T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk); // before the wait, as k_count_rank
+    }
     pdl_begin();
     if (snap_dst && blockIdx.x == 0 && threadIdx.x == 0) { // as k_count_rank
         const uint64_t head = snap_src[0], tail = snap_src[1], sh = snap_src[2], stl = snap_src[3];
@@ -174,7 +180,6 @@ __global__ void __launch_bounds__(kRouteRankWarps * kWarp) k_route_count_rank(
     const int lane = (int)lane_id(), wid = threadIdx.x / kWarp;
     const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
     const int ntok = (int)((T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
-    prefetch_rows_l2(pf, t0, ntok);
     for (int tt = wid; tt < ntok; tt += kRouteRankWarps) {
         int e;
         float wt;
