@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libap.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["common.cu", "route.cu", "dispatch.cu", "combine.cu", "stash.cu", "noalloc.cu", "arena.cu"]
 # bench-only synthetic compute (whole-SM busy blocks for the overlap measurement), not part of libap.so
-BENCH_SOURCES = ["bench/busy.cu"]
+BENCH_SOURCES = ["bench/busy.cu", "bench/green.cu"]
 BENCH_LIB = os.path.join(HERE, "libap_bench.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

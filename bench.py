@@ -679,6 +679,139 @@ def sm_split_report(step, device, free_sms=(0, 8, 19, 38, 76, 114), reps=7, busy
     return out
 
 
+def sm_partition_report(step, device, sizes=(8, 16, 24, 32, 48), reps=9, gemm_reps=6):
+    """Reloads and a GEMM on disjoint SM partitions (green contexts).
+
+    The bench-only libap_bench.so splits the GPU into a partition of at
+    least n SMs, whose stream becomes the paging stream of a pool with the
+    step's configuration, and one of the SMs left, whose stream runs
+    `gemm_reps` bf16 8192 x 2304 x 8192 GEMMs back to back (about 1 ms:
+    reloads on a few SMs take longer than one GEMM, so a partition pays only
+    under longer compute).  The step's records are pushed into that pool and
+    popped while the GEMMs run (early launch, late wait).  For each n: the
+    GEMM alone on its partition, the reloads alone on theirs, and both; and,
+    measured in the same rounds on the whole GPU, the GEMM alone, the reloads
+    alone and both on shared SMs (the paging stream's default grid bound)."""
+    import ctypes
+    import torch
+    import activation_paging_gb300 as ap
+    from activation_paging_gb300 import build as cuda_build
+    lib = ctypes.CDLL(cuda_build.BENCH_LIB)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    lib.apb_green_split.restype = ip
+    lib.apb_green_split.argtypes = [ip, ip] + [ctypes.POINTER(vp)] * 2 + [ctypes.POINTER(ip)] * 2 + \
+        [ctypes.POINTER(vp)] * 2
+    lib.apb_green_destroy.restype = ip
+    lib.apb_green_destroy.argtypes = [vp] * 4
+    dev_index = torch.device(device).index or 0
+    g = torch.Generator(device=device).manual_seed(0)
+    a = torch.randn((8192, 2304), device=device, dtype=torch.bfloat16, generator=g)
+    b = torch.randn((2304, 8192), device=device, dtype=torch.bfloat16, generator=g)
+    c = torch.empty((8192, 8192), device=device, dtype=torch.bfloat16)
+    scrub_buf = torch.ones(256 << 20, device=device, dtype=torch.float16)  # 512 MB, four times L2
+    full = torch.cuda.Stream(device=device, priority=0)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def scrub():
+        with torch.cuda.stream(full):
+            scrub_buf.sum()
+        torch.cuda.synchronize(device)
+
+    def gemm(stream):
+        with torch.cuda.stream(stream):
+            for _ in range(gemm_reps):
+                torch.matmul(a, b, out=c)
+
+    def push(pool, stream):
+        with torch.cuda.stream(stream):
+            for h, d in step.chunks:
+                pool.push(0, [d["disp"]["xd"]], d["disp"]["seg_off"], d["disp"]["live"])
+
+    def pop(pool, stream):
+        with torch.cuda.stream(stream):
+            for h, d in step.chunks:
+                pool.pop(0, [d["dst"]])
+
+    def measure(pool, paging, compute):
+        """(GEMM alone, reloads alone, both) in ms, each after an L2 scrub."""
+        scrub()
+        s0, s1 = ev(), ev()
+        s0.record(compute)
+        gemm(compute)
+        s1.record(compute)
+        torch.cuda.synchronize(device)
+        push(pool, paging)
+        scrub()
+        p0, p1 = ev(), ev()
+        p0.record(paging)
+        pop(pool, paging)
+        p1.record(paging)
+        torch.cuda.synchronize(device)
+        push(pool, paging)
+        scrub()
+        b0, done, b1 = ev(), ev(), ev()
+        b0.record(compute)
+        paging.wait_event(b0)
+        pop(pool, paging)          # early launch of the reloads
+        done.record(paging)
+        gemm(compute)
+        compute.wait_event(done)   # late wait
+        b1.record(compute)
+        torch.cuda.synchronize(device)
+        return s0.elapsed_time(s1), p0.elapsed_time(p1), b0.elapsed_time(b1)
+
+    cfg = step.pool.cfg
+    saved = step.pool.max_ctas
+    step.pool.max_ctas = 0
+    gemm(full)
+    torch.cuda.synchronize(device)
+    out = {"gemm": f"{gemm_reps} x bf16 8192x2304 @ 2304x8192 (cuBLAS), back to back",
+           "reload": f"{len(step.chunks)} pops of the step",
+           "method": f"median of {reps} rounds; per partition size n, green contexts split the GPU into at least "
+                     "n SMs for a pool with the step's configuration (its paging stream at the highest priority) "
+                     "and the SMs left for the GEMM; each part after an L2 scrub with nothing else in flight, "
+                     "reloads launched first and waited on last; whole_gpu is the same measurement with both "
+                     "streams on every SM",
+           "whole_gpu": None, "by_partition": {}}
+    whole = ([], [], [])
+    for n in sizes:
+        s1, s2, c1, c2 = vp(), vp(), vp(), vp()
+        n1, n2 = ip(), ip()
+        rc = lib.apb_green_split(dev_index, n, ctypes.byref(s1), ctypes.byref(s2), ctypes.byref(n1),
+                                 ctypes.byref(n2), ctypes.byref(c1), ctypes.byref(c2))
+        if rc != 0:
+            out["by_partition"][str(n)] = {"unavailable": f"green context split returned {rc}"}
+            continue
+        small = torch.cuda.ExternalStream(s1.value, device=device)
+        rest = torch.cuda.ExternalStream(s2.value, device=device)
+        pool = ap.Pool(cfg.page_tokens, cfg.page_bytes, cfg.num_pages, cfg.num_slots, cfg.max_records_per_slot,
+                       cfg.max_segments, cfg.max_pages_per_record, cfg.spill_pages, device=device, stream=small)
+        parts = ([], [], [])
+        for _ in range(reps):
+            for acc, v in zip(parts, measure(pool, small, rest)):
+                acc.append(v)
+            for acc, v in zip(whole, measure(step.pool, step.stream, full)):
+                acc.append(v)
+        flags = pool.overflow()
+        torch.cuda.synchronize(device)
+        del pool
+        rc = lib.apb_green_destroy(s1, s2, c1, c2)
+        mg, mp, mb = (statistics.median(v) for v in parts)
+        out["by_partition"][str(n)] = {"reload_sms": n1.value, "gemm_sms": n2.value, "gemm_ms": round(mg, 4),
+                                       "reload_ms": round(mp, 4), "both_ms": round(mb, 4), "pool_flags": flags,
+                                       "destroy_rc": rc}
+    step.pool.max_ctas = saved
+    if whole[0]:
+        wg, wp, wb = (statistics.median(v) for v in whole)
+        out["whole_gpu"] = {"gemm_ms": round(wg, 4), "reload_ms": round(wp, 4), "both_ms": round(wb, 4),
+                            "serial_ms": round(wg + wp, 4)}
+        for v in out["by_partition"].values():
+            if "both_ms" in v:
+                v["both_vs_whole_gpu_both"] = round(v["both_ms"] / wb, 4)
+                v["both_vs_serial"] = round(v["both_ms"] / (wg + wp), 4)
+    return out
+
+
 def push_records(step):
     """Stash every chunk's dispatch rows again (on the paging stream)."""
     import torch
@@ -1257,7 +1390,8 @@ def native(args):
                                                               "stream"))
     overlap = None
     if not args.no_overlap and world == 1:
-        overlap = {"beside_gemm": overlap_report(step, device), "sm_split": sm_split_report(step, device)}
+        overlap = {"beside_gemm": overlap_report(step, device), "sm_split": sm_split_report(step, device),
+                   "sm_partition": sm_partition_report(step, device)}
     calibration = calibration_report(step, device) if args.calibrate and world == 1 else None
     backward = backward_report(step, device) if args.backward else None
 

@@ -40,12 +40,52 @@ def gemm_work(stream, n=4096, reps=6):
 
 @pytest.mark.parametrize("max_ctas", [64, 0])
 def test_reloads_overlapped_with_compute_match_oracle(max_ctas):
+    overlapped_schedule(max_ctas, None, torch.cuda.Stream(priority=0))
+
+
+@pytest.fixture
+def green_streams():
+    """Two disjoint SM partitions (green contexts, made by the bench-only
+    libap_bench.so) and a stream in each: (small, rest, SMs of each)."""
+    import ctypes
+    from activation_paging_gb300 import build as cuda_build
+    lib = ctypes.CDLL(cuda_build.BENCH_LIB)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    lib.apb_green_split.restype = ip
+    lib.apb_green_split.argtypes = [ip, ip] + [ctypes.POINTER(vp)] * 2 + [ctypes.POINTER(ip)] * 2 + \
+        [ctypes.POINTER(vp)] * 2
+    lib.apb_green_destroy.restype = ip
+    lib.apb_green_destroy.argtypes = [vp] * 4
+    s1, s2, c1, c2 = vp(), vp(), vp(), vp()
+    n1, n2 = ip(), ip()
+    rc = lib.apb_green_split(torch.cuda.current_device(), 16, ctypes.byref(s1), ctypes.byref(s2), ctypes.byref(n1),
+                             ctypes.byref(n2), ctypes.byref(c1), ctypes.byref(c2))
+    if rc < 0:
+        pytest.skip(f"the driver lacks green-context entry point {-rc} of apb_green_split")
+    assert rc == 0, f"green context split failed: CUDA driver error {rc}"
+    yield (torch.cuda.ExternalStream(s1.value), torch.cuda.ExternalStream(s2.value), n1.value, n2.value)
+    torch.cuda.synchronize()
+    assert lib.apb_green_destroy(s1, s2, c1, c2) == 0
+
+
+def test_reloads_on_an_sm_partition_match_oracle(green_streams):
+    """The same schedule with the paging stream in a green context of at least
+    16 SMs and the GEMMs in one of the other SMs: the pool runs on whatever
+    stream it is given, and the bytes, rings and state still equal the
+    oracle's."""
+    small, rest, n_small, n_rest = green_streams
+    assert n_small >= 16 and n_rest >= 1
+    assert n_small + n_rest <= torch.cuda.get_device_properties(0).multi_processor_count
+    overlapped_schedule(0, small, rest)
+
+
+def overlapped_schedule(max_ctas, paging, compute):
     T, H, E, k, P = 2048, 1024, 64, 8, 32
     rb = 2 * H
     page_bytes = ap.page_bytes_for(P, (rb,))
     nrec = 3
     N = (T * k // P + E) * nrec
-    g = ap.Pool(P, page_bytes, N, 1, 4, E, N, max_ctas=max_ctas, fill=FILL)
+    g = ap.Pool(P, page_bytes, N, 1, 4, E, N, max_ctas=max_ctas, fill=FILL, stream=paging)
     o = oracle.Pool(P, page_bytes, N, 1, 4, E, N, 0, keep_bytes=True, fill=FILL)
     recs = []
     for r in range(nrec):
@@ -62,7 +102,6 @@ def test_reloads_overlapped_with_compute_match_oracle(max_ctas):
     torch.cuda.synchronize()
     assert g.state() == o.state()
 
-    compute = torch.cuda.Stream(priority=0)
     assert g.stream.priority < compute.priority  # the paging stream has the higher priority
     run_gemm, c = gemm_work(compute)
     dst = [torch.full((plan["rows"], H), 0x3C3C, dtype=torch.int16, device="cuda").view(torch.bfloat16)
