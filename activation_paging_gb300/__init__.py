@@ -80,6 +80,43 @@ def dispatch_scratch_bytes(T: int, k: int, E: int) -> int:
     return n.value
 
 
+def count_rank(E: int, idx: torch.Tensor | None = None, logits: torch.Tensor | None = None, k: int | None = None,
+               x: torch.Tensor | None = None, out: dict | None = None, status: torch.Tensor | None = None,
+               stream=None) -> dict:
+    """Count/rank alone (``ap_count_rank``) on ``stream`` (default: the
+    current stream): ``dest`` ([T, k] int32 ranks inside blocks of 64 tokens)
+    and ``scratch`` (the blocks' expert histograms), for a later
+    ``Pool.dispatch_stash(..., ranked=True, out=...)`` ordered after it.  With
+    ``logits`` ([T, E] float32) it routes first and adds ``idx`` and ``w``;
+    else ``idx`` is read.  ``x``: the rows the copy will read (an L2
+    prefetch hint)."""
+    o = dict(out) if out is not None else {}
+    if logits is not None:
+        _need(logits, torch.float32, "logits")
+        T = logits.shape[0]
+        dev = logits.device
+        if "idx" not in o:
+            o["idx"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+        if "w" not in o:
+            o["w"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+        idx = o["idx"]
+    else:
+        _need(idx, torch.int32, "idx")
+        T, k = idx.shape
+        dev = idx.device
+        o["idx"] = idx
+    if "dest" not in o:
+        o["dest"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+    sb = dispatch_scratch_bytes(T, k, E)
+    if "scratch" not in o or o["scratch"].numel() < sb:
+        o["scratch"] = torch.empty(sb, dtype=torch.uint8, device=dev)
+    rb = x.shape[1] * x.element_size() if x is not None else 0
+    check(lib().ap_count_rank(_p(logits), _p(o.get("w") if logits is not None else None), _p(idx), T, k, E, _p(x), rb,
+                              _p(o["dest"]), _p(o["scratch"]), o["scratch"].numel(), _p(status), _stream(stream)),
+          "count_rank")
+    return o
+
+
 def dispatch_permute(x: torch.Tensor, idx: torch.Tensor, E: int, capacity: int = 0, padded: bool = False,
                      fp8: bool = False, out: dict | None = None, status: torch.Tensor | None = None, stream=None):
     """Permute BF16 rows x [T, H] into expert-major rows.
@@ -376,12 +413,18 @@ class Pool:
 
     def dispatch_stash(self, slot: int, x: torch.Tensor, idx: torch.Tensor, E: int, capacity: int = 0,
                        padded: bool = False, fp8: bool = False, out: dict | None = None,
-                       status: torch.Tensor | None = None):
+                       status: torch.Tensor | None = None, ranked: bool = False):
         """Fused dispatch + push into ``slot`` (BF16 rows, or E4M3 codes and
         row scales as two planes): returns the dispatch dict (as
-        ``dispatch_permute``) with the record id under ``record_id``."""
+        ``dispatch_permute``) with the record id under ``record_id``.
+        ``ranked``: ``out`` holds ``count_rank``'s ``dest`` and ``scratch``
+        for this idx (``ap_dispatch_stash_ranked``: no count/rank launch); the
+        paging stream must already be ordered after the stream that ran it
+        (this call orders it after the caller's current stream)."""
         _need(idx, torch.int32, "idx")
-        return self._dispatch_stash(slot, x, idx, idx.shape[1], E, capacity, padded, fp8, out, status)
+        if ranked and (out is None or "dest" not in out or "scratch" not in out):
+            raise ValueError("ranked dispatch_stash needs out['dest'] and out['scratch'] from count_rank")
+        return self._dispatch_stash(slot, x, idx, idx.shape[1], E, capacity, padded, fp8, out, status, ranked=ranked)
 
     def route_dispatch_stash(self, slot: int, logits: torch.Tensor, x: torch.Tensor, k: int, E: int | None = None,
                              capacity: int = 0, padded: bool = False, fp8: bool = False, out: dict | None = None,
@@ -401,7 +444,8 @@ class Pool:
         return self._dispatch_stash(slot, x, o["idx"], k, E, capacity, padded, fp8, o, status, logits=logits,
                                     w=o["w"])
 
-    def _dispatch_stash(self, slot, x, idx, k, E, capacity, padded, fp8, out, status, logits=None, w=None):
+    def _dispatch_stash(self, slot, x, idx, k, E, capacity, padded, fp8, out, status, logits=None, w=None,
+                        ranked=False):
         _need(x, torch.bfloat16, "x")
         T, H = x.shape
         dev = x.device
@@ -425,7 +469,10 @@ class Pool:
         tail = (DTYPE_E4M3 if fp8 else DTYPE_BF16, _p(xd), _p(o.get("xd_scale") if fp8 else None), xd.shape[0],
                 _p(o["counts"]), _p(o["live"]), _p(o["seg_off"]), _p(o["dest"]), _p(o["src_tok"]), _p(o["scratch"]),
                 o["scratch"].numel(), _p(status), ctypes.byref(rid), self.stream.cuda_stream)
-        if logits is None:
+        if ranked:
+            check(self.lib.ap_dispatch_stash_ranked(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity,
+                                                    int(padded), *tail), "dispatch_stash_ranked")
+        elif logits is None:
             check(self.lib.ap_dispatch_stash(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity, int(padded),
                                              *tail), "dispatch_stash")
         else:

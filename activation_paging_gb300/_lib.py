@@ -23,7 +23,7 @@ class PoolConfig(ctypes.Structure):
 
 class PoolState(ctypes.Structure):
     _fields_ = [("head", u64), ("tail", u64), ("spill_head", u64), ("spill_tail", u64), ("flags", u32),
-                ("pad0", u32), ("high_water", i64), ("spill_high_water", i64), ("held", i64),
+                ("copy_done", u32), ("high_water", i64), ("spill_high_water", i64), ("held", i64),
                 ("held_high_water", i64), ("num_pages", i64), ("pad", i64 * 6)]
 
 
@@ -56,6 +56,9 @@ SIGNATURES = {
     "ap_stash_pop": (i32, [P, i32, i32, P, i64, P, P]),
     "ap_dispatch_stash": (i32, [P, i32, P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P, i64, P,
                                 P, P]),
+    "ap_dispatch_stash_ranked": (i32, [P, i32, P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P,
+                                       i64, P, P, P]),
+    "ap_count_rank": (i32, [P, P, P, i64, i32, i32, P, i64, P, P, i64, P, P]),
     "ap_pool_time_copies": (i32, [P, P, P]),
     "ap_route_dispatch_stash": (i32, [P, i32, P, P, P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P,
                                       P, P, i64, P, P, P]),

@@ -39,20 +39,16 @@ ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E,
 // runs its own scan (see dispatch_scan.cuh).  x / x_rb (here, in
 // dispatch_metadata and in dispatch_route_count_rank): the input rows the row
 // copy after these kernels reads; each count/rank block prefetches its own
-// rows into L2 (nullptr: none).  snap_src / snap_dst: the pool's four
-// free-ring counters and where in the record header to copy them (a fused
-// dispatch + push whose copy kernel plans the record; nullptr: no copy).
+// rows into L2 (nullptr: none).
 ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
-                              uint32_t *d_status, cudaStream_t st, const void *x = nullptr, int64_t x_rb = 0,
-                              const uint64_t *snap_src = nullptr, uint64_t *snap_dst = nullptr);
+                              uint32_t *d_status, cudaStream_t st, const void *x = nullptr, int64_t x_rb = 0);
 int dispatch_blocks(int64_t T);
 // Route (as ap_route_topk, into idx and w) and count/rank in one launch: the
 // same outputs as ap_route_topk followed by dispatch_count_rank.  Arguments
 // are checked by the caller.
 ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
                                     void *scratch, int32_t *dest, cudaStream_t st, const void *x = nullptr,
-                                    int64_t x_rb = 0, const uint64_t *snap_src = nullptr,
-                                    uint64_t *snap_dst = nullptr);
+                                    int64_t x_rb = 0);
 
 // ---- NVTX ranges ---------------------------------------------------------------
 // Every entry point that enqueues GPU work or waits on the GPU opens a range

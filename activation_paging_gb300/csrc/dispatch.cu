@@ -121,27 +121,15 @@ __device__ __forceinline__ void prefetch_rows_l2(RowPrefetch pf, int64_t t0, int
 }
 
 // Count/rank blocks of kTokPerBlk tokens reading idx from global memory.
-// snap_src / snap_dst (a fused dispatch + push whose copy kernel plans the
-// record itself): block 0 copies the pool's free-ring counters (head, tail,
-// spill head, spill tail) into the record header (head0, spill_head0,
-// tail0, spill_tail0) after its wait, when no kernel changes them.
 __global__ void __launch_bounds__(kRankThreads) k_count_rank(const int32_t *__restrict__ idx, int64_t T, int k, int E,
                                                              int32_t *__restrict__ blk, int32_t *__restrict__ dest,
-                                                             uint32_t *d_status, RowPrefetch pf,
-                                                             const uint64_t *snap_src, uint64_t *snap_dst)
+                                                             uint32_t *d_status, RowPrefetch pf)
 {
     { // a hint that changes no value: issued before the wait, so it overlaps the previous kernel's tail
         const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
         prefetch_rows_l2(pf, t0, (T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk);
     }
     pdl_begin();
-    if (snap_dst && blockIdx.x == 0 && threadIdx.x == 0) {
-        const uint64_t head = snap_src[0], tail = snap_src[1], sh = snap_src[2], stl = snap_src[3];
-        snap_dst[0] = head;
-        snap_dst[1] = sh;
-        snap_dst[2] = tail;
-        snap_dst[3] = stl;
-    }
     extern __shared__ int32_t cnt[]; // [kRankWarps][E]
     const int64_t p0 = (int64_t)blockIdx.x * kTokPerBlk * k;
     const int64_t p1 = (p0 + (int64_t)kTokPerBlk * k < T * k) ? p0 + (int64_t)kTokPerBlk * k : T * k;
@@ -159,21 +147,13 @@ constexpr int kRouteRankWarps = 32;
 template <int NV>
 __global__ void __launch_bounds__(kRouteRankWarps * kWarp) k_route_count_rank(
     const float *__restrict__ logits, int64_t T, int E, int k, int32_t *__restrict__ idx, float *__restrict__ w,
-    int32_t *__restrict__ blk, int32_t *__restrict__ dest, RowPrefetch pf, const uint64_t *snap_src,
-    uint64_t *snap_dst)
+    int32_t *__restrict__ blk, int32_t *__restrict__ dest, RowPrefetch pf)
 {
     {
         const int64_t t0 = (int64_t)blockIdx.x * kTokPerBlk;
         prefetch_rows_l2(pf, t0, (T - t0 < kTokPerBlk) ? T - t0 : kTokPerBlk); // before the wait, as k_count_rank
     }
     pdl_begin();
-    if (snap_dst && blockIdx.x == 0 && threadIdx.x == 0) { // as k_count_rank
-        const uint64_t head = snap_src[0], tail = snap_src[1], sh = snap_src[2], stl = snap_src[3];
-        snap_dst[0] = head;
-        snap_dst[1] = sh;
-        snap_dst[2] = tail;
-        snap_dst[3] = stl;
-    }
     extern __shared__ int32_t smem[]; // cnt [32][E], then the block's ids [kTokPerBlk * k]
     int32_t *cnt = smem;
     int32_t *sidx = smem + kRouteRankWarps * E;
@@ -484,14 +464,13 @@ static RowPrefetch row_prefetch(const void *x, int64_t x_rb)
 }
 
 ap_status dispatch_count_rank(int64_t T, const int32_t *idx, int32_t k, int32_t E, void *scratch, int32_t *dest,
-                              uint32_t *d_status, cudaStream_t st, const void *x, int64_t x_rb,
-                              const uint64_t *snap_src, uint64_t *snap_dst)
+                              uint32_t *d_status, cudaStream_t st, const void *x, int64_t x_rb)
 {
     const int64_t nb = nblocks(T);
     if (nb == 0) return AP_OK;
     const size_t smem = (size_t)kRankWarps * E * sizeof(int32_t);
     launch(k_count_rank, (unsigned)nb, kRankThreads, smem, st, idx, T, k, E, static_cast<int32_t *>(scratch), dest,
-           d_status, row_prefetch(x, x_rb), snap_src, snap_dst);
+           d_status, row_prefetch(x, x_rb));
     AP_CHECK_LAUNCH("dispatch count/rank launch");
     return AP_OK;
 }
@@ -500,8 +479,7 @@ int dispatch_blocks(int64_t T) { return (int)nblocks(T); }
 
 template <int NV>
 ap_status launch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
-                                  int32_t *blk, int32_t *dest, cudaStream_t st, RowPrefetch pf,
-                                  const uint64_t *snap_src, uint64_t *snap_dst)
+                                  int32_t *blk, int32_t *dest, cudaStream_t st, RowPrefetch pf)
 {
     const size_t smem = ((size_t)kRouteRankWarps * E + (size_t)kTokPerBlk * k) * sizeof(int32_t);
     static const cudaError_t attr = cudaFuncSetAttribute((const void *)k_route_count_rank<NV>,
@@ -510,27 +488,26 @@ ap_status launch_route_count_rank(const float *logits, int64_t T, int32_t E, int
                                                                sizeof(int32_t)));
     if (attr != cudaSuccess) return cuda_fail(attr, "route + count/rank: shared memory limit");
     launch(k_route_count_rank<NV>, (unsigned)nblocks(T), kRouteRankWarps * kWarp, smem, st, logits, T, E, k, idx, w,
-           blk, dest, pf, snap_src, snap_dst);
+           blk, dest, pf);
     AP_CHECK_LAUNCH("route + count/rank launch");
     return AP_OK;
 }
 
 ap_status dispatch_route_count_rank(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *idx, float *w,
-                                    void *scratch, int32_t *dest, cudaStream_t st, const void *x, int64_t x_rb,
-                                    const uint64_t *snap_src, uint64_t *snap_dst)
+                                    void *scratch, int32_t *dest, cudaStream_t st, const void *x, int64_t x_rb)
 {
     if (nblocks(T) == 0) return AP_OK;
     int32_t *blk = static_cast<int32_t *>(scratch);
     const RowPrefetch pf = row_prefetch(x, x_rb);
-    if (E <= 32) return launch_route_count_rank<1>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
-    if (E <= 64) return launch_route_count_rank<2>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
-    if (E <= 128) return launch_route_count_rank<4>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
-    if (E <= 256) return launch_route_count_rank<8>(logits, T, E, k, idx, w, blk, dest, st, pf, snap_src, snap_dst);
+    if (E <= 32) return launch_route_count_rank<1>(logits, T, E, k, idx, w, blk, dest, st, pf);
+    if (E <= 64) return launch_route_count_rank<2>(logits, T, E, k, idx, w, blk, dest, st, pf);
+    if (E <= 128) return launch_route_count_rank<4>(logits, T, E, k, idx, w, blk, dest, st, pf);
+    if (E <= 256) return launch_route_count_rank<8>(logits, T, E, k, idx, w, blk, dest, st, pf);
     // more than 8 candidates per lane do not fit a 1024-thread block's
     // registers: route and count/rank as two launches
     ap_status s = ap_route_topk(logits, T, E, k, idx, w, st);
     if (s != AP_OK) return s;
-    return dispatch_count_rank(T, idx, k, E, scratch, dest, nullptr, st, x, x_rb, snap_src, snap_dst);
+    return dispatch_count_rank(T, idx, k, E, scratch, dest, nullptr, st, x, x_rb);
 }
 
 ap_status dispatch_metadata(int64_t T, const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
@@ -601,6 +578,26 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
     }
     AP_CHECK_LAUNCH("dispatch copy launch");
     return AP_OK;
+}
+
+extern "C" ap_status ap_count_rank(const float *logits, float *w, int32_t *idx, int64_t T, int32_t k, int32_t E,
+                                   const void *x, int64_t row_bytes, int32_t *dest, void *scratch,
+                                   int64_t scratch_bytes, uint32_t *d_status, void *stream)
+{
+    AP_NVTX_RANGE("ap_count_rank");
+    using namespace ap;
+    if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024 || T * (int64_t)k >= (int64_t(1) << 31))
+        return fail(AP_EINVAL, "count_rank: bad sizes T=%lld k=%d E=%d", (long long)T, k, E);
+    if (logits && k > E) return fail(AP_EINVAL, "count_rank: k=%d > E=%d", k, E);
+    int64_t need = 0;
+    ap_dispatch_scratch_bytes(T, k, E, &need);
+    if (scratch_bytes < need)
+        return fail(AP_EINVAL, "count_rank: scratch %lld < %lld bytes", (long long)scratch_bytes, (long long)need);
+    if (!scratch || (T > 0 && (!idx || !dest || (logits && !w)))) return fail(AP_EINVAL, "count_rank: NULL pointer");
+    if (row_bytes < 0) return fail(AP_EINVAL, "count_rank: row_bytes %lld < 0", (long long)row_bytes);
+    cudaStream_t st = (cudaStream_t)stream;
+    return logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, row_bytes)
+                  : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, row_bytes);
 }
 
 extern "C" ap_status ap_cast_e4m3(const float *in, uint8_t *out, int64_t n, void *stream)

@@ -52,8 +52,7 @@ struct RecHdr {
     int32_t pad0;
     int64_t npages, ndev, nspill, nlost;
     uint64_t head0, spill_head0;
-    uint64_t tail0, spill_tail0; // free-ring tails at the push (written with head0 by an inline-planned push)
-    int64_t pad1[7];
+    int64_t pad1[9];
 };
 static_assert(sizeof(RecHdr) == 128, "record header layout");
 static_assert(sizeof(ap_pool_state) == 128, "state layout");
@@ -181,7 +180,7 @@ __global__ void k_reset(ap_pool_state *st, int32_t *ring, int64_t N, int64_t NMA
         st->spill_head = 0;
         st->spill_tail = (uint64_t)SP;
         st->flags = 0;
-        st->pad0 = 0;
+        st->copy_done = 0;
         st->high_water = 0;
         st->spill_high_water = 0;
         st->held = 0;
@@ -556,7 +555,8 @@ struct InlineArgs {
     int enabled; // 0: k_scan_plan ran before the copy
     int nblk, padded;
     int32_t *counts, *live; // dispatch outputs (seg_off is the copy kernel's own argument)
-    int64_t src_rows, max_pages;
+    int64_t src_rows;       // rows of the dispatch buffer (both paths: no dispatch row reaches past it)
+    int64_t max_pages;
 };
 
 struct InlinePlan {
@@ -602,19 +602,19 @@ __device__ __forceinline__ V block_exclusive_scan256(V v, V *ws, V *total)
 // of this block's tokens.  Ends with a barrier: pl is complete for the block.
 template <bool kVecReads>
 __device__ __forceinline__ void inline_plan(InlinePlan &pl, const int32_t *__restrict__ blk, int b, int E,
-                                            int capacity, const InlineArgs &ia, const RecPtr &rec, int P)
+                                            int capacity, const InlineArgs &ia, const ap_pool_state *st, int P)
 {
     constexpr int kPartials = kVecReads ? 1024 : 256;
     __shared__ __align__(16) int32_t s_lt[kPartials], s_all[kPartials]; // partial sums: [row group][expert]
     __shared__ int64_t s_ws[8];
     const int tid = threadIdx.x;
     const int nblk = ia.nblk;
-    if (tid == 0) {
+    if (tid == 0) { // the free rings as the previous call left them (the last block commits this call's)
         pl.bad = 0;
-        pl.head0 = rec.hdr->head0;
-        pl.sh0 = rec.hdr->spill_head0;
-        pl.tail0 = rec.hdr->tail0;
-        pl.stail0 = rec.hdr->spill_tail0;
+        pl.head0 = __ldcg(&st->head);
+        pl.sh0 = __ldcg(&st->spill_head);
+        pl.tail0 = __ldcg(&st->tail);
+        pl.stail0 = __ldcg(&st->spill_tail);
     }
     // each thread sums expert columns over a strided set of rows: the counts
     // of the rows before b (this block's base) and of all rows (totals).  One
@@ -721,11 +721,10 @@ __device__ __forceinline__ void inline_plan(InlinePlan &pl, const int32_t *__res
     __syncthreads();
 }
 
-// Block 0 of an inline-planned copy: the dispatch outputs, the record and the
-// pool state, exactly as k_scan_plan writes them.
+// Block 0 of an inline-planned copy: the dispatch outputs and the record,
+// exactly as k_scan_plan writes them (the pool state is inline_finish's).
 __device__ __forceinline__ void inline_commit(const InlinePlan &pl, int E, const InlineArgs &ia,
-                                              int32_t *__restrict__ seg_off, const RecPtr &rec, ap_pool_state *st,
-                                              const PageSpace &ps)
+                                              int32_t *__restrict__ seg_off, const RecPtr &rec)
 {
     const int tid = threadIdx.x;
     if (tid < E) {
@@ -738,29 +737,43 @@ __device__ __forceinline__ void inline_commit(const InlinePlan &pl, int E, const
     }
     if (tid == 0) {
         rec.pg_base[E] = pl.npages;
-        const int64_t kept = pl.kept, ndev = pl.ndev, nspill = pl.nspill;
-        const int64_t nlost = kept - ndev - nspill;
-        uint32_t f = pl.bad;
-        if (pl.npages > ia.max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
-        if (kept > ndev) f |= AP_FLAG_POOL_OVERFLOW;
-        if (nlost > 0) f |= AP_FLAG_SPILL_OVERFLOW;
         rec.hdr->nseg = E;
-        rec.hdr->npages = kept;
-        rec.hdr->ndev = ndev;
-        rec.hdr->nspill = nspill;
-        rec.hdr->nlost = nlost;
-        const StateSnap snap = load_state(st);
-        st->head = pl.head0 + (uint64_t)ndev;
-        st->spill_head = pl.sh0 + (uint64_t)nspill;
-        const int64_t in_use = ps.N - (int64_t)(pl.tail0 - (pl.head0 + (uint64_t)ndev));
-        if (in_use > snap.hw) st->high_water = in_use;
-        const int64_t s_use = ps.SP - (int64_t)(pl.stail0 - (pl.sh0 + (uint64_t)nspill));
-        if (s_use > snap.shw) st->spill_high_water = s_use;
-        const int64_t held = snap.held + kept;
-        st->held = held;
-        if (held > snap.hhw) st->held_high_water = held;
-        st->flags = snap.flags | f;
+        rec.hdr->npages = pl.kept;
+        rec.hdr->ndev = pl.ndev;
+        rec.hdr->nspill = pl.nspill;
+        rec.hdr->nlost = pl.kept - pl.ndev - pl.nspill;
+        rec.hdr->head0 = pl.head0;
+        rec.hdr->spill_head0 = pl.sh0;
     }
+}
+
+// Every block of an inline-planned copy, once its plan is complete: counts
+// itself in the state's copy_done; the last block to do so (every block has
+// read the free rings by then) moves the pool state on, as k_scan_plan does,
+// and clears the count for the next call.  The flags are or-ed in, since
+// other blocks may still be adding AP_FLAG_CORRUPT.
+__device__ __forceinline__ void inline_finish(const InlinePlan &pl, const InlineArgs &ia, ap_pool_state *st,
+                                              const PageSpace &ps)
+{
+    if (threadIdx.x != 0) return;
+    if (atomicAdd(&st->copy_done, 1u) + 1u != gridDim.x) return;
+    st->copy_done = 0;
+    const int64_t kept = pl.kept, ndev = pl.ndev, nspill = pl.nspill;
+    uint32_t f = pl.bad;
+    if (pl.npages > ia.max_pages) f |= AP_FLAG_RECORD_OVERFLOW;
+    if (kept > ndev) f |= AP_FLAG_POOL_OVERFLOW;
+    if (kept - ndev - nspill > 0) f |= AP_FLAG_SPILL_OVERFLOW;
+    const int64_t hw = __ldcg(&st->high_water), shw = __ldcg(&st->spill_high_water);
+    const int64_t held = __ldcg(&st->held) + kept, hhw = __ldcg(&st->held_high_water);
+    st->head = pl.head0 + (uint64_t)ndev;
+    st->spill_head = pl.sh0 + (uint64_t)nspill;
+    const int64_t in_use = ps.N - (int64_t)(pl.tail0 - (pl.head0 + (uint64_t)ndev));
+    if (in_use > hw) st->high_water = in_use;
+    const int64_t s_use = ps.SP - (int64_t)(pl.stail0 - (pl.sh0 + (uint64_t)nspill));
+    if (s_use > shw) st->spill_high_water = s_use;
+    st->held = held;
+    if (held > hhw) st->held_high_water = held;
+    if (f) atomicOr(&st->flags, f);
 }
 
 // A pair's dispatch row and, for a kept pair, its place in the record being
@@ -775,14 +788,15 @@ struct PairPlace {
     int64_t r;   // row within the expert segment (kept pairs)
     int64_t ord; // page ordinal in the record, or -1 (dropped, or past the record's live rows)
     int64_t lv;  // live rows of the expert segment in the record
+    bool bad;    // the rank put the row outside the dispatch buffer (dropped; AP_FLAG_BAD_COUNT)
 };
 
 __device__ __forceinline__ PairPlace resolve_pair(const int32_t *__restrict__ idx, int32_t *__restrict__ dest,
                                                   int32_t *__restrict__ src_tok, const int32_t *__restrict__ blk,
                                                   const int32_t *__restrict__ seg_off, const RecPtr &rec,
-                                                  int64_t t, int j, int k, int E, int capacity, int P)
+                                                  int64_t t, int j, int k, int E, int capacity, int P, int64_t rows)
 {
-    PairPlace pp{-1, 0, -1, 0};
+    PairPlace pp{-1, 0, -1, 0, false};
     const int64_t p = t * k + j;
     const int32_t lr = dest[p];
     const int e = idx[p];
@@ -791,7 +805,9 @@ __device__ __forceinline__ PairPlace resolve_pair(const int32_t *__restrict__ id
     const int32_t so = seg_off[e];
     const int64_t lv = rec.live[e], pg0 = rec.pg_base[e];
     const int32_t r = base + lr;
-    if (capacity <= 0 || r < capacity) {
+    if ((capacity <= 0 || r < capacity) && (uint64_t)((int64_t)so + r) >= (uint64_t)rows) {
+        pp.bad = true; // ranks that do not match the counts (ranked input)
+    } else if (capacity <= 0 || r < capacity) {
         pp.d = so + r;
         if (src_tok) src_tok[pp.d] = (int32_t)t;
         pp.r = r;
@@ -809,13 +825,16 @@ __device__ __forceinline__ PairPlace resolve_pair(const int32_t *__restrict__ id
 // lr and e: the pair's in-block rank (dest) and expert id, already loaded.
 __device__ __forceinline__ PairPlace resolve_pair_inline(int32_t lr, int e, int32_t *__restrict__ dest,
                                                          int32_t *__restrict__ src_tok, const InlinePlan &pl,
-                                                         int64_t t, int j, int k, int E, int capacity, int P)
+                                                         int64_t t, int j, int k, int E, int capacity, int P,
+                                                         int64_t rows)
 {
-    PairPlace pp{-1, 0, -1, 0};
+    PairPlace pp{-1, 0, -1, 0, false};
     const int64_t p = t * k + j;
     if (lr < 0 || e < 0 || e >= E) return pp; // an invalid expert id: dest is already -1
     const int32_t r = pl.base[e] + lr;
-    if (capacity <= 0 || r < capacity) {
+    if ((capacity <= 0 || r < capacity) && (uint64_t)((int64_t)pl.off[e] + r) >= (uint64_t)rows) {
+        pp.bad = true; // ranks that do not match the counts (ranked input)
+    } else if (capacity <= 0 || r < capacity) {
         pp.d = pl.off[e] + r;
         if (src_tok) src_tok[pp.d] = (int32_t)t;
         pp.r = r;
@@ -848,8 +867,9 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
     __shared__ InlinePlan pl;
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
         inline_plan<true>(pl, blk, (int)(((int64_t)blockIdx.x * (blockDim.x / kWarp)) / kTokPerBlk), E, capacity, ia,
-                    rec, P);
-        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
+                          st, P);
+        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec);
+        inline_finish(pl, ia, st, ps);
     }
     const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;
     const int64_t ndev = ia.enabled ? pl.ndev : rec.hdr->ndev, nspill = ia.enabled ? pl.nspill : rec.hdr->nspill;
@@ -860,8 +880,10 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
         if (lane < k) {
             const PairPlace pp =
                 ia.enabled ? resolve_pair_inline(dest[t * k + lane], idx[t * k + lane], dest, src_tok, pl, t, lane, k,
-                                                 E, capacity, P)
-                           : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+                                                 E, capacity, P, ia.src_rows)
+                           : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P,
+                                          ia.src_rows);
+            if (pp.bad) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
             my_d = pp.d;
             if (pp.ord >= 0 && pp.ord < npages) {
                 bool corrupt;
@@ -945,8 +967,9 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
     const int half0 = (nstep + 1) / 2;
     const int s_begin = h ? half0 : 0, s_end = h ? nstep : half0;
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
-        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
+        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, st, P);
+        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec);
+        inline_finish(pl, ia, st, ps);
     }
     const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;
     const int64_t ndev = ia.enabled ? pl.ndev : rec.hdr->ndev, nspill = ia.enabled ? pl.nspill : rec.hdr->nspill;
@@ -968,8 +991,10 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
             if (lane < k) {
                 const PairPlace pp =
                     ia.enabled ? resolve_pair_inline(dest[t * k + lane], idx[t * k + lane], dest, src_tok, pl, t,
-                                                     lane, k, E, capacity, P)
-                               : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+                                                     lane, k, E, capacity, P, ia.src_rows)
+                               : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P,
+                                              ia.src_rows);
+                if (pp.bad) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
                 my_d = pp.d;
                 if (pp.ord >= 0 && pp.ord < npages) {
                     bool corrupt;
@@ -1077,8 +1102,9 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3_units(
     const int ub = h ? u0 : 0, un = h ? nu - u0 : u0; // this warp's first unit and unit count
     const int la = h ? (lone ? nstep - 1 : -1) : (2 * u0 < nstep ? 2 * u0 : -1); // lookahead vector
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, rec, P);
-        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec, st, ps);
+        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, st, P);
+        if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec);
+        inline_finish(pl, ia, st, ps);
     }
     const int64_t npages = ia.enabled ? pl.kept : rec.hdr->npages;
     const int64_t ndev = ia.enabled ? pl.ndev : rec.hdr->ndev, nspill = ia.enabled ? pl.nspill : rec.hdr->nspill;
@@ -1102,8 +1128,10 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3_units(
             if (lane < k) {
                 const PairPlace pp =
                     ia.enabled ? resolve_pair_inline(dest[t * k + lane], idx[t * k + lane], dest, src_tok, pl, t,
-                                                     lane, k, E, capacity, P)
-                               : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P);
+                                                     lane, k, E, capacity, P, ia.src_rows)
+                               : resolve_pair(idx, dest, src_tok, blk, seg_off, rec, t, lane, k, E, capacity, P,
+                                              ia.src_rows);
+                if (pp.bad) atomicOr(&st->flags, AP_FLAG_BAD_COUNT);
                 my_d = pp.d;
                 if (pp.ord >= 0 && pp.ord < npages) {
                     bool corrupt;
@@ -1582,7 +1610,8 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
                               int32_t H, int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
                               int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows, int32_t *counts,
                               int32_t *live, int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
-                              int64_t scratch_bytes, uint32_t *d_status, uint64_t *record_id, void *stream)
+                              int64_t scratch_bytes, uint32_t *d_status, uint64_t *record_id, void *stream,
+                              bool ranked = false)
 {
     using namespace ap;
     if (!p) return fail(AP_EINVAL, "dispatch_stash: NULL pool");
@@ -1620,13 +1649,11 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     ap_pool_state *stt = reinterpret_cast<ap_pool_state *>(p->dev_meta);
     // few block counts: the copy kernel plans the record itself (no scan + plan launch)
     const bool inl = T > 0 && (int64_t)dispatch_blocks(T) * E <= ap::kInlineMaxCounts && E <= ap::kInlineMaxE;
-    const uint64_t *snap_src = inl ? &stt->head : nullptr;
-    uint64_t *snap_dst = inl ? &rec.hdr->head0 : nullptr;
-    s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, (int64_t)H * 2, snap_src,
-                                           snap_dst)
-               : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, (int64_t)H * 2, snap_src,
-                                     snap_dst);
-    if (s != AP_OK) return s;
+    if (!ranked) { // else dest and scratch hold ap_count_rank's results for idx
+        s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, (int64_t)H * 2)
+                   : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, (int64_t)H * 2);
+        if (s != AP_OK) return s;
+    }
 
     HostRec &h = p->q[index];
     h.id = p->next_id;
@@ -1642,13 +1669,13 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     if (bound > p->cfg.max_pages_per_record) bound = p->cfg.max_pages_per_record;
     h.bound_pages = bound;
     ap::InlineArgs ia{};
+    ia.src_rows = xd_rows; // the copy kernels' bound on a dispatch row
     if (inl) {
         ia.enabled = 1;
         ia.nblk = dispatch_blocks(T);
         ia.padded = padded;
         ia.counts = counts;
         ia.live = live;
-        ia.src_rows = xd_rows;
         ia.max_pages = p->cfg.max_pages_per_record;
     } else {
         ap::launch(ap::k_scan_plan, 1, ap::kPlanThreads, 0, st, static_cast<int32_t *>(scratch), dispatch_blocks(T),
@@ -1737,6 +1764,19 @@ extern "C" ap_status ap_route_dispatch_stash(ap_pool *p, int32_t slot, const flo
     return dispatch_stash_impl(p, slot, logits ? logits : &kNoLogits, w, x, T, H, idx, k, E, capacity, padded,
                                out_dtype, xd, xd_scale, xd_rows, counts, live, seg_off, dest, src_tok, scratch,
                                scratch_bytes, d_status, record_id, stream);
+}
+
+extern "C" ap_status ap_dispatch_stash_ranked(ap_pool *p, int32_t slot, const void *x, int64_t T, int32_t H,
+                                              const int32_t *idx, int32_t k, int32_t E, int32_t capacity,
+                                              int32_t padded, int32_t out_dtype, void *xd, float *xd_scale,
+                                              int64_t xd_rows, int32_t *counts, int32_t *live, int32_t *seg_off,
+                                              int32_t *dest, int32_t *src_tok, void *scratch, int64_t scratch_bytes,
+                                              uint32_t *d_status, uint64_t *record_id, void *stream)
+{
+    AP_NVTX_RANGE("ap_dispatch_stash_ranked");
+    return dispatch_stash_impl(p, slot, nullptr, nullptr, x, T, H, const_cast<int32_t *>(idx), k, E, capacity,
+                               padded, out_dtype, xd, xd_scale, xd_rows, counts, live, seg_off, dest, src_tok,
+                               scratch, scratch_bytes, d_status, record_id, stream, true);
 }
 
 extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, void *const *dst_planes,

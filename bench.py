@@ -304,16 +304,18 @@ class Step:
             fork = torch.cuda.Event()
             fork.record(s)
             side.wait_event(fork)
-            with torch.cuda.stream(side):
-                ap.route_topk(d1["logits"], wl.k, d1["idx"], d1["w"], stream=side)
+            with torch.cuda.stream(side):  # chunk 1 routed, counted and ranked beside chunk 0's call
+                ap.count_rank(wl.E, logits=d1["logits"], k=wl.k, x=d1["x"], stream=side,
+                              out={"idx": d1["idx"], "w": d1["w"], "dest": d1["disp"]["dest"],
+                                   "scratch": d1["disp"]["scratch"]})
                 r1 = torch.cuda.Event()
                 r1.record(side)
             # chunk 0: routing inside its dispatch + push (one launch fewer on
-            # the paging stream); chunk 1 was routed on the side stream
+            # the paging stream); chunk 1's copy follows it directly
             self.pool.route_dispatch_stash(0, d0["logits"], d0["x"], wl.k, wl.E,
                                            out=dict(d0["disp"], idx=d0["idx"], w=d0["w"]))
             s.wait_event(r1)
-            self.pool.dispatch_stash(0, d1["x"], d1["idx"], wl.E, out=d1["disp"])
+            self.pool.dispatch_stash(0, d1["x"], d1["idx"], wl.E, out=d1["disp"], ranked=True)
             self.pool.pop(0, [d0["dst"]])
             p0 = torch.cuda.Event()
             p0.record(s)
@@ -916,13 +918,15 @@ class ScheduleStep:
             for op, name in self.sched:
                 d = self.src[name]
                 if op == "push":
-                    with torch.cuda.stream(side):
-                        ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=side)
+                    with torch.cuda.stream(side):  # routing and count/rank ahead of the copy
+                        ap.count_rank(wl.E, logits=d["logits"], k=wl.k, x=d["x"], stream=side,
+                                      out={"idx": d["idx"], "w": d["w"], "dest": d["disp"]["dest"],
+                                           "scratch": d["disp"]["scratch"]})
                         routed = torch.cuda.Event()
                         routed.record(side)
                     s.wait_event(routed)
                     self.pool.dispatch_stash(d["slot"], d["x"], d["idx"], wl.E, wl.capacity, wl.padded, fp8=wl.fp8,
-                                             out=d["disp"])
+                                             out=d["disp"], ranked=True)
                 else:
                     self.pool.pop(d["slot"], self.dst)
                     popped = torch.cuda.Event()
@@ -1117,8 +1121,8 @@ def measure_schedule(wl, device, passes=None, op_passes=1, warmup=3, target_s=0.
                           "spill_pages": wl.spill_pages, "records_per_pass": sum(1 for op, _ in st.sched
                                                                                  if op == "push"),
                           "launch": "CUDA graph of the whole schedule: pool calls on the paging stream in schedule "
-                                    "order, each routing ahead of its push and each combine after its pop on a "
-                                    "second stream"},
+                                    "order (each push ranked: ap_dispatch_stash_ranked), each routing + count/rank "
+                                    "ahead of its push and each combine after its pop on a second stream"},
                "ops": ops, "pool_flags": flags, "gpu_launches_per_pass": launches_per_pass, "clocks": clocks}
         if bound:
             res["link_bound"] = bound
@@ -1386,8 +1390,9 @@ def native(args):
 
     launched_as = ("eager" if graph is None else
                    "CUDA graph of one step, replayed" + ("" if (args.serial or not fused_main)
-                                                         else "; chunk 1 routing and chunk 0 combine on a second "
-                                                              "stream"))
+                                                         else "; chunk 1 routing + count/rank (ap_count_rank, its "
+                                                              "dispatch + push then ranked) and chunk 0 combine on a "
+                                                              "second stream"))
     overlap = None
     if not args.no_overlap and world == 1:
         overlap = {"beside_gemm": overlap_report(step, device), "sm_split": sm_split_report(step, device),

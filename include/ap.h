@@ -281,7 +281,10 @@ typedef struct {
     uint64_t head, tail;             /* free device ring: free = tail - head   */
     uint64_t spill_head, spill_tail; /* free spill ring                        */
     uint32_t flags;                  /* sticky AP_FLAG_* bits                  */
-    uint32_t pad0;
+    uint32_t copy_done;              /* blocks of the running fused copy that
+                                        have read the rings (its last block
+                                        moves the state on and sets it back
+                                        to 0); 0 between calls                */
     int64_t high_water;              /* most device pages ever in use          */
     int64_t spill_high_water;        /* most spill pages ever in use           */
     int64_t held;                    /* pages (device + spill + lost) of the
@@ -408,6 +411,43 @@ ap_status ap_route_dispatch_stash(ap_pool *pool, int32_t slot, const float *logi
                                   int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest,
                                   int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
                                   uint64_t *record_id, void *stream);
+
+/* Count/rank alone, on any stream: the first launch of ap_dispatch_stash
+ * (and, with logits != NULL, of ap_route_dispatch_stash, routing into idx
+ * and w first), for callers that overlap it with other work and then call
+ * ap_dispatch_stash_ranked on the paging stream.  The ranking of pairs is the
+ * one ap_dispatch_permute documents (t-then-j order within each expert).
+ *
+ *   logits   [T, E] f32 (device, read) or NULL: idx is then an input
+ *   w        [T, k] f32 (device, written when logits != NULL, else unused)
+ *   idx      [T, k] int32 (device; written when logits != NULL, else read)
+ *   x        the [T, row_bytes] rows the later copy reads (device, may be
+ *            NULL): prefetched into L2 as a hint when 16-byte aligned
+ *   dest     [T, k] int32 (device, written): each pair's rank inside its
+ *            block of 64 tokens, -1 for an id outside [0, E)
+ *   scratch  ap_dispatch_scratch_bytes(T, k, E) bytes (device, written): the
+ *            blocks' expert histograms
+ *   d_status device uint32 word (may be NULL): AP_FLAG_BAD_INDEX for an id
+ *            outside [0, E)
+ * Limits and errors as ap_dispatch_permute (plus AP_EINVAL for k > E with
+ * logits, NULL w with logits and T > 0, or row_bytes < 0). */
+ap_status ap_count_rank(const float *logits, float *w, int32_t *idx, int64_t T, int32_t k, int32_t E,
+                        const void *x, int64_t row_bytes, int32_t *dest, void *scratch, int64_t scratch_bytes,
+                        uint32_t *d_status, void *stream);
+
+/* ap_dispatch_stash without its count/rank launch: dest and scratch must
+ * hold the results of ap_count_rank for the same idx, T, k and E, ordered
+ * before this call (an event, or the same stream); idx, dest and scratch
+ * must not change between the two calls.  Same arguments, results and
+ * errors as ap_dispatch_stash.  Ranks that do not match the counts put no
+ * row outside the dispatch buffer or a page: such a pair is dropped
+ * (dest -1) and AP_FLAG_BAD_COUNT is set. */
+ap_status ap_dispatch_stash_ranked(ap_pool *pool, int32_t slot, const void *x, int64_t T, int32_t H,
+                                   const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
+                                   int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows,
+                                   int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest,
+                                   int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
+                                   uint64_t *record_id, void *stream);
 
 /* Pop the oldest record of `slot` into dst_planes (host array of nplanes
  * device pointers, each [dst_rows, row_bytes of the push]).  A page whose

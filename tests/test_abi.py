@@ -126,6 +126,30 @@ def test_dispatch_rejects_bad_arguments(lib):
     assert call(E=2000) == -1
 
 
+def test_count_rank_rejects_bad_arguments(lib):
+    """ap_count_rank checks its sizes, work space and pointers before any
+    launch (no GPU is touched), and ap_dispatch_stash_ranked a NULL pool."""
+    p = ctypes.c_void_p(256)
+    n = ctypes.c_int64()
+    assert lib.ap_dispatch_scratch_bytes(1000, 8, 128, ctypes.byref(n)) == 0
+
+    def call(logits=None, w=None, idx=p, T=1000, k=8, E=128, x=None, rb=0, dest=p, scratch=p, sb=n.value):
+        return lib.ap_count_rank(logits, w, idx, T, k, E, x, rb, dest, scratch, sb, None, None)
+    n0 = lib.ap_launch_count()
+    assert call(k=0) == -1
+    assert call(k=33) == -1
+    assert call(E=2000) == -1
+    assert call(logits=p, w=p, k=8, E=4) == -1   # routing needs k <= E
+    assert call(logits=p, w=None) == -1          # routing writes w
+    assert call(sb=n.value - 256) == -1          # work space too small
+    assert call(dest=None) == -1
+    assert call(rb=-1) == -1
+    assert b"count_rank" in lib.ap_last_error()
+    assert lib.ap_launch_count() == n0
+    assert lib.ap_dispatch_stash_ranked(None, 0, p, 10, 64, p, 2, 8, 0, 0, 0, p, None, 20, p, p, p, p, None, p,
+                                        n.value, None, None, None) == -1
+
+
 def test_combine_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(256)
     assert lib.ap_combine_unpermute(p, 10, 0, p, p, 4, 2, p, None, None) == -1   # H = 0
