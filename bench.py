@@ -305,9 +305,7 @@ class Step:
             fork.record(s)
             side.wait_event(fork)
             with torch.cuda.stream(side):  # chunk 1 routed, counted and ranked beside chunk 0's call
-                ap.count_rank(wl.E, logits=d1["logits"], k=wl.k, x=d1["x"], stream=side,
-                              out={"idx": d1["idx"], "w": d1["w"], "dest": d1["disp"]["dest"],
-                                   "scratch": d1["disp"]["scratch"]})
+                rank_beside(ap, wl, d1, side)
                 r1 = torch.cuda.Event()
                 r1.record(side)
             # chunk 0: routing inside its dispatch + push (one launch fewer on
@@ -814,6 +812,23 @@ def sm_partition_report(step, device, sizes=(8, 16, 24, 32, 48), reps=9, gemm_re
     return out
 
 
+def rank_beside(ap, wl, d, side, prefetch=True):
+    """Route and count/rank one source on the second stream, for its ranked
+    dispatch + push on the paging stream.  A record of at most 64 count/rank
+    blocks takes the one routing + count/rank launch; its 1024-thread blocks
+    hold whole SMs, so beside a copy of a larger record they would start only
+    in its tail, and those take routing and count/rank as two small-block
+    launches.  prefetch: the count/rank prefetches the rows into L2."""
+    x = d["x"] if prefetch else None
+    if (wl.T + 63) // 64 <= 64:
+        ap.count_rank(wl.E, logits=d["logits"], k=wl.k, x=x, stream=side,
+                      out={"idx": d["idx"], "w": d["w"], "dest": d["disp"]["dest"], "scratch": d["disp"]["scratch"]})
+    else:
+        ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=side)
+        ap.count_rank(wl.E, idx=d["idx"], x=x, stream=side,
+                      out={"dest": d["disp"]["dest"], "scratch": d["disp"]["scratch"]})
+
+
 def push_records(step):
     """Stash every chunk's dispatch rows again (on the paging stream)."""
     import torch
@@ -919,9 +934,7 @@ class ScheduleStep:
                 d = self.src[name]
                 if op == "push":
                     with torch.cuda.stream(side):  # routing and count/rank ahead of the copy
-                        ap.count_rank(wl.E, logits=d["logits"], k=wl.k, x=d["x"], stream=side,
-                                      out={"idx": d["idx"], "w": d["w"], "dest": d["disp"]["dest"],
-                                           "scratch": d["disp"]["scratch"]})
+                        rank_beside(ap, wl, d, side)
                         routed = torch.cuda.Event()
                         routed.record(side)
                     s.wait_event(routed)
