@@ -13,6 +13,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 namespace {
 
 struct Green {
@@ -48,9 +50,8 @@ bool entry(const char *name, F *fn)
 const Green &green()
 {
     static Green g;
-    static bool done = false;
-    if (!done) {
-        done = true;
+    static std::once_flag once;
+    std::call_once(once, [] {
         const bool found[] = {entry("cuDeviceGet", &g.device_get),
                               entry("cuDeviceGetDevResource", &g.get_resource),
                               entry("cuDevSmResourceSplitByCount", &g.split),
@@ -65,7 +66,7 @@ const Green &green()
                 g.ok = false;
                 g.missing = i + 1;
             }
-    }
+    });
     return g;
 }
 
