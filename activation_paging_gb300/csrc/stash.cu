@@ -805,8 +805,8 @@ __device__ __forceinline__ PairPlace resolve_pair(const int32_t *__restrict__ id
     const int32_t so = seg_off[e];
     const int64_t lv = rec.live[e], pg0 = rec.pg_base[e];
     const int32_t r = base + lr;
-    if ((capacity <= 0 || r < capacity) && (uint64_t)((int64_t)so + r) >= (uint64_t)rows) {
-        pp.bad = true; // ranks that do not match the counts (ranked input)
+    if ((capacity <= 0 || r < capacity) && (r < 0 || (uint64_t)((int64_t)so + r) >= (uint64_t)rows)) {
+        pp.bad = true; // ranks that do not match the counts (ranked input): no row outside xd or a page
     } else if (capacity <= 0 || r < capacity) {
         pp.d = so + r;
         if (src_tok) src_tok[pp.d] = (int32_t)t;
@@ -832,8 +832,8 @@ __device__ __forceinline__ PairPlace resolve_pair_inline(int32_t lr, int e, int3
     const int64_t p = t * k + j;
     if (lr < 0 || e < 0 || e >= E) return pp; // an invalid expert id: dest is already -1
     const int32_t r = pl.base[e] + lr;
-    if ((capacity <= 0 || r < capacity) && (uint64_t)((int64_t)pl.off[e] + r) >= (uint64_t)rows) {
-        pp.bad = true; // ranks that do not match the counts (ranked input)
+    if ((capacity <= 0 || r < capacity) && (r < 0 || (uint64_t)((int64_t)pl.off[e] + r) >= (uint64_t)rows)) {
+        pp.bad = true; // ranks that do not match the counts (ranked input): no row outside xd or a page
     } else if (capacity <= 0 || r < capacity) {
         pp.d = pl.off[e] + r;
         if (src_tok) src_tok[pp.d] = (int32_t)t;

@@ -439,9 +439,11 @@ ap_status ap_count_rank(const float *logits, float *w, int32_t *idx, int64_t T, 
  * hold the results of ap_count_rank for the same idx, T, k and E, ordered
  * before this call (an event, or the same stream); idx, dest and scratch
  * must not change between the two calls.  Same arguments, results and
- * errors as ap_dispatch_stash.  Ranks that do not match the counts put no
- * row outside the dispatch buffer or a page: such a pair is dropped
- * (dest -1) and AP_FLAG_BAD_COUNT is set. */
+ * errors as ap_dispatch_stash.  Ranks or histograms that do not match idx
+ * leave the dispatch rows, the record and the pool's contents unspecified,
+ * but no write leaves the dispatch buffer, the pages or the metadata: a
+ * pair whose row would fall outside its buffer or page is dropped (dest -1)
+ * and AP_FLAG_BAD_COUNT is set. */
 ap_status ap_dispatch_stash_ranked(ap_pool *pool, int32_t slot, const void *x, int64_t T, int32_t H,
                                    const int32_t *idx, int32_t k, int32_t E, int32_t capacity, int32_t padded,
                                    int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows,
