@@ -542,10 +542,11 @@ __global__ void __launch_bounds__(kCopyThreads, 4) k_pop_copy(ap_pool_state *st,
 // kernel would have written, from the count/rank output, in a prologue: its
 // own base rank per expert (the counts of the earlier count/rank blocks), the
 // expert totals, live counts, segment offsets, the record's page ordinals
-// and the allocation (from the free-ring counters count/rank copied into the
-// record header).  Block 0 then writes the dispatch outputs, the record and
-// the pool state; no other block reads those, and the kernel after this one
-// on the paging stream waits for it.  Each block's tokens lie in one
+// and the allocation (from the pool's free-ring counters, read after the
+// dependency wait).  Block 0 then writes the dispatch outputs and the
+// record, and the last block to finish its plan moves the pool state on
+// (inline_finish); no other block reads those, and the kernel after this
+// one on the paging stream waits for it.  Each block's tokens lie in one
 // count/rank block (its first token is a multiple of its token count, which
 // divides kTokPerBlk) and the grid covers every token in one pass.
 constexpr int kInlineMaxE = 256;

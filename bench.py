@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -1192,6 +1193,10 @@ def kernel_hash() -> str:
     dev = stash[stash.index("// ---- kernels"):stash.index("// ---- host runtime")]
     dev += common[common.index("// ---- device helpers"):]
     dev += open(os.path.join(csrc, "dispatch_scan.cuh")).read()  # device helpers of the fused copies
+    # the code alone: comments and blank lines do not change a kernel
+    dev = re.sub(r"/\*.*?\*/", "", dev, flags=re.S)
+    dev = "\n".join(line.split("//")[0].rstrip() for line in dev.splitlines())
+    dev = "\n".join(line for line in dev.splitlines() if line)
     return hashlib.sha256(dev.encode()).hexdigest()[:16]
 
 
