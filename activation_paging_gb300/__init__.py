@@ -82,14 +82,16 @@ def dispatch_scratch_bytes(T: int, k: int, E: int) -> int:
 
 def count_rank(E: int, idx: torch.Tensor | None = None, logits: torch.Tensor | None = None, k: int | None = None,
                x: torch.Tensor | None = None, out: dict | None = None, status: torch.Tensor | None = None,
-               stream=None) -> dict:
+               stream=None, scan: bool = False, capacity: int = 0, padded: bool = False) -> dict:
     """Count/rank alone (``ap_count_rank``) on ``stream`` (default: the
     current stream): ``dest`` ([T, k] int32 ranks inside blocks of 64 tokens)
     and ``scratch`` (the blocks' expert histograms), for a later
     ``Pool.dispatch_stash(..., ranked=True, out=...)`` ordered after it.  With
     ``logits`` ([T, E] float32) it routes first and adds ``idx`` and ``w``;
     else ``idx`` is read.  ``x``: the rows the copy will read (an L2
-    prefetch hint)."""
+    prefetch hint).  ``scan``: also the dispatch's expert scan for
+    ``capacity`` / ``padded`` (adds ``counts``, ``live``, ``seg_off``; the
+    scratch then holds block bases, and the dict is marked ``scanned``)."""
     o = dict(out) if out is not None else {}
     if logits is not None:
         _need(logits, torch.float32, "logits")
@@ -110,10 +112,16 @@ def count_rank(E: int, idx: torch.Tensor | None = None, logits: torch.Tensor | N
     sb = dispatch_scratch_bytes(T, k, E)
     if "scratch" not in o or o["scratch"].numel() < sb:
         o["scratch"] = torch.empty(sb, dtype=torch.uint8, device=dev)
+    if scan:
+        for name in ("counts", "live", "seg_off"):
+            if name not in o:
+                o[name] = torch.empty(E, dtype=torch.int32, device=dev)
     rb = x.shape[1] * x.element_size() if x is not None else 0
     check(lib().ap_count_rank(_p(logits), _p(o.get("w") if logits is not None else None), _p(idx), T, k, E, _p(x), rb,
-                              _p(o["dest"]), _p(o["scratch"]), o["scratch"].numel(), _p(status), _stream(stream)),
-          "count_rank")
+                              _p(o["dest"]), _p(o["scratch"]), o["scratch"].numel(), capacity, int(padded),
+                              _p(o["counts"] if scan else None), _p(o["live"] if scan else None),
+                              _p(o["seg_off"] if scan else None), _p(status), _stream(stream)), "count_rank")
+    o["scanned"] = scan
     return o
 
 
@@ -418,12 +426,16 @@ class Pool:
         row scales as two planes): returns the dispatch dict (as
         ``dispatch_permute``) with the record id under ``record_id``.
         ``ranked``: ``out`` holds ``count_rank``'s ``dest`` and ``scratch``
-        for this idx (``ap_dispatch_stash_ranked``: no count/rank launch); the
-        paging stream must already be ordered after the stream that ran it
-        (this call orders it after the caller's current stream)."""
+        for this idx (``ap_dispatch_stash_ranked``: no count/rank launch), and
+        its ``counts``, ``live`` and ``seg_off`` when it ran the scan
+        (``out["scanned"]``, for the same capacity and padded); the paging
+        stream must already be ordered after the stream that ran it (this
+        call orders it after the caller's current stream)."""
         _need(idx, torch.int32, "idx")
         if ranked and (out is None or "dest" not in out or "scratch" not in out):
             raise ValueError("ranked dispatch_stash needs out['dest'] and out['scratch'] from count_rank")
+        if ranked and out.get("scanned") and any(n not in out for n in ("counts", "live", "seg_off")):
+            raise ValueError("a scanned count_rank's counts, live and seg_off belong in out")
         return self._dispatch_stash(slot, x, idx, idx.shape[1], E, capacity, padded, fp8, out, status, ranked=ranked)
 
     def route_dispatch_stash(self, slot: int, logits: torch.Tensor, x: torch.Tensor, k: int, E: int | None = None,
@@ -470,8 +482,10 @@ class Pool:
                 _p(o["counts"]), _p(o["live"]), _p(o["seg_off"]), _p(o["dest"]), _p(o["src_tok"]), _p(o["scratch"]),
                 o["scratch"].numel(), _p(status), ctypes.byref(rid), self.stream.cuda_stream)
         if ranked:
+            scanned = int(bool(o.get("scanned", False)))
             check(self.lib.ap_dispatch_stash_ranked(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity,
-                                                    int(padded), *tail), "dispatch_stash_ranked")
+                                                    int(padded), *tail[:-1], scanned, tail[-1]),
+                  "dispatch_stash_ranked")
         elif logits is None:
             check(self.lib.ap_dispatch_stash(self.handle, slot, _p(x), T, H, _p(idx), k, E, capacity, int(padded),
                                              *tail), "dispatch_stash")

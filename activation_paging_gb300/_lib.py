@@ -57,8 +57,8 @@ SIGNATURES = {
     "ap_dispatch_stash": (i32, [P, i32, P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P, i64, P,
                                 P, P]),
     "ap_dispatch_stash_ranked": (i32, [P, i32, P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P,
-                                       i64, P, P, P]),
-    "ap_count_rank": (i32, [P, P, P, i64, i32, i32, P, i64, P, P, i64, P, P]),
+                                       i64, P, P, i32, P]),
+    "ap_count_rank": (i32, [P, P, P, i64, i32, i32, P, i64, P, P, i64, i32, i32, P, P, P, P, P]),
     "ap_pool_time_copies": (i32, [P, P, P]),
     "ap_route_dispatch_stash": (i32, [P, i32, P, P, P, i64, i32, P, i32, i32, i32, i32, i32, P, P, i64, P, P, P, P,
                                       P, P, i64, P, P, P]),

@@ -582,7 +582,8 @@ extern "C" ap_status ap_dispatch_permute(const void *x, int64_t T, int32_t H, co
 
 extern "C" ap_status ap_count_rank(const float *logits, float *w, int32_t *idx, int64_t T, int32_t k, int32_t E,
                                    const void *x, int64_t row_bytes, int32_t *dest, void *scratch,
-                                   int64_t scratch_bytes, uint32_t *d_status, void *stream)
+                                   int64_t scratch_bytes, int32_t capacity, int32_t padded, int32_t *counts,
+                                   int32_t *live, int32_t *seg_off, uint32_t *d_status, void *stream)
 {
     AP_NVTX_RANGE("ap_count_rank");
     using namespace ap;
@@ -595,9 +596,20 @@ extern "C" ap_status ap_count_rank(const float *logits, float *w, int32_t *idx, 
         return fail(AP_EINVAL, "count_rank: scratch %lld < %lld bytes", (long long)scratch_bytes, (long long)need);
     if (!scratch || (T > 0 && (!idx || !dest || (logits && !w)))) return fail(AP_EINVAL, "count_rank: NULL pointer");
     if (row_bytes < 0) return fail(AP_EINVAL, "count_rank: row_bytes %lld < 0", (long long)row_bytes);
+    const bool scan = counts || live || seg_off;
+    if (scan && (!counts || !live || !seg_off)) return fail(AP_EINVAL, "count_rank: counts, live, seg_off: all or none");
+    if (scan && padded && capacity <= 0) return fail(AP_EINVAL, "count_rank: padded layout needs capacity > 0");
     cudaStream_t st = (cudaStream_t)stream;
-    return logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, row_bytes)
-                  : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, row_bytes);
+    ap_status s = logits ? dispatch_route_count_rank(logits, T, E, k, idx, w, scratch, dest, st, x, row_bytes)
+                         : dispatch_count_rank(T, idx, k, E, scratch, dest, d_status, st, x, row_bytes);
+    if (s != AP_OK || !scan) return s;
+    // the dispatch's expert scan: block bases in place of the histograms, counts, live, seg_off
+    // the fewest threads the scan takes (at least E): a small block finds room beside running copies sooner
+    const int threads = E <= 256 ? 256 : (E <= 512 ? 512 : 1024);
+    launch(k_scan, 1, threads, 0, st, static_cast<int32_t *>(scratch), (int)nblocks(T), E, capacity, padded, counts,
+           live, seg_off);
+    AP_CHECK_LAUNCH("count_rank scan launch");
+    return AP_OK;
 }
 
 extern "C" ap_status ap_cast_e4m3(const float *in, uint8_t *out, int64_t n, void *stream)

@@ -412,6 +412,20 @@ __global__ void __launch_bounds__(kPlanThreads) k_scan_plan(int32_t *__restrict_
                    my_live);
 }
 
+// Fused dispatch + stash whose expert scan already ran (ap_count_rank with the
+// scan): the record's page plan alone, from the dispatch's offsets and live
+// counts; the copy writes the page descriptors, as after k_scan_plan.
+__global__ void __launch_bounds__(kPlanThreads) k_scanned_plan(ap_pool_state *st, RecPtr rec, int nseg,
+                                                                const int32_t *__restrict__ seg_off,
+                                                                const int32_t *__restrict__ live, int64_t src_rows,
+                                                                int P, int64_t max_pages, int64_t N, int64_t SP)
+{
+    pdl_begin();
+    StateSnap snap;
+    if (threadIdx.x == 0) snap = load_state(st);
+    push_plan_body(st, rec, nseg, seg_off, live, src_rows, P, max_pages, N, SP, snap, false);
+}
+
 struct Planes {
     uint8_t *p[2];
     int64_t rb[2];
@@ -553,7 +567,8 @@ constexpr int kInlineMaxE = 256;
 constexpr int kInlineMaxCounts = 16384;
 
 struct InlineArgs {
-    int enabled; // 0: k_scan_plan ran before the copy
+    int enabled; // 0: a plan kernel ran before the copy; 1: the copy plans the record from the count/rank
+                 // block histograms; 2: from the expert scan's block bases, live counts and offsets
     int nblk, padded;
     int32_t *counts, *live; // dispatch outputs (seg_off is the copy kernel's own argument)
     int64_t src_rows;       // rows of the dispatch buffer (both paths: no dispatch row reaches past it)
@@ -722,6 +737,58 @@ __device__ __forceinline__ void inline_plan(InlinePlan &pl, const int32_t *__res
     __syncthreads();
 }
 
+// The prologue of a copy whose record's expert scan already ran (mode 2: the
+// scratch holds each count/rank block's base rank per expert, and seg_off and
+// ia.live the dispatch's offsets and live counts): the record's page ordinals
+// and the allocation alone.  b: the count/rank block of this block's tokens.
+// Ends with a barrier: pl is complete for the block.
+__device__ __forceinline__ void inline_plan_scanned(InlinePlan &pl, const int32_t *__restrict__ blk, int b, int E,
+                                                    const int32_t *__restrict__ seg_off, const InlineArgs &ia,
+                                                    const ap_pool_state *st, int P)
+{
+    __shared__ int64_t s_ws[8];
+    const int tid = threadIdx.x;
+    if (tid == 0) { // the free rings as the previous call left them (the last block commits this call's)
+        pl.bad = 0;
+        pl.head0 = __ldcg(&st->head);
+        pl.sh0 = __ldcg(&st->spill_head);
+        pl.tail0 = __ldcg(&st->tail);
+        pl.stail0 = __ldcg(&st->spill_tail);
+    }
+    int32_t base = 0, off = 0, l = 0;
+    if (tid < E) {
+        base = blk[(int64_t)b * E + tid];
+        off = seg_off[tid];
+        l = ia.live[tid];
+    }
+    // a segment outside the rows is not copied (as k_scan_plan)
+    const bool out = tid < E && (l < 0 || off < 0 || (int64_t)off + (int64_t)l > ia.src_rows);
+    const int32_t lr = out ? 0 : l;
+    int64_t npages;
+    const int64_t pg = block_exclusive_scan256<int64_t>((tid < E) ? ((int64_t)lr + P - 1) / P : 0, s_ws, &npages);
+    if (out) atomicOr(&pl.bad, AP_FLAG_BAD_COUNT); // after the scan's barriers: pl.bad is initialised
+    if (tid < E) {
+        pl.base[tid] = base;
+        pl.off[tid] = off;
+        pl.lrec[tid] = lr;
+        pl.pg[tid] = pg;
+    }
+    if (tid == 0) {
+        pl.pg[E] = npages;
+        pl.npages = npages;
+        const int64_t kept = npages < ia.max_pages ? npages : ia.max_pages;
+        const int64_t avail = (int64_t)(pl.tail0 - pl.head0);
+        const int64_t savail = (int64_t)(pl.stail0 - pl.sh0);
+        const int64_t ndev = kept < avail ? kept : avail;
+        int64_t nspill = kept - ndev;
+        if (nspill > savail) nspill = savail;
+        pl.kept = kept;
+        pl.ndev = ndev;
+        pl.nspill = nspill;
+    }
+    __syncthreads();
+}
+
 // Block 0 of an inline-planned copy: the dispatch outputs and the record,
 // exactly as k_scan_plan writes them (the pool state is inline_finish's).
 __device__ __forceinline__ void inline_commit(const InlinePlan &pl, int E, const InlineArgs &ia,
@@ -729,9 +796,11 @@ __device__ __forceinline__ void inline_commit(const InlinePlan &pl, int E, const
 {
     const int tid = threadIdx.x;
     if (tid < E) {
-        ia.counts[tid] = pl.tot[tid];
-        ia.live[tid] = pl.ldisp[tid];
-        seg_off[tid] = pl.off[tid];
+        if (ia.enabled == 1) { // in mode 2 the expert scan wrote them
+            ia.counts[tid] = pl.tot[tid];
+            ia.live[tid] = pl.ldisp[tid];
+            seg_off[tid] = pl.off[tid];
+        }
         rec.seg_off[tid] = pl.off[tid];
         rec.live[tid] = pl.lrec[tid];
         rec.pg_base[tid] = pl.pg[tid];
@@ -867,8 +936,9 @@ __global__ void __launch_bounds__(256) k_dispatch_stash_copy(const uint8_t *__re
     const int64_t nvec = rb / (int64_t)sizeof(V);
     __shared__ InlinePlan pl;
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan<true>(pl, blk, (int)(((int64_t)blockIdx.x * (blockDim.x / kWarp)) / kTokPerBlk), E, capacity, ia,
-                          st, P);
+        const int b = (int)(((int64_t)blockIdx.x * (blockDim.x / kWarp)) / kTokPerBlk);
+        if (ia.enabled == 2) inline_plan_scanned(pl, blk, b, E, seg_off, ia, st, P);
+        else inline_plan<true>(pl, blk, b, E, capacity, ia, st, P);
         if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec);
         inline_finish(pl, ia, st, ps);
     }
@@ -968,7 +1038,9 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3(
     const int half0 = (nstep + 1) / 2;
     const int s_begin = h ? half0 : 0, s_end = h ? nstep : half0;
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, st, P);
+        const int b = (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk);
+        if (ia.enabled == 2) inline_plan_scanned(pl, blk, b, E, seg_off, ia, st, P);
+        else inline_plan<false>(pl, blk, b, E, capacity, ia, st, P);
         if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec);
         inline_finish(pl, ia, st, ps);
     }
@@ -1103,7 +1175,9 @@ __global__ void __launch_bounds__(256, 4) k_dispatch_stash_e4m3_units(
     const int ub = h ? u0 : 0, un = h ? nu - u0 : u0; // this warp's first unit and unit count
     const int la = h ? (lone ? nstep - 1 : -1) : (2 * u0 < nstep ? 2 * u0 : -1); // lookahead vector
     if (ia.enabled) { // the record is planned here: this block's tokens lie in one count/rank block
-        inline_plan<false>(pl, blk, (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk), E, capacity, ia, st, P);
+        const int b = (int)(((int64_t)blockIdx.x * kPairs) / kTokPerBlk);
+        if (ia.enabled == 2) inline_plan_scanned(pl, blk, b, E, seg_off, ia, st, P);
+        else inline_plan<false>(pl, blk, b, E, capacity, ia, st, P);
         if (blockIdx.x == 0) inline_commit(pl, E, ia, seg_off, rec);
         inline_finish(pl, ia, st, ps);
     }
@@ -1612,7 +1686,7 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
                               int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows, int32_t *counts,
                               int32_t *live, int32_t *seg_off, int32_t *dest, int32_t *src_tok, void *scratch,
                               int64_t scratch_bytes, uint32_t *d_status, uint64_t *record_id, void *stream,
-                              bool ranked = false)
+                              bool ranked = false, bool scanned = false)
 {
     using namespace ap;
     if (!p) return fail(AP_EINVAL, "dispatch_stash: NULL pool");
@@ -1672,12 +1746,17 @@ ap_status dispatch_stash_impl(ap_pool *p, int32_t slot, const float *logits, flo
     ap::InlineArgs ia{};
     ia.src_rows = xd_rows; // the copy kernels' bound on a dispatch row
     if (inl) {
-        ia.enabled = 1;
+        ia.enabled = scanned ? 2 : 1;
         ia.nblk = dispatch_blocks(T);
         ia.padded = padded;
         ia.counts = counts;
         ia.live = live;
         ia.max_pages = p->cfg.max_pages_per_record;
+    } else if (scanned) { // the expert scan ran with the count/rank: the page plan alone
+        ap::launch(ap::k_scanned_plan, 1, ap::kPlanThreads, 0, st, stt, rec, E, static_cast<const int32_t *>(seg_off),
+                   static_cast<const int32_t *>(live), xd_rows, p->cfg.page_tokens, p->cfg.max_pages_per_record,
+                   p->cfg.num_pages, p->cfg.spill_pages);
+        AP_CHECK_LAUNCH("dispatch_stash plan launch");
     } else {
         ap::launch(ap::k_scan_plan, 1, ap::kPlanThreads, 0, st, static_cast<int32_t *>(scratch), dispatch_blocks(T),
                    E, capacity, padded, counts, live, seg_off, stt, rec, xd_rows, p->cfg.page_tokens,
@@ -1772,12 +1851,14 @@ extern "C" ap_status ap_dispatch_stash_ranked(ap_pool *p, int32_t slot, const vo
                                               int32_t padded, int32_t out_dtype, void *xd, float *xd_scale,
                                               int64_t xd_rows, int32_t *counts, int32_t *live, int32_t *seg_off,
                                               int32_t *dest, int32_t *src_tok, void *scratch, int64_t scratch_bytes,
-                                              uint32_t *d_status, uint64_t *record_id, void *stream)
+                                              uint32_t *d_status, uint64_t *record_id, int32_t scanned,
+                                              void *stream)
 {
     AP_NVTX_RANGE("ap_dispatch_stash_ranked");
+    if (scanned != 0 && scanned != 1) return ap::fail(AP_EINVAL, "dispatch_stash_ranked: scanned must be 0 or 1");
     return dispatch_stash_impl(p, slot, nullptr, nullptr, x, T, H, const_cast<int32_t *>(idx), k, E, capacity,
                                padded, out_dtype, xd, xd_scale, xd_rows, counts, live, seg_off, dest, src_tok,
-                               scratch, scratch_bytes, d_status, record_id, stream, true);
+                               scratch, scratch_bytes, d_status, record_id, stream, true, scanned != 0);
 }
 
 extern "C" ap_status ap_stash_pop(ap_pool *p, int32_t slot, int32_t nplanes, void *const *dst_planes,

@@ -816,14 +816,19 @@ def sm_partition_report(step, device, sizes=(8, 16, 24, 32, 48), reps=9, gemm_re
 def rank_beside(ap, wl, d, side, prefetch=True):
     """Route and count/rank one source on the second stream, for its ranked
     dispatch + push on the paging stream.  A record of at most 64 count/rank
-    blocks takes the one routing + count/rank launch; its 1024-thread blocks
+    blocks takes the one routing + count/rank launch and the expert scan
+    there too (the copy then plans only the pages); their 1024-thread blocks
     hold whole SMs, so beside a copy of a larger record they would start only
     in its tail, and those take routing and count/rank as two small-block
     launches.  prefetch: the count/rank prefetches the rows into L2."""
     x = d["x"] if prefetch else None
     if (wl.T + 63) // 64 <= 64:
-        ap.count_rank(wl.E, logits=d["logits"], k=wl.k, x=x, stream=side,
-                      out={"idx": d["idx"], "w": d["w"], "dest": d["disp"]["dest"], "scratch": d["disp"]["scratch"]})
+        r = ap.count_rank(wl.E, logits=d["logits"], k=wl.k, x=x, stream=side, scan=True, capacity=wl.capacity,
+                          padded=wl.padded,
+                          out={"idx": d["idx"], "w": d["w"], "dest": d["disp"]["dest"], "scratch": d["disp"]["scratch"],
+                               "counts": d["disp"]["counts"], "live": d["disp"]["live"],
+                               "seg_off": d["disp"]["seg_off"]})
+        d["disp"]["scanned"] = r["scanned"]
     else:
         ap.route_topk(d["logits"], wl.k, d["idx"], d["w"], stream=side)
         ap.count_rank(wl.E, idx=d["idx"], x=x, stream=side,

@@ -427,19 +427,30 @@ ap_status ap_route_dispatch_stash(ap_pool *pool, int32_t slot, const float *logi
  *            block of 64 tokens, -1 for an id outside [0, E)
  *   scratch  ap_dispatch_scratch_bytes(T, k, E) bytes (device, written): the
  *            blocks' expert histograms
+ *   counts, live, seg_off  [E] int32 (device, written) or all three NULL:
+ *            with them the call also runs the dispatch's expert scan for
+ *            capacity and padded (as ap_dispatch_permute), and the scratch
+ *            then holds each block's base rank per expert instead of its
+ *            histogram; ap_dispatch_stash_ranked(..., scanned = 1) then plans
+ *            only the record's pages
  *   d_status device uint32 word (may be NULL): AP_FLAG_BAD_INDEX for an id
  *            outside [0, E)
  * Limits and errors as ap_dispatch_permute (plus AP_EINVAL for k > E with
- * logits, NULL w with logits and T > 0, or row_bytes < 0). */
+ * logits, NULL w with logits and T > 0, row_bytes < 0, or only some of
+ * counts, live and seg_off). */
 ap_status ap_count_rank(const float *logits, float *w, int32_t *idx, int64_t T, int32_t k, int32_t E,
                         const void *x, int64_t row_bytes, int32_t *dest, void *scratch, int64_t scratch_bytes,
+                        int32_t capacity, int32_t padded, int32_t *counts, int32_t *live, int32_t *seg_off,
                         uint32_t *d_status, void *stream);
 
 /* ap_dispatch_stash without its count/rank launch: dest and scratch must
  * hold the results of ap_count_rank for the same idx, T, k and E, ordered
  * before this call (an event, or the same stream); idx, dest and scratch
- * must not change between the two calls.  Same arguments, results and
- * errors as ap_dispatch_stash.  Ranks or histograms that do not match idx
+ * must not change between the two calls.  scanned = 1: that ap_count_rank
+ * call also ran the expert scan into counts, live and seg_off (passed here
+ * too, with the same capacity and padded), so the call does not scan again
+ * (0 or 1, else AP_EINVAL).  Same arguments, results and errors as
+ * ap_dispatch_stash.  Ranks or histograms that do not match idx
  * leave the dispatch rows, the record and the pool's contents unspecified,
  * but no write leaves the dispatch buffer, the pages or the metadata: a
  * pair whose row would fall outside its buffer or page is dropped (dest -1)
@@ -449,7 +460,7 @@ ap_status ap_dispatch_stash_ranked(ap_pool *pool, int32_t slot, const void *x, i
                                    int32_t out_dtype, void *xd, float *xd_scale, int64_t xd_rows,
                                    int32_t *counts, int32_t *live, int32_t *seg_off, int32_t *dest,
                                    int32_t *src_tok, void *scratch, int64_t scratch_bytes, uint32_t *d_status,
-                                   uint64_t *record_id, void *stream);
+                                   uint64_t *record_id, int32_t scanned, void *stream);
 
 /* Pop the oldest record of `slot` into dst_planes (host array of nplanes
  * device pointers, each [dst_rows, row_bytes of the push]).  A page whose

@@ -133,8 +133,10 @@ def test_count_rank_rejects_bad_arguments(lib):
     n = ctypes.c_int64()
     assert lib.ap_dispatch_scratch_bytes(1000, 8, 128, ctypes.byref(n)) == 0
 
-    def call(logits=None, w=None, idx=p, T=1000, k=8, E=128, x=None, rb=0, dest=p, scratch=p, sb=n.value):
-        return lib.ap_count_rank(logits, w, idx, T, k, E, x, rb, dest, scratch, sb, None, None)
+    def call(logits=None, w=None, idx=p, T=1000, k=8, E=128, x=None, rb=0, dest=p, scratch=p, sb=n.value, cap=0,
+             padded=0, counts=None, live=None, seg=None):
+        return lib.ap_count_rank(logits, w, idx, T, k, E, x, rb, dest, scratch, sb, cap, padded, counts, live, seg,
+                                 None, None)
     n0 = lib.ap_launch_count()
     assert call(k=0) == -1
     assert call(k=33) == -1
@@ -144,10 +146,12 @@ def test_count_rank_rejects_bad_arguments(lib):
     assert call(sb=n.value - 256) == -1          # work space too small
     assert call(dest=None) == -1
     assert call(rb=-1) == -1
+    assert call(counts=p, live=p) == -1                # the scan needs all three outputs
+    assert call(counts=p, live=p, seg=p, padded=1) == -1  # padded needs a capacity
     assert b"count_rank" in lib.ap_last_error()
     assert lib.ap_launch_count() == n0
     assert lib.ap_dispatch_stash_ranked(None, 0, p, 10, 64, p, 2, 8, 0, 0, 0, p, None, 20, p, p, p, p, None, p,
-                                        n.value, None, None, None) == -1
+                                        n.value, None, None, 0, None) == -1
 
 
 def test_combine_rejects_bad_arguments(lib):

@@ -1,6 +1,6 @@
 """GPU parity of the split fused dispatch + push: count/rank (ap_count_rank,
-optionally routing first) on a second stream, then ap_dispatch_stash_ranked
-on the paging stream after an event.
+optionally routing first and optionally with the expert scan) on a second
+stream, then ap_dispatch_stash_ranked on the paging stream after an event.
 
 Same results as the oracle's dispatch followed by its push (torchtitan pull
 5541, "AI-Generated Details": the stash committed by the producer of the
@@ -22,6 +22,7 @@ ap = pytest.importorskip("activation_paging_gb300")
 FILL = 0xA5
 
 
+@pytest.mark.parametrize("scan", [False, True])
 @pytest.mark.parametrize("T,H,E,k,C,padded,P,N,SP,fp8,route", [
     (4096, 256, 64, 6, 0, False, 32, 900, 0, False, False),     # planned in the copy kernel, one-column reads
     (8192, 256, 128, 8, 0, False, 64, 1200, 0, False, True),    # the headline's counts (128 x 128), routed
@@ -30,7 +31,7 @@ FILL = 0xA5
     (4096, 2056, 64, 6, 0, False, 128, 120, 0, True, False),    # E4M3, rows 8 bytes off; the pool overflows
     (512, 128, 8, 2, 0, False, 16, 10, 4, False, True),         # spill exhausted: lost pages
 ])
-def test_ranked_dispatch_stash_matches_oracle(T, H, E, k, C, padded, P, N, SP, fp8, route):
+def test_ranked_dispatch_stash_matches_oracle(T, H, E, k, C, padded, P, N, SP, fp8, route, scan):
     rb = (H, 4) if fp8 else (2 * H,)
     page_bytes = ap.page_bytes_for(P, rb)
     g = ap.Pool(P, page_bytes, N, 1, 4, E, N + SP + E, SP, fill=FILL)
@@ -53,13 +54,14 @@ def test_ranked_dispatch_stash_matches_oracle(T, H, E, k, C, padded, P, N, SP, f
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):  # count/rank beside the paging stream
             if route:
-                r = ap.count_rank(E, logits=to_dev(logits), k=k, x=xg, stream=side)
+                r = ap.count_rank(E, logits=to_dev(logits), k=k, x=xg, stream=side, scan=scan, capacity=C,
+                                  padded=padded)
             else:
-                r = ap.count_rank(E, idx=to_dev(idx_o), x=xg, stream=side)
+                r = ap.count_rank(E, idx=to_dev(idx_o), x=xg, stream=side, scan=scan, capacity=C, padded=padded)
             ranked = torch.cuda.Event()
             ranked.record(side)
         g.stream.wait_event(ranked)
-        out.update(dest=r["dest"], scratch=r["scratch"])
+        out.update({key: r[key] for key in ("dest", "scratch", "counts", "live", "seg_off", "scanned") if key in r})
         with torch.cuda.stream(g.stream):
             d = g.dispatch_stash(0, xg, r["idx"], E, C, padded, fp8=fp8, out=out, ranked=True)
         torch.cuda.synchronize()
