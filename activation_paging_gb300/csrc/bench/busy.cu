@@ -1,5 +1,6 @@
-// Synthetic compute for the reload-overlap measurement of bench.py.  Not part
-// of the library (libap.so) or its ABI: it is built into libap_bench.so.
+// Synthetic compute for the reload-overlap measurement of bench.py, and the
+// host NUMA query its host-side setup uses.  Not part of the library
+// (libap.so) or its ABI: it is built into libap_bench.so.
 //
 // Each block of k_busy holds one whole SM: 1024 threads and the largest
 // dynamic shared-memory allocation a block may take, so no other block (every
@@ -47,4 +48,17 @@ extern "C" int apb_busy_sms(int nblocks, long long iters, float *sink, void *str
     if (e != cudaSuccess) return (int)e;
     k_busy<<<nblocks, 1024, smem, (cudaStream_t)stream>>>(iters, sink);
     return (int)cudaGetLastError();
+}
+
+// The host NUMA node nearest `device` (cudaDevAttrHostNumaId), or -1 when the
+// system reports none or the query fails.  The bench runs its host threads
+// there, so the pinned buffers it allocates sit next to the GPU.
+extern "C" int apb_host_numa_id(int device)
+{
+    int v = -1;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrHostNumaId, device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    return v;
 }

@@ -1240,6 +1240,36 @@ def measured_peaks():
         return None
 
 
+def bind_host_numa(device_index):
+    """Run this process's host threads on the CPUs of the host NUMA node
+    nearest the GPU (cudaDevAttrHostNumaId, through the bench-only
+    libap_bench.so), so the pinned buffers it allocates afterwards sit next to
+    the GPU rather than across the CPU-to-CPU link.  Returns what was done."""
+    import ctypes
+    from activation_paging_gb300 import build as cuda_build
+    try:
+        lib = ctypes.CDLL(cuda_build.BENCH_LIB)
+        lib.apb_host_numa_id.restype = ctypes.c_int
+        lib.apb_host_numa_id.argtypes = [ctypes.c_int]
+        node = lib.apb_host_numa_id(device_index)
+        if node < 0:
+            return {"node": None, "note": "the device reports no host NUMA node"}
+        cpus = set()
+        for part in open(f"/sys/devices/system/node/node{node}/cpulist").read().strip().split(","):
+            if part:
+                a, _, b = part.partition("-")
+                cpus.update(range(int(a), int(b or a) + 1))
+        allowed = os.sched_getaffinity(0)
+        use = cpus & allowed
+        if not use:
+            return {"node": node, "note": "none of the node's CPUs is available to this process; left unbound"}
+        if use != allowed:
+            os.sched_setaffinity(0, use)
+        return {"node": node, "cpus": len(use)}
+    except (OSError, ValueError) as e:
+        return {"node": None, "note": f"not bound: {e}"}
+
+
 def native(args):
     import torch
     from activation_paging_gb300 import inputs, build as cuda_build
@@ -1251,6 +1281,7 @@ def native(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     cuda_build.build()
+    host_numa = bind_host_numa(local)  # before any pinned host buffer is allocated
     wl = inputs.WORKLOADS[WORKLOAD]
     step = Step(wl, device, seed_base=1000 * rank)
     ap = step.ap
@@ -1409,7 +1440,8 @@ def native(args):
                "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps, "ms_per_step": round(e_el * 1e3 / args.e2e_steps, 4),
                "note": "inputs copied from pinned host memory and output copied back inside the timed region, "
-                       "pipelined per chunk on separate copy streams"}
+                       "pipelined per chunk on separate copy streams",
+               "host_numa": host_numa}
 
     launched_as = ("eager" if graph is None else
                    "CUDA graph of one step, replayed" + ("" if (args.serial or not fused_main)
