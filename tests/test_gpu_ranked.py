@@ -29,6 +29,8 @@ FILL = 0xA5
     (6000, 64, 48, 4, 560, True, 16, 1800, 0, False, False),    # padded, four-column reads, ragged row groups
     (17000, 64, 64, 4, 0, False, 64, 900, 200, False, True),    # scan + plan kernel (272 x 64 counts); spill
     (4096, 2056, 64, 6, 0, False, 128, 120, 0, True, False),    # E4M3, rows 8 bytes off; the pool overflows
+    (4096, 2048, 64, 6, 0, False, 128, 260, 0, True, True),     # E4M3, aligned rows, routed; every page kept
+    (3000, 1024, 32, 4, 300, True, 64, 200, 16, True, False),   # E4M3 padded with drops; spill
     (512, 128, 8, 2, 0, False, 16, 10, 4, False, True),         # spill exhausted: lost pages
 ])
 def test_ranked_dispatch_stash_matches_oracle(T, H, E, k, C, padded, P, N, SP, fp8, route, scan):
