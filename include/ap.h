@@ -416,7 +416,11 @@ ap_status ap_route_dispatch_stash(ap_pool *pool, int32_t slot, const float *logi
  * (and, with logits != NULL, of ap_route_dispatch_stash, routing into idx
  * and w first), for callers that overlap it with other work and then call
  * ap_dispatch_stash_ranked on the paging stream.  The ranking of pairs is the
- * one ap_dispatch_permute documents (t-then-j order within each expert).
+ * one ap_dispatch_permute documents (t-then-j order within each expert; the
+ * capacity-shaped, expert-major dispatch of Megatron-LM pull 7342, "Summary",
+ * and torchtitan pull 5541, "AI-Generated Details").  Overlapping it with the
+ * previous pool call is the early-launch, late-wait scheduling of torchtitan
+ * pull 5542 (body) applied to the dispatch's metadata work.
  *
  *   logits   [T, E] f32 (device, read) or NULL: idx is then an input
  *   w        [T, k] f32 (device, written when logits != NULL, else unused)
@@ -443,7 +447,9 @@ ap_status ap_count_rank(const float *logits, float *w, int32_t *idx, int64_t T, 
                         int32_t capacity, int32_t padded, int32_t *counts, int32_t *live, int32_t *seg_off,
                         uint32_t *d_status, void *stream);
 
-/* ap_dispatch_stash without its count/rank launch: dest and scratch must
+/* ap_dispatch_stash without its count/rank launch (the stash committed by
+ * the producer of the rows: torchtitan pull 5541, "AI-Generated Details",
+ * first paragraph): dest and scratch must
  * hold the results of ap_count_rank for the same idx, T, k and E, ordered
  * before this call (an event, or the same stream); idx, dest and scratch
  * must not change between the two calls.  scanned = 1: that ap_count_rank
